@@ -1,0 +1,25 @@
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
+    config.addinivalue_line("markers", "slow: full-size workloads")
+
+
+def pytest_collection_modifyitems(config, items):
+    # GPU tests never silently pass on a machine without a GPU: they are skipped
+    # only when no CUDA device exists at all, and fail loudly otherwise.
+    import torch
+    if torch.cuda.is_available():
+        return
+    skip = pytest.mark.skip(reason="no CUDA device in this machine")
+    for item in items:
+        if "gpu" in item.keywords:
+            item.add_marker(skip)

@@ -1,0 +1,255 @@
+"""Pins of the CPU oracle to facts fixed outside of it.
+
+Each test ties the oracle to something it could not get right by accident:
+hand-derived closed forms (tests/golden), a high-precision brute force written
+in a different form, invariants of the softmax, exhaustive subset search for
+the top-k, a textbook per-token top-k for c = 1, and the structure of
+Algorithm 2.  Citations: "ChunkKV ... (NeurIPS'25) notes" §4.1 Algorithm 1,
+§4.2 Algorithm 2; "Kara" §2 Eq. (1).
+"""
+import heapq
+import itertools
+import json
+import math
+import os
+
+import mpmath
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synthetic import configs, generator as gen
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "closed_forms.json")
+
+
+def _ev(expr: str) -> float:
+    return float(eval(expr, {"__builtins__": {}}, {"sqrt": math.sqrt, "log": math.log,
+                                                    "exp": math.exp}))
+
+
+def _load_cases():
+    with open(GOLDEN) as f:
+        return json.load(f)["cases"]
+
+
+@pytest.mark.parametrize("case", _load_cases(), ids=lambda c: c["name"])
+def test_golden_closed_forms(case):
+    q = np.array([[[_ev(x) for x in row] for row in hq] for hq in case["q_win"]])   # [w,Hq,d]
+    k = np.array([[[_ev(x) for x in row] for row in tok] for tok in case["k"]])      # [T,Hkv,d]
+    G = case["Hq"] // case["Hkv"]
+    for h in range(case["Hkv"]):
+        A, sel, idx = oracle.chunkkv_head(oracle.group_window_rows(q, h, G), k[:, h, :],
+                                          case["c"], case["w"], case["L_max"])
+        want = [_ev(x) for x in case["expect_scores"][h]]
+        assert np.allclose(A, want, rtol=1e-13, atol=1e-14), (A, want)
+        assert idx.tolist() == case["expect_indices"][h]
+
+
+def _brute_scores(rows, keys, c):
+    """Chunk scores at 50 digits: p_qj = 1 / sum_j' exp(s_qj' - s_qj), tokens mapped to chunks."""
+    mpmath.mp.dps = 50
+    R, d = rows.shape
+    T = keys.shape[0]
+    inv = 1 / mpmath.sqrt(d)
+    bins = {}
+    for q in range(R):
+        s = [mpmath.fsum(mpmath.mpf(float(rows[q, e])) * mpmath.mpf(float(keys[j, e]))
+                         for e in range(d)) * inv for j in range(T)]
+        for j in range(T):
+            pj = 1 / mpmath.fsum(mpmath.e ** (s[i] - s[j]) for i in range(T))
+            bins[j // c] = bins.get(j // c, mpmath.mpf(0)) + pj
+    return [float(bins[i]) for i in range(len(bins))]
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_brute_force_high_precision(seed):
+    rng = np.random.default_rng(seed)
+    T = int(rng.integers(1, 13))
+    d = int(rng.integers(1, 5))
+    R = int(rng.integers(1, 5))
+    c = int(rng.integers(1, 5))
+    rows = rng.normal(size=(R, d)) * 2
+    keys = rng.normal(size=(T, d)) * 2
+    A = oracle.chunk_scores(oracle.key_scores(rows, keys), c)
+    assert np.allclose(A, _brute_scores(rows, keys, c), rtol=1e-12, atol=1e-14)
+
+
+def _rand_case(seed, T=97, d=16, w=5, G=3, Hkv=2, c=7):
+    rng = np.random.default_rng(100 + seed)
+    q = rng.normal(size=(w, G * Hkv, d))
+    k = rng.normal(size=(T, Hkv, d)) * 1.5
+    return q, k, G, c
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_scores_sum_to_window_times_group(seed):
+    # every softmax row sums to one, so the chunk scores of a KV head add up to w * G
+    q, k, G, c = _rand_case(seed)
+    w = q.shape[0]
+    for h in range(k.shape[1]):
+        A = oracle.chunk_scores(oracle.key_scores(oracle.group_window_rows(q, h, G), k[:, h]), c)
+        assert abs(A.sum() - w * G) < 1e-11
+
+
+def test_zero_keys_give_uniform_mass():
+    # K = 0: every logit is 0, p = 1/T, so A_i = w G |chunk_i| / T (last chunk short)
+    T, c, w, G, d = 53, 10, 4, 2, 8
+    q = np.random.default_rng(1).normal(size=(w, G, d))
+    A = oracle.chunk_scores(oracle.key_scores(oracle.group_window_rows(q, 0, G), np.zeros((T, d))), c)
+    sizes = [10, 10, 10, 10, 10, 3]
+    assert np.allclose(A, [w * G * s / T for s in sizes], rtol=1e-14)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_shift_of_all_keys_leaves_scores_unchanged(seed):
+    # adding one vector u to every key adds <q,u>/sqrt(d) to a whole softmax row
+    q, k, G, c = _rand_case(seed)
+    u = np.random.default_rng(seed).normal(size=k.shape[2])
+    rows = oracle.group_window_rows(q, 1, G)
+    a0 = oracle.key_scores(rows, k[:, 1])
+    a1 = oracle.key_scores(rows, k[:, 1] + u)
+    assert np.allclose(a0, a1, rtol=1e-10, atol=1e-13)
+    # ...while scaling the keys does change them (the normalisation is per query row)
+    assert not np.allclose(a0, oracle.key_scores(rows, 2 * k[:, 1]), rtol=1e-3)
+
+
+def test_single_query_is_textbook_softmax():
+    # G = 1, w = 1, c = 1: the chunk scores are one softmax row of q.k / sqrt(d)
+    rng = np.random.default_rng(5)
+    q = rng.normal(size=(1, 1, 8))
+    k = rng.normal(size=(20, 8))
+    s = torch.tensor(k @ q[0, 0] / math.sqrt(8))
+    want = torch.softmax(s, dim=0).numpy()
+    A = oracle.chunk_scores(oracle.key_scores(oracle.group_window_rows(q, 0, 1), k), 1)
+    assert np.allclose(A, want, rtol=1e-12)
+
+
+def test_top_chunks_brute_force_subsets():
+    rng = np.random.default_rng(7)
+    for trial in range(60):
+        C = int(rng.integers(1, 11))
+        k = int(rng.integers(0, C + 1))
+        A = rng.integers(0, 4, size=C).astype(np.float64)   # integers: exact sums, many ties
+        best, best_set = None, None
+        for comb in itertools.combinations(range(C), k):     # lexicographic order
+            s = sum(A[i] for i in comb)
+            if best is None or s > best:
+                best, best_set = s, list(comb)
+        assert oracle.top_chunks(A, k) == best_set, (A, k)
+
+
+def test_all_equal_scores_keep_lowest_chunks():
+    assert oracle.top_chunks(np.full(9, 0.25), 4) == [0, 1, 2, 3]
+
+
+def test_chunk_size_one_is_per_token_topk():
+    # c = 1: selection is a plain top-L_max over per-token mass (ties to the lower token)
+    q, k, G, _ = _rand_case(3, T=64)
+    rows = oracle.group_window_rows(q, 0, G)
+    a = oracle.key_scores(rows, k[:, 0])
+    L_max, w = 11, 5
+    A, sel, idx = oracle.chunkkv_head(rows, k[:, 0], 1, w, L_max)
+    want = sorted(heapq.nlargest(L_max, range(64), key=lambda j: (a[j], -j)))
+    assert sel == want
+    assert idx.tolist() == sorted(set(want) | set(range(64 - w, 64)))
+
+
+@pytest.mark.parametrize("T,c,w,L_max", [(97, 7, 5, 30), (97, 7, 0, 30), (20, 7, 30, 7),
+                                         (64, 8, 8, 16), (10, 3, 2, 0), (1, 4, 1, 4)])
+def test_kept_indices_characterised(T, c, w, L_max):
+    q, k, G, _ = _rand_case(1, T=T)
+    rows = oracle.group_window_rows(q, 0, G)
+    A, sel, idx = oracle.chunkkv_head(rows, k[:, 0], c, w, L_max)
+    C = -(-T // c)
+    assert len(sel) == min(L_max // c, C) and len(set(sel)) == len(sel)
+    idx = idx.tolist()
+    assert all(b > a for a, b in zip(idx, idx[1:])) and all(0 <= j < T for j in idx)
+    recent = set(range(max(0, T - w), T))
+    for j in range(T):       # j kept  <=>  its chunk was selected or it is recent
+        assert (j in idx) == ((j // c) in sel or j in recent)
+
+
+def test_budget_at_least_prompt_keeps_everything():
+    q, k, G, c = _rand_case(2, T=45)
+    rows = oracle.group_window_rows(q, 0, G)
+    A, sel, idx = oracle.chunkkv_head(rows, k[:, 0], c, 3, 45)
+    assert idx.tolist() == list(range(45))
+    assert np.array_equal(oracle.gather(k[:, 0], idx), k[:, 0])
+
+
+def test_planted_chunk_is_selected_tiny():
+    wl = configs.tiny()
+    q, k, v, spans = gen.make_all_layers(wl, "cpu")
+    (s, e), = spans[0][0]
+    res = oracle.compress_layers([q[0].numpy()], [k[0].numpy()], [v[0].numpy()], wl.cu_seqlens,
+                                 wl.Hq, wl.Hkv, wl.w, wl.c, wl.L_max, wl.n_reuse)
+    for h in range(wl.Hkv):
+        assert s // wl.c in res["chunks"][0][0][h]
+        A = res["scores"][0][0][h]
+        assert int(np.argmax(A)) == s // wl.c
+
+
+def test_needle_spans_are_found_llama_layer():
+    # every needle span at least one chunk long contains a selected chunk, in every KV head
+    wl = configs.llama_layer()
+    q, k, v, spans = gen.make_all_layers(wl, "cpu")
+    qf = q[0].float().numpy()
+    kf = k[0].float().numpy()
+    G = wl.G
+    for h in range(wl.Hkv):
+        A, sel, idx = oracle.chunkkv_head(oracle.group_window_rows(qf[0], h, G), kf[:, h],
+                                          wl.c, wl.w, wl.L_max)
+        sel = set(sel)
+        for (s, e) in spans[0][0]:
+            full = [i for i in range(-(-s // wl.c), e // wl.c) if (i + 1) * wl.c <= e]
+            if full:
+                assert sel & set(full), (h, s, e)
+
+
+def _layers(n_layers, T=40, Hkv=2, G=2, w=4, d=8, seed=0):
+    rng = np.random.default_rng(seed)
+    qs = [rng.normal(size=(1, w, Hkv * G, d)) for _ in range(n_layers)]
+    ks = [rng.normal(size=(T, Hkv, d)) for _ in range(n_layers)]
+    vs = [rng.normal(size=(T, Hkv, d)) for _ in range(n_layers)]
+    return qs, ks, vs
+
+
+def test_reuse_layers_share_indices_and_gather_their_own_kv():
+    qs, ks, vs = _layers(5)
+    r = oracle.compress_layers(qs, ks, vs, [0, 40], 4, 2, 4, 5, 15, n_reuse=2)
+    assert sorted(r["indices"]) == [0, 1, 2]                  # layers 0, 2, 4 score
+    for layer in range(5):
+        g = layer // 2
+        for h in range(2):
+            idx = r["indices"][g][0][h]
+            assert np.array_equal(r["k_out"][layer][0][h], ks[layer][idx, h])
+            assert np.array_equal(r["v_out"][layer][0][h], vs[layer][idx, h])
+
+
+def test_reuse_depth_changes_only_the_reusing_layers():
+    qs, ks, vs = _layers(4, seed=3)
+    r1 = oracle.compress_layers(qs, ks, vs, [0, 40], 4, 2, 4, 5, 15, n_reuse=1)
+    r2 = oracle.compress_layers(qs, ks, vs, [0, 40], 4, 2, 4, 5, 15, n_reuse=2)
+    for layer in (0, 2):                                       # scoring layers agree
+        for h in range(2):
+            assert np.array_equal(r1["indices"][layer][0][h], r2["indices"][layer // 2][0][h])
+    # with N_reuse = 1 layer 1 selects from its own scores; they differ from layer 0 here
+    assert any(not np.array_equal(r1["indices"][1][0][h], r1["indices"][0][0][h]) for h in range(2))
+
+
+def test_ragged_batch_is_per_sequence():
+    rng = np.random.default_rng(11)
+    T = [30, 0, 17]
+    cu = [0, 30, 30, 47]
+    q = rng.normal(size=(3, 4, 4, 8))
+    k = rng.normal(size=(47, 2, 8))
+    v = rng.normal(size=(47, 2, 8))
+    r = oracle.compress_layers([q], [k], [v], cu, 4, 2, 4, 5, 10, 1)
+    for b in range(3):
+        for h in range(2):
+            A, sel, idx = oracle.chunkkv_head(oracle.group_window_rows(q[b], h, 2),
+                                              k[cu[b]:cu[b + 1], h], 5, 4, 10)
+            assert np.array_equal(r["indices"][0][b][h], idx)
+    assert r["indices"][0][1][0].size == 0
