@@ -1,0 +1,211 @@
+// Window scoring, portable SIMT path, and the per-unit finalisation shared by
+// every scoring path.
+//
+// ChunkKV §4.1 Algorithm 1 steps 1-3 with the probabilities of Kara §2 Eq. (1):
+//   A[b][h][i] = sum_{rows r of head h} sum_{j in chunk i} exp(s_rj - lse_r),
+//   s_rj = <Q_w row r, K_j> / sqrt(d),  lse_r = log sum_{j < T_b} exp(s_rj).
+//
+// The keys of a (sequence, head) are split into units of `cpu` whole chunks.
+// A scoring kernel writes, per unit and window row r,
+//   R_r   a reference exponent (base 2: logits times log2(e)/sqrt(d)),
+//   l_r   = sum_{j in unit} 2^(t_rj - R_r),
+//   bin[i][r] = sum_{j in chunk i} 2^(t_rj - R_r)   for the unit's chunks,
+// all in fp32.  finalize_kernel then forms lse_r over every unit of the head,
+// the weights 2^(R_r - lse_r) and A_i = sum_r bin[i][r] * weight_r.  This
+// single pass over K needs no second read of the keys and no grid barrier.
+#include "common.cuh"
+
+namespace chunkkv {
+
+// ------------------------------------------------------------------ SIMT scoring
+// One CTA per unit, one thread per window row (rows in blocks of kRows); K is
+// staged through shared memory in tiles of kKeys keys.  The unit's row maximum
+// is found in a first sweep so that the bins use the exact unit maximum as
+// reference (the portable path trades a second dot product for simplicity).
+constexpr int kSimtRows = 128;
+constexpr int kSimtKeys = 32;
+
+template <typename E>
+__global__ void __launch_bounds__(kSimtRows)
+score_simt_kernel(const E* __restrict__ q, const E* __restrict__ k, ScoreGeom g,
+                  const __grid_constant__ SeqTable st, float* __restrict__ rl,
+                  float* __restrict__ bins) {
+  extern __shared__ float smem[];
+  const int ld = g.d + 1;                       // padded rows: conflict-free per-thread rows
+  float* qs = smem;                             // [kSimtRows][ld]
+  float* ks = smem + kSimtRows * ld;            // [kSimtKeys][ld]
+
+  int b, h, u;
+  const int gu = blockIdx.x;
+  decode_unit(st, g.Hkv, gu, b, h, u);
+  const int T = st.cu[b + 1] - st.cu[b];
+  const int k0 = u * g.ku;
+  const int nk = min(g.ku, T - k0);
+  const E* kbase = k + (int64_t)(st.cu[b] + k0) * g.kv_stride_t + (int64_t)h * g.kv_stride_h;
+  const int tid = threadIdx.x;
+
+  for (int rb = 0; rb < g.wG; rb += kSimtRows) {
+    __syncthreads();
+    for (int i = tid; i < kSimtRows * g.d; i += blockDim.x) {
+      int row = i / g.d, e = i % g.d, r = rb + row;
+      float val = 0.f;
+      if (r < g.wG) {
+        int gm = r / g.w, qi = r % g.w;           // row r = (group member gm, window row qi)
+        val = to_float(q[(int64_t)b * g.q_stride_b + (int64_t)qi * g.q_stride_w +
+                         (int64_t)(h * g.G + gm) * g.q_stride_h + e]);
+      }
+      qs[row * ld + e] = val;
+    }
+    const int r = rb + tid;
+    const bool active = r < g.wG;
+    const float* qrow = qs + tid * ld;
+
+    // sweep 1: row maximum of the base-2 exponents over the unit
+    float m = -INFINITY;
+    for (int kt = 0; kt < nk; kt += kSimtKeys) {
+      const int nt = min(kSimtKeys, nk - kt);
+      __syncthreads();
+      for (int i = tid; i < nt * g.d; i += blockDim.x) {
+        int j = i / g.d, e = i % g.d;
+        ks[j * ld + e] = to_float(kbase[(int64_t)(kt + j) * g.kv_stride_t + e]);
+      }
+      __syncthreads();
+      if (active) {
+        for (int j = 0; j < nt; ++j) {
+          float dot = 0.f;
+          const float* kr = ks + j * ld;
+          for (int e = 0; e < g.d; ++e) dot = fmaf(qrow[e], kr[e], dot);
+          m = fmaxf(m, dot * g.alpha);
+        }
+      }
+    }
+    // sweep 2: exponentials relative to the unit maximum, summed per chunk
+    float acc = 0.f, l = 0.f;
+    int cur = 0;
+    float* brow = bins + (int64_t)gu * g.cpu * g.wG + r;
+    for (int kt = 0; kt < nk; kt += kSimtKeys) {
+      const int nt = min(kSimtKeys, nk - kt);
+      __syncthreads();
+      for (int i = tid; i < nt * g.d; i += blockDim.x) {
+        int j = i / g.d, e = i % g.d;
+        ks[j * ld + e] = to_float(kbase[(int64_t)(kt + j) * g.kv_stride_t + e]);
+      }
+      __syncthreads();
+      if (active) {
+        for (int j = 0; j < nt; ++j) {
+          float dot = 0.f;
+          const float* kr = ks + j * ld;
+          for (int e = 0; e < g.d; ++e) dot = fmaf(qrow[e], kr[e], dot);
+          const int ch = (kt + j) / g.c;
+          if (ch != cur) {
+            brow[(int64_t)cur * g.wG] = acc;
+            acc = 0.f;
+            cur = ch;
+          }
+          const float p = exp2f(dot * g.alpha - m);
+          acc += p;
+          l += p;
+        }
+      }
+    }
+    if (active) {
+      brow[(int64_t)cur * g.wG] = acc;
+      rl[((int64_t)gu * 2 + 0) * g.wG + r] = m;
+      rl[((int64_t)gu * 2 + 1) * g.wG + r] = l;
+    }
+  }
+}
+
+cudaError_t launch_score_simt(const Plan& pl, const ScoreGeom& g, const SeqTable& st, const void* q,
+                              const void* k, float* rl, float* bins, cudaStream_t s) {
+  if (g.n_units == 0 || g.wG == 0) return cudaSuccess;
+  const size_t smem = (size_t)(kSimtRows + kSimtKeys) * (g.d + 1) * sizeof(float);
+  cudaError_t e;
+  if (pl.elt == 2) {
+    e = cudaFuncSetAttribute(score_simt_kernel<__nv_bfloat16>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    score_simt_kernel<__nv_bfloat16><<<g.n_units, kSimtRows, smem, s>>>(
+        (const __nv_bfloat16*)q, (const __nv_bfloat16*)k, g, st, rl, bins);
+  } else {
+    e = cudaFuncSetAttribute(score_simt_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+    if (e != cudaSuccess) return e;
+    score_simt_kernel<float><<<g.n_units, kSimtRows, smem, s>>>((const float*)q, (const float*)k, g,
+                                                               st, rl, bins);
+  }
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ finalisation
+// One CTA per unit.  lse_r is formed from the (R, l) pairs of every unit of the
+// same (sequence, head); the unit's bins are then weighted by 2^(R_r - lse_r)
+// and summed over rows, one warp per chunk (coalesced over rows).
+constexpr int kFinThreads = 256;
+
+__global__ void __launch_bounds__(kFinThreads)
+finalize_kernel(ScoreGeom g, const __grid_constant__ SeqTable st, const float* __restrict__ rl,
+                const float* __restrict__ bins, float* __restrict__ scores) {
+  extern __shared__ float wts[];                // [wG]
+  int b, h, u;
+  const int gu = blockIdx.x;
+  decode_unit(st, g.Hkv, gu, b, h, u);
+  const int T = st.cu[b + 1] - st.cu[b];
+  const int C = (T + g.c - 1) / g.c;
+  const int U = st.uoff[b + 1] - st.uoff[b];
+  const int64_t stride_u = (int64_t)g.Hkv * 2 * g.wG;          // between units of one head
+  const float* rl_head = rl + ((int64_t)st.uoff[b] * g.Hkv + h) * 2 * g.wG;
+
+  for (int r = threadIdx.x; r < g.wG; r += blockDim.x) {
+    float M = -INFINITY;
+    for (int v = 0; v < U; ++v) M = fmaxf(M, rl_head[v * stride_u + r]);
+    float S = 0.f;
+    for (int v = 0; v < U; ++v) S += rl_head[v * stride_u + g.wG + r] * exp2f(rl_head[v * stride_u + r] - M);
+    const float lse = M + log2f(S);
+    wts[r] = exp2f(rl[(int64_t)gu * 2 * g.wG + r] - lse);
+  }
+  __syncthreads();
+
+  const int nc = min(g.cpu, C - u * g.cpu);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const float* ub = bins + (int64_t)gu * g.cpu * g.wG;
+  float* out = scores + ((int64_t)b * g.Hkv + h) * g.C_max + (int64_t)u * g.cpu;
+  for (int ch = warp; ch < nc; ch += kFinThreads / 32) {
+    float acc = 0.f;
+    for (int r = lane; r < g.wG; r += 32) acc = fmaf(ub[(int64_t)ch * g.wG + r], wts[r], acc);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) out[ch] = acc;
+  }
+}
+
+// Scores of a head with no window rows are all zero (no attention mass).
+__global__ void zero_scores_kernel(ScoreGeom g, const __grid_constant__ SeqTable st, float* scores) {
+  int b, h, u;
+  decode_unit(st, g.Hkv, blockIdx.x, b, h, u);
+  const int T = st.cu[b + 1] - st.cu[b];
+  const int C = (T + g.c - 1) / g.c;
+  const int nc = min(g.cpu, C - u * g.cpu);
+  float* out = scores + ((int64_t)b * g.Hkv + h) * g.C_max + (int64_t)u * g.cpu;
+  for (int ch = threadIdx.x; ch < nc; ch += blockDim.x) out[ch] = 0.f;
+}
+
+cudaError_t launch_finalize(const Plan& pl, const ScoreGeom& g, const SeqTable& st, float* rl,
+                            const float* bins, float* scores, cudaStream_t s) {
+  (void)pl;
+  if (g.n_units == 0) return cudaSuccess;
+  if (g.wG == 0) {
+    zero_scores_kernel<<<g.n_units, 128, 0, s>>>(g, st, scores);
+    return cudaGetLastError();
+  }
+  const size_t smem = (size_t)g.wG * sizeof(float);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(finalize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  finalize_kernel<<<g.n_units, kFinThreads, smem, s>>>(g, st, rl, bins, scores);
+  return cudaGetLastError();
+}
+
+}  // namespace chunkkv

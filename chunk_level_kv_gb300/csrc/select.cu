@@ -1,0 +1,139 @@
+// Top-k chunk selection and kept-index construction.
+//
+// ChunkKV §4.1 Algorithm 1 steps 4-6: per (sequence b, KV head h) keep the
+// k_b = min(L_max / c, C_b) chunks of largest score (ties to the lower chunk
+// index), force in the last w tokens, and write the ascending, duplicate-free
+// union of token positions.
+//
+// One CTA per (b, h):
+//  1. radix select (4 passes of 8 bits) of the k-th largest order key, where
+//     the order key is the fp32 bit pattern mapped to an unsigned integer that
+//     sorts like the float (-0.0 canonicalised to +0.0);
+//  2. one ordered sweep over the chunks: chunk i is kept if its key is above
+//     the threshold, or equal to it and among the first `need_eq` equal keys in
+//     index order (the tie rule);
+//  3. expansion: with R = max(0, T - w) and s = floor(R / c), the kept chunks
+//     below s are whole and land at rank * c; the chunk s straddling R (if kept)
+//     contributes [s*c, R); the recent tokens [R, T) follow.  This order is
+//     ascending by construction, so no sort is needed.
+#include <cub/block/block_scan.cuh>
+
+#include "common.cuh"
+
+namespace chunkkv {
+
+constexpr int kSelThreads = 512;
+
+__device__ __forceinline__ uint32_t order_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  if ((u & 0x7fffffffu) == 0u) u = 0u;                // -0.0 == +0.0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__global__ void __launch_bounds__(kSelThreads)
+select_kernel(SelectGeom sg, const __grid_constant__ SeqTable st, const float* __restrict__ scores,
+              int32_t* __restrict__ indices, int32_t* __restrict__ counts) {
+  using Scan = cub::BlockScan<int, kSelThreads>;
+  __shared__ typename Scan::TempStorage scan_tmp;
+  __shared__ int hist[256];
+  __shared__ uint32_t sh_prefix;
+  __shared__ int sh_remaining;
+  __shared__ int sh_carry_eq, sh_carry_sel, sh_straddle;
+
+  const int bh = blockIdx.x;
+  const int b = bh / sg.Hkv;
+  const int tid = threadIdx.x;
+  const int T = st.cu[b + 1] - st.cu[b];
+  const int c = sg.c;
+  const int C = (T + c - 1) / c;
+  const int k = min(sg.L_max / c, C);
+  const float* A = scores + (int64_t)bh * sg.C_max;
+  int32_t* out = indices + (int64_t)bh * sg.n_cap;
+
+  // ---- 1. threshold key (k-th largest) and how many chunks equal to it are kept
+  uint32_t thr = 0;
+  int need_eq = 0;
+  if (k > 0 && k < C) {
+    uint32_t prefix = 0, mask = 0;
+    int remaining = k;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0;
+      __syncthreads();
+      for (int i = tid; i < C; i += blockDim.x) {
+        const uint32_t key = order_key(A[i]);
+        if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1);
+      }
+      __syncthreads();
+      // descending digits: thread t holds the count of digit 255 - t
+      const int cnt = tid < 256 ? hist[255 - tid] : 0;
+      int incl;
+      Scan(scan_tmp).InclusiveSum(cnt, incl);
+      const int excl = incl - cnt;
+      if (tid < 256 && excl < remaining && incl >= remaining) {
+        sh_prefix = prefix | ((uint32_t)(255 - tid) << shift);
+        sh_remaining = remaining - excl;
+      }
+      __syncthreads();
+      prefix = sh_prefix;
+      remaining = sh_remaining;
+      mask |= 255u << shift;
+      __syncthreads();
+    }
+    thr = prefix;
+    need_eq = remaining;
+  }
+
+  // ---- 2./3. ordered sweep: keep flags, ranks, expansion of whole chunks below s
+  const int Rs = max(0, T - sg.w);
+  const int s = Rs / c;
+  const int part = Rs - s * c;                      // tokens of chunk s below Rs
+  if (tid == 0) { sh_carry_eq = 0; sh_carry_sel = 0; sh_straddle = 0; }
+  __syncthreads();
+  const int limit = min(C, s + 1);                  // chunks that can add tokens below Rs
+  for (int base = 0; base < C && base < limit + 0; base += blockDim.x) {
+    const int i = base + tid;
+    int keep = 0, eq = 0;
+    if (i < C && k > 0) {
+      if (k >= C) {
+        keep = 1;
+      } else {
+        const uint32_t key = order_key(A[i]);
+        eq = key == thr;
+        keep = key > thr;
+      }
+    }
+    int eq_excl, eq_tot;
+    Scan(scan_tmp).ExclusiveSum(eq, eq_excl, eq_tot);
+    __syncthreads();
+    if (eq && sh_carry_eq + eq_excl < need_eq) keep = 1;
+    const int low = (i < s) ? keep : 0;             // whole chunks below Rs
+    int rank_excl, low_tot;
+    Scan(scan_tmp).ExclusiveSum(low, rank_excl, low_tot);
+    if (low) {
+      const int rank = sh_carry_sel + rank_excl;
+      int32_t* o = out + (int64_t)rank * c;
+      for (int t = 0; t < c; ++t) o[t] = i * c + t;
+    }
+    if (i == s && part > 0 && keep) sh_straddle = 1;
+    __syncthreads();
+    if (tid == 0) { sh_carry_eq += eq_tot; sh_carry_sel += low_tot; }
+    __syncthreads();
+  }
+  const int n_low = sh_carry_sel;
+  const int tail0 = n_low * c;
+  const int strad = sh_straddle ? part : 0;
+  for (int t = tid; t < strad; t += blockDim.x) out[tail0 + t] = s * c + t;
+  const int rec0 = tail0 + strad;
+  for (int t = tid; t < T - Rs; t += blockDim.x) out[rec0 + t] = Rs + t;
+  if (tid == 0) counts[bh] = rec0 + (T - Rs);
+}
+
+cudaError_t launch_select(const Plan& pl, const SelectGeom& sg, const SeqTable& st, const float* scores,
+                          int32_t* indices, int32_t* counts, cudaStream_t s) {
+  const int n = pl.B * pl.Hkv;
+  if (n == 0) return cudaSuccess;
+  select_kernel<<<n, kSelThreads, 0, s>>>(sg, st, scores, indices, counts);
+  return cudaGetLastError();
+}
+
+}  // namespace chunkkv

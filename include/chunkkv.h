@@ -1,0 +1,174 @@
+/*
+ * chunkkv.h - ChunkKV chunk-level KV-cache compression on one NVIDIA GB300 (sm_103a).
+ *
+ * The operation is the one of "ChunkKV: Semantic-Preserving KV Cache
+ * Compression for Efficient Long-Context LLM Inference" (NeurIPS'25 notes):
+ *   §4.1 Algorithm 1  - score every key against an observation window of the
+ *                       last w queries, sum the scores per chunk of c tokens,
+ *                       keep the top k = floor(L_max / c) chunks plus the last
+ *                       w tokens, index_select K and V by the kept positions;
+ *   §4.2 Algorithm 2  - layers with l mod N_reuse != 0 do not score; they
+ *                       gather with the index list of layer
+ *                       floor(l / N_reuse) * N_reuse.
+ * The window scores are attention probabilities as in "Kara" §2 Eq. (1):
+ * softmax over all T keys of (Q_w K^T / sqrt(d)) for each window-query row,
+ * summed over the w window rows and over the G = Hq / Hkv query heads that
+ * share a KV head (query head hq belongs to KV head hq / G).  There is no
+ * causal mask inside the window.  Top-k ties go to the lower chunk index.
+ * The kept list is the ascending, duplicate-free union of the selected
+ * chunks' tokens and the last w tokens.
+ *
+ * Conventions for every call
+ *  - Device pointers point to GPU global memory owned by the caller; the
+ *    library never allocates or frees device memory and keeps no per-call
+ *    state between calls.  Host arrays (cu_seqlens, pointer tables) are read
+ *    during the call only.
+ *  - Every call is asynchronous on the given stream (0 = legacy default).
+ *  - Arguments are checked on the host before anything is launched; a bad
+ *    argument returns an error code and launches nothing.  A failed launch
+ *    returns CHUNKKV_ERR_CUDA.  Conditions the GPU detects (a pipeline wait
+ *    that ran out of time) are recorded in the workspace and reported by
+ *    chunkkv_status_check.
+ *  - Layouts (elements; the head dimension d is always contiguous):
+ *      q_win        [B, w, Hq, d]  at q_win[b*q_stride_b + i*q_stride_w + hq*q_stride_h + e]
+ *      k, v         [T_total, Hkv, d] at x[t*kv_stride_t + h*kv_stride_h + e], sequence b
+ *                   owning rows cu_seqlens[b] .. cu_seqlens[b+1]-1 (varlen, ragged)
+ *      chunk_scores [B, Hkv, C_max] fp32, chunk i of sequence b at [b][h][i], i < C_b
+ *      indices      [B, Hkv, n_cap_max] int32, positions local to the sequence
+ *      counts       [B, Hkv] int32
+ *      k_out, v_out [B, Hkv, n_cap_max, d] in the input dtype
+ *    Rows at or beyond counts[b][h] of indices / k_out / v_out, and chunk
+ *    scores at or beyond C_b, are left unwritten.
+ *  - Alignment: q_win, k, v, k_out and v_out start on 16-byte boundaries, and
+ *    kv_stride_t, kv_stride_h, q_stride_* and d are multiples of 16 bytes.
+ */
+#ifndef CHUNKKV_H_
+#define CHUNKKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* chunkkv_stream_t;   /* the same type as cudaStream_t */
+
+typedef enum chunkkv_status {
+  CHUNKKV_OK = 0,
+  CHUNKKV_ERR_INVALID_ARG = 1,         /* a size, pointer, stride or alignment is invalid   */
+  CHUNKKV_ERR_UNSUPPORTED = 2,         /* valid, but outside what this build implements    */
+  CHUNKKV_ERR_WORKSPACE_TOO_SMALL = 3, /* ws_bytes < chunkkv_workspace_size(...)            */
+  CHUNKKV_ERR_CUDA = 4,                /* a CUDA runtime call or kernel launch failed        */
+  CHUNKKV_ERR_TIMEOUT = 5              /* a device-side wait gave up (chunkkv_status_check) */
+} chunkkv_status;
+
+typedef enum chunkkv_dtype { CHUNKKV_F32 = 0, CHUNKKV_BF16 = 1 } chunkkv_dtype;
+
+/* Largest batch one call accepts (the sequence table travels as a launch argument). */
+#define CHUNKKV_MAX_BATCH 1024
+/* Largest number of layers one chunkkv_gather call moves. */
+#define CHUNKKV_MAX_GATHER_LAYERS 64
+
+typedef struct chunkkv_params {
+  int32_t B;        /* sequences, 0 <= B <= CHUNKKV_MAX_BATCH                                  */
+  int32_t Hq;       /* query heads; Hq % Hkv == 0                                               */
+  int32_t Hkv;      /* key/value heads, >= 1                                                    */
+  int32_t d;        /* head dimension, 1..256                                                   */
+  int32_t w;        /* observation window = number of window queries = recent tokens kept, >= 0 */
+  int32_t c;        /* chunk size, >= 1                                                         */
+  int32_t L_max;    /* compressed budget; k = min(L_max / c, C_b) chunks per (b, head), >= 0     */
+  int32_t dtype;    /* chunkkv_dtype of q_win, k, v, k_out, v_out                                */
+  const int32_t* cu_seqlens;  /* HOST array [B+1]: cu[0] = 0, non-decreasing; T_b = cu[b+1]-cu[b] */
+  int64_t q_stride_b, q_stride_w, q_stride_h;   /* element strides of q_win                     */
+  int64_t kv_stride_t, kv_stride_h;             /* element strides of k and v (and their layers) */
+} chunkkv_params;
+
+/*
+ * Output capacities: n_cap_max = max_b min(T_b, k_b*c + min(w, T_b)) is the row
+ * capacity per (b, head) of indices/k_out/v_out; C_max = max_b ceil(T_b / c) is
+ * the chunk capacity of chunk_scores.  Either output pointer may be NULL.
+ */
+chunkkv_status chunkkv_out_capacity(const chunkkv_params* p, int32_t* n_cap_max, int32_t* C_max);
+
+/*
+ * Bytes of device workspace chunkkv_score / chunkkv_compress_layers need for
+ * these shapes (n_layers, n_reuse as passed to chunkkv_compress_layers; use
+ * 1, 1 for chunkkv_score).  The workspace must be zero-filled before its first
+ * use (cudaMemset / torch.zeros); afterwards the library keeps it consistent.
+ * One workspace must not be used by two calls that can run at the same time.
+ */
+chunkkv_status chunkkv_workspace_size(const chunkkv_params* p, int32_t n_layers, int32_t n_reuse,
+                                      size_t* bytes);
+
+/*
+ * Window scores per chunk for one layer (ChunkKV §4.1 Algorithm 1 steps 1-3,
+ * with the probabilities of Kara §2 Eq. (1)):
+ *   A[b][h][i] = sum over g < G, q < w, j in chunk i of softmax_j(Q_w[b,q,h*G+g,:] . K[b,j,h,:] / sqrt(d))
+ * q_win, k: device, layouts above.  chunk_scores: device, written for i < C_b.
+ * ws: device workspace of ws_bytes >= chunkkv_workspace_size(p, 1, 1).
+ */
+chunkkv_status chunkkv_score(const chunkkv_params* p, const void* q_win, const void* k,
+                             float* chunk_scores, void* ws, size_t ws_bytes, chunkkv_stream_t stream);
+
+/*
+ * Top-k chunk selection and kept-index construction (ChunkKV §4.1 Algorithm 1
+ * steps 4-6): for each (b, h) keep the k_b = min(L_max / c, C_b) chunks of
+ * largest chunk_scores (ties to the lower chunk index; -0.0 equals +0.0; the
+ * scores must not be NaN), and write the ascending union of their tokens and
+ * of the last w tokens to indices[b][h][0 .. counts[b][h]).
+ * chunk_scores: device [B, Hkv, C_max]; indices, counts: device outputs.
+ */
+chunkkv_status chunkkv_select(const chunkkv_params* p, const float* chunk_scores, int32_t* indices,
+                              int32_t* counts, chunkkv_stream_t stream);
+
+/*
+ * index_select of K and V by a kept-index list (ChunkKV §4.1 Algorithm 1 step
+ * 6), for n_layers layers that share one list (ChunkKV §4.2 Algorithm 2):
+ *   k_out[l][b][h][r][:] = k[l][cu_seqlens[b] + indices[b][h][r]][h][:]  for r < counts[b][h]
+ * and the same for v.  k, v, k_out, v_out: HOST arrays of n_layers device
+ * pointers (1 <= n_layers <= CHUNKKV_MAX_GATHER_LAYERS); indices, counts: device.
+ * Indices must lie in [0, T_b); the copy is bit-exact.
+ */
+chunkkv_status chunkkv_gather(const chunkkv_params* p, int32_t n_layers, const int32_t* indices,
+                              const int32_t* counts, const void* const* k, const void* const* v,
+                              void* const* k_out, void* const* v_out, chunkkv_stream_t stream);
+
+/*
+ * The whole path over n_layers layers (ChunkKV §4.2 Algorithm 2 around §4.1
+ * Algorithm 1): layers with l % n_reuse == 0 run score + select into index
+ * group g = l / n_reuse; every layer l gathers its own K, V with group
+ * l / n_reuse.
+ *   q_win: HOST array of n_layers device pointers (entries of layers with
+ *          l % n_reuse != 0 are not read and may be NULL);
+ *   k, v, k_out, v_out: HOST arrays of n_layers device pointers;
+ *   indices: device [ceil(n_layers / n_reuse), B, Hkv, n_cap_max];
+ *   counts:  device [ceil(n_layers / n_reuse), B, Hkv];
+ *   chunk_scores: NULL, or device [ceil(n_layers / n_reuse), B, Hkv, C_max];
+ *   ws: device workspace of ws_bytes >= chunkkv_workspace_size(p, n_layers, n_reuse).
+ */
+chunkkv_status chunkkv_compress_layers(const chunkkv_params* p, int32_t n_layers, int32_t n_reuse,
+                                       const void* const* q_win, const void* const* k,
+                                       const void* const* v, void* const* k_out, void* const* v_out,
+                                       int32_t* indices, int32_t* counts, float* chunk_scores,
+                                       void* ws, size_t ws_bytes, chunkkv_stream_t stream);
+
+/*
+ * Synchronises the stream, then reads and clears the device-side error word of
+ * the workspace.  Returns CHUNKKV_ERR_TIMEOUT if a kernel gave up waiting since
+ * the last check (device_code, if not NULL, receives the raw code: the site
+ * that gave up), CHUNKKV_ERR_CUDA if the stream reported an error, else CHUNKKV_OK.
+ */
+chunkkv_status chunkkv_status_check(void* ws, chunkkv_stream_t stream, int32_t* device_code);
+
+/* Static description of a status code. */
+const char* chunkkv_status_string(chunkkv_status s);
+
+/* Which scoring kernel chunkkv_score would use for these shapes: 0 = SIMT, 1 = tensor-core. */
+int32_t chunkkv_score_path(const chunkkv_params* p);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CHUNKKV_H_ */

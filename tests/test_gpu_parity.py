@@ -1,0 +1,217 @@
+"""CUDA library vs CPU oracle on seeded inputs (needs a GB300; calls go through the C-ABI)."""
+import itertools
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity import check_gather, check_indices, check_scores, f64
+from synthetic import configs, generator as gen
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0") if torch.cuda.is_available() else None
+
+
+@pytest.fixture(scope="module")
+def ckv():
+    import chunk_level_kv_gb300 as m     # fails loudly if the library was not built
+    return m
+
+
+def run_and_check(ckv, wl, layers_to_check=None, heads=None, seqs=None, qs=None, ks=None, vs=None,
+                  spans=None):
+    """Compress all layers on the GPU; compare scoring groups / heads / sequences with the oracle."""
+    if ks is None:
+        qs, ks, vs, spans = gen.make_all_layers(wl, DEV)
+    out = ckv.compress_layers(qs, ks, vs, wl.cu_seqlens, Hq=wl.Hq, Hkv=wl.Hkv, w=wl.w, c=wl.c,
+                              L_max=wl.L_max, n_reuse=wl.n_reuse, return_scores=True)
+    assert ckv.chunkkv_status_check(out.workspace) == 0
+    cu = wl.cu_seqlens
+    G = wl.G
+    groups = range(-(-wl.n_layers // wl.n_reuse)) if layers_to_check is None else layers_to_check
+    heads = range(wl.Hkv) if heads is None else heads
+    seqs = range(wl.B) if seqs is None else seqs
+    scores = out.chunk_scores.cpu().numpy()
+    idx = out.indices.cpu().numpy()
+    cnt = out.counts.cpu().numpy()
+    verdicts = []
+    for g in groups:
+        layer = g * wl.n_reuse
+        qf = f64(qs[layer])
+        kf = ks[layer]
+        for b in seqs:
+            T = cu[b + 1] - cu[b]
+            kb = f64(kf[cu[b]:cu[b + 1]])
+            for h in heads:
+                A = oracle.chunk_scores(oracle.key_scores(oracle.group_window_rows(qf[b], h, G), kb[:, h]),
+                                        wl.c)
+                what = f"{wl.name} group {g} seq {b} head {h}"
+                check_scores(scores[g, b, h], A, what)
+                n = int(cnt[g, b, h])
+                verdicts.append(check_indices(idx[g, b, h, :n], A, T, wl.c, wl.w, wl.L_max, what))
+                for layer2 in range(layer, min(layer + wl.n_reuse, wl.n_layers)):
+                    src = ks[layer2][cu[b]:cu[b + 1], h]
+                    check_gather(out.k_out[layer2][b, h, :n], src, idx[g, b, h, :n], what + " K'")
+                    check_gather(out.v_out[layer2][b, h, :n], vs[layer2][cu[b]:cu[b + 1], h],
+                                 idx[g, b, h, :n], what + " V'")
+    return out, verdicts
+
+
+def test_tiny_fp32_exact(ckv):
+    wl = configs.tiny()
+    out, verdicts = run_and_check(ckv, wl)
+    assert verdicts == ["exact", "exact"]
+    # the planted chunk wins in both heads
+    spans = gen.needle_spans(wl)[0][0]
+    (s, e), = spans
+    sc = out.chunk_scores[0, 0].cpu().numpy()
+    assert all(int(np.argmax(sc[h, :52])) == s // wl.c for h in range(2))
+
+
+@pytest.mark.parametrize("T,c,w,Hq,Hkv,L_max", [
+    (3001, 10, 32, 32, 8, 300),      # several tiles, ragged last chunk and unit
+    (2999, 3, 16, 8, 8, 256),        # c = 3, G = 1
+    (4500, 30, 64, 28, 4, 900),      # c = 30, G = 7, window rows 448
+    (1777, 1, 8, 4, 2, 100),         # token-level selection (c = 1)
+    (640, 7, 5, 6, 2, 70),           # odd chunk, odd window
+])
+def test_bf16_shapes(ckv, T, c, w, Hq, Hkv, L_max):
+    wl = configs.llama_layer().with_params(seqlens=(T,), c=c, w=w, Hq=Hq, Hkv=Hkv, L_max=L_max,
+                                           name=f"bf16_T{T}_c{c}_w{w}_G{Hq // Hkv}")
+    run_and_check(ckv, wl)
+
+
+def test_ragged_batch_with_degenerate_sequences(ckv):
+    # empty sequence, shorter than the window, shorter than one chunk, budget above T
+    wl = configs.mistral_ragged().with_params(seqlens=(1000, 0, 20, 2500, 7, 333), B=6, n_layers=3,
+                                              L_max=256, name="ragged6")
+    run_and_check(ckv, wl)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(L_max=100000),              # every chunk kept: K' = K
+    dict(L_max=5),                   # L_max < c: only the recent window
+    dict(w=0),                       # no window: scores all zero, ties to the lowest chunks
+    dict(c=5000),                    # one chunk longer than the prompt
+])
+def test_degenerate_parameters(ckv, kw):
+    wl = configs.llama_layer().with_params(seqlens=(1234,), name=f"deg_{list(kw)[0]}", **kw)
+    out, _ = run_and_check(ckv, wl)
+    if kw.get("L_max") == 100000:
+        n = int(out.counts[0, 0, 0])
+        assert n == 1234 and torch.equal(out.indices[0, 0, 0, :n].cpu(), torch.arange(1234, dtype=torch.int32))
+
+
+def test_layer_reuse_groups(ckv):
+    wl = configs.llama_model().with_params(seqlens=(2048,), n_layers=5, n_reuse=2, L_max=409,
+                                           name="reuse5")
+    out, _ = run_and_check(ckv, wl)
+    assert out.indices.shape[0] == 3
+
+
+def test_select_is_bit_exact_on_given_scores(ckv):
+    # both sides decide on the same fp32 scores: the selection must match exactly (ties included)
+    rng = np.random.default_rng(0)
+    seqlens = [1000, 57, 0, 4096, 333]
+    cu = [0] + list(itertools.accumulate(seqlens))
+    c, w, L_max, Hkv = 10, 16, 200, 3
+    p, keep = ckv.make_params(cu_seqlens=cu, Hq=Hkv, Hkv=Hkv, d=64, w=w, c=c, L_max=L_max,
+                              dtype=torch.bfloat16)
+    n_cap, C_max = ckv.chunkkv_out_capacity(p)
+    scores = rng.integers(0, 6, size=(len(seqlens), Hkv, C_max)).astype(np.float32) * 0.125
+    scores[1] = -scores[1]                    # negative scores and -0.0 order correctly too
+    dev_scores = torch.from_numpy(scores).to(DEV)
+    indices = torch.full((len(seqlens), Hkv, n_cap), -1, dtype=torch.int32, device=DEV)
+    counts = torch.zeros(len(seqlens), Hkv, dtype=torch.int32, device=DEV)
+    ckv.chunkkv_select(p, dev_scores, indices, counts)
+    torch.cuda.synchronize()
+    for b, T in enumerate(seqlens):
+        C = -(-T // c)
+        for h in range(Hkv):
+            A = scores[b, h, :C].astype(np.float64)
+            want = oracle.kept_indices(oracle.top_chunks(A, oracle.n_select(T, c, L_max)), T, c, w)
+            n = int(counts[b, h])
+            assert n == len(want)
+            assert np.array_equal(indices[b, h, :n].cpu().numpy(), want)
+
+
+def test_gather_is_bit_exact(ckv):
+    rng = np.random.default_rng(1)
+    seqlens = [300, 1, 77]
+    cu = [0] + list(itertools.accumulate(seqlens))
+    Hkv, d = 2, 128
+    p, keep = ckv.make_params(cu_seqlens=cu, Hq=Hkv, Hkv=Hkv, d=d, w=4, c=10, L_max=64,
+                              dtype=torch.bfloat16)
+    n_cap, _ = ckv.chunkkv_out_capacity(p)
+    k = [torch.randn(cu[-1], Hkv, d, device=DEV).to(torch.bfloat16) for _ in range(3)]
+    v = [torch.randn(cu[-1], Hkv, d, device=DEV).to(torch.bfloat16) for _ in range(3)]
+    counts = torch.tensor([[min(n_cap, T), min(n_cap, T) // 2] for T in seqlens], dtype=torch.int32)
+    idx = torch.zeros(len(seqlens), Hkv, n_cap, dtype=torch.int32)
+    for b, T in enumerate(seqlens):
+        for h in range(Hkv):
+            n = int(counts[b, h])
+            idx[b, h, :n] = torch.from_numpy(np.sort(rng.choice(T, size=n, replace=False))).int()
+    ko = [torch.zeros(len(seqlens), Hkv, n_cap, d, dtype=torch.bfloat16, device=DEV) for _ in range(3)]
+    vo = [torch.zeros_like(x) for x in ko]
+    ckv.chunkkv_gather(p, idx.to(DEV), counts.to(DEV), k, v, ko, vo)
+    torch.cuda.synchronize()
+    for layer in range(3):
+        for b in range(len(seqlens)):
+            for h in range(Hkv):
+                n = int(counts[b, h])
+                check_gather(ko[layer][b, h, :n], k[layer][cu[b]:cu[b + 1], h], idx[b, h, :n].numpy())
+                check_gather(vo[layer][b, h, :n], v[layer][cu[b]:cu[b + 1], h], idx[b, h, :n].numpy())
+                assert not ko[layer][b, h, n:].any()          # rows beyond the count are untouched
+
+
+def test_score_entry_point_alone(ckv):
+    wl = configs.llama_layer().with_params(seqlens=(5000, 3000), B=2, name="score_only")
+    q, k, v, _ = gen.make_all_layers(wl, DEV)
+    p, keep = ckv.params_for(q[0], k[0], wl.cu_seqlens, Hkv=wl.Hkv, w=wl.w, c=wl.c, L_max=wl.L_max)
+    n_cap, C_max = ckv.chunkkv_out_capacity(p)
+    ws = torch.zeros(ckv.chunkkv_workspace_size(p), dtype=torch.uint8, device=DEV)
+    scores = torch.zeros(2, wl.Hkv, C_max, device=DEV)
+    ckv.chunkkv_score(p, q[0], k[0], scores, ws)
+    assert ckv.chunkkv_status_check(ws) == 0
+    qf = f64(q[0])
+    cu = wl.cu_seqlens
+    for b in range(2):
+        kb = f64(k[0][cu[b]:cu[b + 1]])
+        for h in (0, 5):
+            A = oracle.chunk_scores(oracle.key_scores(oracle.group_window_rows(qf[b], h, wl.G), kb[:, h]), wl.c)
+            check_scores(scores[b, h].cpu().numpy(), A, f"seq {b} head {h}")
+
+
+# ------------------------------------------------------------------ full-size workloads
+
+def test_full_llama_layer_8k(ckv):
+    _, verdicts = run_and_check(ckv, configs.llama_layer())
+    assert len(verdicts) == 8
+
+
+def test_full_llama_model_32k(ckv):
+    # all 32 layers run exactly as the benchmark runs them; groups 0, 7 and 15 are checked
+    # against the oracle in every head, and every layer's gather is checked bit-exactly
+    wl = configs.llama_model()
+    run_and_check(ckv, wl, layers_to_check=[0, 7, 15])
+
+
+def test_full_qwen_128k(ckv):
+    wl = configs.qwen_128k()
+    run_and_check(ckv, wl, layers_to_check=[0, 13], heads=[0, 3])
+
+
+@pytest.mark.parametrize("c,L_max", configs.MISTRAL_SWEEP)
+def test_full_mistral_ragged_sweep(ckv, c, L_max, mistral_inputs):
+    wl, qs, ks, vs, spans = mistral_inputs
+    wl = wl.with_params(c=c, L_max=L_max, name=f"mistral_c{c}_L{L_max}")
+    run_and_check(ckv, wl, layers_to_check=[0, 15], heads=[0, 7], seqs=[0, 5, 15],
+                  qs=qs, ks=ks, vs=vs, spans=spans)
+
+
+@pytest.fixture(scope="module")
+def mistral_inputs():
+    wl = configs.mistral_ragged()
+    qs, ks, vs, spans = gen.make_all_layers(wl, DEV)
+    return wl, qs, ks, vs, spans

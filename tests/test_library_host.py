@@ -1,0 +1,120 @@
+"""libchunkkv.so on the host: it loads, exports the header's symbols, and checks arguments.
+
+Nothing here launches a kernel: every call below either computes sizes or is
+rejected by the host-side argument checks before any CUDA call.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "chunkkv.h")
+LIBPATH = os.path.join(ROOT, "chunk_level_kv_gb300", "libchunkkv.so")
+
+
+@pytest.fixture(scope="module")
+def ckv():
+    if not os.path.exists(LIBPATH):
+        import __graft_entry__
+        __graft_entry__.build()
+    import chunk_level_kv_gb300 as m
+    return m
+
+
+def test_exports_every_declared_function(ckv):
+    text = open(HEADER).read()
+    names = set(re.findall(r"^\s*(?:const\s+char\*|chunkkv_status|int32_t)\s+(chunkkv_\w+)\s*\(", text,
+                           flags=re.M))
+    assert {"chunkkv_score", "chunkkv_select", "chunkkv_gather", "chunkkv_compress_layers",
+            "chunkkv_workspace_size", "chunkkv_out_capacity", "chunkkv_status_check"} <= names
+    lib = ctypes.CDLL(LIBPATH)
+    for n in sorted(names):
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(ckv):
+    from chunk_level_kv_gb300._lib import LIB
+    for code in range(6):
+        assert LIB.chunkkv_status_string(code)
+    assert LIB.chunkkv_status_string(0) == b"ok"
+
+
+def _p(ckv, **kw):
+    import torch
+    args = dict(cu_seqlens=[0, 512], Hq=4, Hkv=2, d=64, w=8, c=10, L_max=128, dtype=torch.float32)
+    args.update(kw)
+    return ckv.make_params(**args)
+
+
+@pytest.mark.parametrize("T,w,c,L_max,n_cap,C", [
+    (32768, 32, 10, 6553, 6582, 3277),          # LLaMA-3-8B 32K, 20 % budget
+    (131072, 64, 10, 13107, 13164, 13108),      # Qwen2-7B 128K, 10 % budget
+    (8192, 32, 10, 819, 842, 820),              # LLaMA-3-8B single layer, 10 %
+    (512, 8, 10, 128, 128, 52),                 # tiny
+    (20, 30, 7, 7, 20, 3),                      # window longer than the prompt
+    (100, 5, 10, 0, 5, 10),                     # no chunk budget: recent window only
+    (0, 5, 10, 50, 0, 0),                       # empty sequence
+])
+def test_out_capacity(ckv, T, w, c, L_max, n_cap, C):
+    import torch
+    p, keep = _p(ckv, cu_seqlens=[0, T], w=w, c=c, L_max=L_max, d=128, Hq=32, Hkv=8,
+                 dtype=torch.bfloat16)
+    assert ckv.chunkkv_out_capacity(p) == (n_cap, C)
+
+
+def test_workspace_size_grows_with_window(ckv):
+    import torch
+    small, k1 = _p(ckv, cu_seqlens=[0, 4096], w=8, d=128, Hq=8, Hkv=8, dtype=torch.bfloat16)
+    big, k2 = _p(ckv, cu_seqlens=[0, 4096], w=64, d=128, Hq=8, Hkv=8, dtype=torch.bfloat16)
+    assert 0 < ckv.chunkkv_workspace_size(small) < ckv.chunkkv_workspace_size(big)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Hq=3, Hkv=2), 1),                      # Hq not a multiple of Hkv
+    (dict(c=0), 1),
+    (dict(w=-1), 1),
+    (dict(L_max=-5), 1),
+    (dict(d=6), 1),                              # 24-byte fp32 rows are not 16-byte multiples
+    (dict(d=512), 2),                            # beyond the head-dimension limit
+    (dict(cu_seqlens=[0, 10, 5]), 1),            # decreasing offsets
+    (dict(cu_seqlens=[3, 10]), 1),               # offsets must start at 0
+    (dict(cu_seqlens=[0] * 1100), 2),            # batch beyond CHUNKKV_MAX_BATCH
+    (dict(w=2048, Hq=8, Hkv=2), 2),              # w * G beyond the window-row limit
+    (dict(kv_strides=(64 * 2 + 1, 64)), 1),      # token stride breaks 16-byte rows
+])
+def test_invalid_params_rejected(ckv, kw, code):
+    p, keep = _p(ckv, **kw)
+    from chunk_level_kv_gb300._lib import LIB
+    n = ctypes.c_size_t()
+    assert LIB.chunkkv_workspace_size(ctypes.byref(p), 1, 1, ctypes.byref(n)) == code
+
+
+def test_null_and_misaligned_pointers_rejected_before_launch(ckv):
+    from chunk_level_kv_gb300._lib import LIB
+    p, keep = _p(ckv)
+    P = ctypes.byref(p)
+    ws_bytes = ckv.chunkkv_workspace_size(p)
+    # null inputs, a misaligned pointer, a workspace that is too small: no launch happens
+    assert LIB.chunkkv_score(P, None, None, None, None, 0, None) == 1
+    assert LIB.chunkkv_score(P, 0x1001, 0x2000, 0x3000, 0x4000, ws_bytes, None) == 1
+    assert LIB.chunkkv_score(P, 0x1000, 0x2000, 0x3000, 0x4000, 16, None) == 3
+    assert LIB.chunkkv_select(P, None, None, None, None) == 1
+    arr = (ctypes.c_void_p * 1)(0x1000)
+    assert LIB.chunkkv_gather(P, 0, 0x1000, 0x2000, arr, arr, arr, arr, None) == 1   # zero layers
+    assert LIB.chunkkv_gather(P, 65, 0x1000, 0x2000, arr, arr, arr, arr, None) == 1  # too many
+    bad = (ctypes.c_void_p * 1)(0x1008)
+    assert LIB.chunkkv_gather(P, 1, 0x1000, 0x2000, bad, arr, arr, arr, None) == 1
+    assert LIB.chunkkv_compress_layers(P, 1, 0, arr, arr, arr, arr, arr, 0x1000, 0x2000, None,
+                                       0x3000, ws_bytes, None) == 1                  # n_reuse 0
+    assert LIB.chunkkv_status_check(None, None, None) == 1
+
+
+def test_empty_batch_is_a_no_op(ckv):
+    from chunk_level_kv_gb300._lib import LIB
+    p, keep = _p(ckv, cu_seqlens=[0])
+    assert ckv.chunkkv_out_capacity(p) == (0, 0)
+    arr = (ctypes.c_void_p * 1)(0)
+    assert LIB.chunkkv_compress_layers(ctypes.byref(p), 1, 1, arr, arr, arr, arr, arr, None, None, None,
+                                       None, 0, None) == 0
