@@ -1,0 +1,348 @@
+"""ChunkKV compression throughput on GB300: HBM GB/s and tokens/s of the full path.
+
+One step = one chunkkv_compress_layers call over every layer of the workload
+(score + select on the scoring layers of Algorithm 2, gather on every layer),
+inputs resident in HBM.  value = algorithmic bytes / device time, where the
+algorithmic bytes are the keys read by every scoring layer plus the kept K and
+V rows read and written on every layer (plus the window queries).
+
+--impl reference times the CPU oracle on the host cores on a bounded sample
+of the same workload (one scoring layer of a few heads per step) and reports
+the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from synthetic import configs, generator as gen  # noqa: E402
+
+METRIC = "chunkkv_compress_hbm_gbps"
+UNIT = "GB/s"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([x.strip() for x in line.split(",")])
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm = [float(r[1]) for r in self.rows if len(r) >= 9 and r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if len(r) >= 9 and r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in self.rows:
+            if len(r) >= 9:
+                for n, v in zip(names, r[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(self.rows)}
+
+
+def algorithmic_bytes(wl, counts) -> int:
+    """K read by the scoring layers + kept K, V rows read and written on every layer + Q_w."""
+    elt = 2 if wl.dtype == "bf16" else 4
+    n_score = -(-wl.n_layers // wl.n_reuse)
+    k_read = n_score * wl.T_total * wl.Hkv * wl.d * elt
+    q_read = n_score * wl.B * wl.w * wl.Hq * wl.d * elt
+    kept = 0
+    cnt = counts.to("cpu").numpy().astype(np.int64)         # [groups, B, Hkv]
+    for layer in range(wl.n_layers):
+        kept += int(cnt[layer // wl.n_reuse].sum())
+    return k_read + q_read + 4 * kept * wl.d * elt
+
+
+def run_gpu(args):
+    import chunk_level_kv_gb300 as ckv
+    ws_n, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws_n > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    wl = configs.ALL[args.workload]()
+    qs, ks, vs, _ = gen.make_all_layers(wl, dev)
+    p, keep = ckv.params_for(next(q for q in qs if q is not None), ks[0], wl.cu_seqlens, Hkv=wl.Hkv, w=wl.w,
+                             c=wl.c, L_max=wl.L_max)
+    n_cap, C_max = ckv.chunkkv_out_capacity(p)
+    groups = -(-wl.n_layers // wl.n_reuse)
+    ko = [torch.empty(wl.B, wl.Hkv, n_cap, wl.d, dtype=ks[0].dtype, device=dev) for _ in range(wl.n_layers)]
+    vo = [torch.empty_like(x) for x in ko]
+    idx = torch.empty(groups, wl.B, wl.Hkv, n_cap, dtype=torch.int32, device=dev)
+    cnt = torch.empty(groups, wl.B, wl.Hkv, dtype=torch.int32, device=dev)
+    ws = torch.zeros(ckv.chunkkv_workspace_size(p, wl.n_layers, wl.n_reuse), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ckv.chunkkv_compress_layers(p, wl.n_reuse, qs, ks, vs, ko, vo, idx, cnt, None, ws)
+
+    for _ in range(args.warmup):
+        step()
+    ckv.chunkkv_status_check(ws)
+    in_bytes = sum(x.numel() * x.element_size() for x in ks + vs) + \
+        sum(q.numel() * q.element_size() for q in qs if q is not None)
+    l2_note = "inputs larger than L2 (no flush)" if in_bytes > 2 * 129e6 else "L2 flushed between steps"
+    flush = torch.empty(int(2 * 129e6) // 4, dtype=torch.float32, device=dev) if in_bytes <= 2 * 129e6 else None
+
+    sampler = ClockSampler(local)
+    if ws_n > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    times = []
+    for _ in range(args.steps):
+        if flush is not None:
+            flush.fill_(1.0)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        times.append((e0, e1))
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = [a.elapsed_time(b) for a, b in times]
+    ckv.chunkkv_status_check(ws)
+    step_ms = sum(ms) / len(ms)
+    if ws_n > 1:
+        t = torch.tensor([step_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        step_ms = float(t)
+    nbytes = algorithmic_bytes(wl, cnt)
+    value = nbytes * ws_n / (step_ms * 1e-3) / 1e9
+    tokens_s = wl.T_total * ws_n / (step_ms * 1e-3)
+
+    # ---- per-stage device time of the dominant kernel (window scoring), same stream, same data
+    score_ms = []
+    sc = torch.empty(wl.B, wl.Hkv, max(C_max, 1), device=dev)
+    ckv.chunkkv_score(p, qs[0], ks[0], sc, ws)
+    for layer in range(0, wl.n_layers, wl.n_reuse):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        ckv.chunkkv_score(p, qs[layer], ks[layer], sc, ws)
+        e1.record(stream)
+        score_ms.append((e0, e1))
+    torch.cuda.synchronize()
+    score_avg = sum(a.elapsed_time(b) for a, b in score_ms) / len(score_ms)
+    peaks, peak_src = measured_peaks()
+    elt = 2 if wl.dtype == "bf16" else 4
+    score_bytes = wl.T_total * wl.Hkv * wl.d * elt + wl.B * wl.w * wl.Hq * wl.d * elt
+    path = ckv.chunkkv_score_path(p)
+    roof_peak = peaks["hbm_gbs"]
+    achieved = score_bytes / (score_avg * 1e-3) / 1e9
+    launches_per_step = groups * 4          # score, finalize, select, gather per reuse group
+
+    # ---- end to end through the C-ABI with host buffers (pinned), copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        hq = [q.cpu().pin_memory() if q is not None else None for q in qs]
+        hk = [x.cpu().pin_memory() for x in ks]
+        hv = [x.cpu().pin_memory() for x in vs]
+        hko = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in ko]
+        hvo = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in vo]
+        hidx = torch.empty(idx.shape, dtype=idx.dtype).pin_memory()
+        hcnt = torch.empty(cnt.shape, dtype=cnt.dtype).pin_memory()
+        h2d = sum(x.numel() * x.element_size() for x in hk + hv) + \
+            sum(q.numel() * q.element_size() for q in hq if q is not None)
+        d2h = sum(x.numel() * x.element_size() for x in hko + hvo) + hidx.numel() * 4 + hcnt.numel() * 4
+
+        def e2e_step():
+            for dq, hqq in zip(qs, hq):
+                if dq is not None:
+                    dq.copy_(hqq, non_blocking=True)
+            for dk, hkk in zip(ks, hk):
+                dk.copy_(hkk, non_blocking=True)
+            for dv, hvv in zip(vs, hv):
+                dv.copy_(hvv, non_blocking=True)
+            step()
+            for a, b in zip(hko, ko):
+                a.copy_(b, non_blocking=True)
+            for a, b in zip(hvo, vo):
+                a.copy_(b, non_blocking=True)
+            hidx.copy_(idx, non_blocking=True)
+            hcnt.copy_(cnt, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_e2e = max(1, min(args.steps, 3))
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / n_e2e
+        e2e = {"value": round(nbytes * ws_n / (e2e_ms * 1e-3) / 1e9, 3), "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms, 4)}
+
+    cpu = None
+    if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl, qs, ks, budget_s=args.cpu_seconds)
+
+    if ws_n > 1:
+        torch.distributed.barrier()
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": ws_n, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic (seeded, needles planted)",
+        "config": {"workload": wl.name, "B": wl.B, "T": list(wl.seqlens) if wl.B <= 4 else "ragged",
+                   "T_total": wl.T_total, "layers": wl.n_layers, "n_reuse": wl.n_reuse, "Hq": wl.Hq,
+                   "Hkv": wl.Hkv, "d": wl.d, "w": wl.w, "c": wl.c, "L_max": wl.L_max,
+                   "l2": l2_note, "parallelism": f"replicas x{ws_n}"},
+        "tokens_per_s": round(tokens_s, 1),
+        "algorithmic_bytes_per_step": nbytes,
+        "hbm_roof_frac": round(value / ws_n / peaks["hbm_gbs"], 4),
+        "roofline": {"kernel": "window scoring (chunkkv_score: " + ("tcgen05" if path == 1 else "SIMT") +
+                     " + finalize)", "bound": "hbm", "achieved": round(achieved, 2), "peak": roof_peak,
+                     "unit": "GB/s", "frac": round(achieved / roof_peak, 4), "traffic": None,
+                     "peak_source": f"{peak_src} hbm_gbs", "avg_launch_ms": round(score_avg, 5)},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(wl, qs, ks, budget_s: float = 15.0):
+    """The oracle as it stands on this host: Algorithm 1 for whole heads of scoring layer 0."""
+    import oracle
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    q = qs[0].detach().to("cpu", torch.float32).numpy().astype(np.float64)
+    cu = wl.cu_seqlens
+    elt = 2 if wl.dtype == "bf16" else 4
+    done_bytes, done_tokens, heads = 0, 0, 0
+    t0 = time.perf_counter()
+    for b in range(wl.B):
+        kb = ks[0][cu[b]:cu[b + 1]].detach().to("cpu", torch.float32).numpy().astype(np.float64)
+        T = cu[b + 1] - cu[b]
+        for h in range(wl.Hkv):
+            A, sel, idx = oracle.chunkkv_head(oracle.group_window_rows(q[b], h, wl.G), kb[:, h], wl.c, wl.w,
+                                              wl.L_max)
+            oracle.gather(kb[:, h], idx)
+            done_bytes += T * wl.d * elt + 2 * len(idx) * wl.d * elt
+            done_tokens += T
+            heads += 1
+            if time.perf_counter() - t0 > budget_s:
+                break
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(done_bytes / dt / 1e9, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"Algorithm 1 on {heads} (sequence, KV head) pairs of scoring layer 0 "
+                      f"({done_tokens} tokens, {dt:.1f} s), fp64 numpy, K read + kept K/V counted "
+                      f"like the GPU metric", "threads": "numpy/BLAS default"}
+
+
+def run_reference(args):
+    ws_n, rank, local = dist_env()
+    if rank != 0:
+        return
+    wl = configs.ALL[args.workload]()
+    qs, ks = [], []
+    q, k, v = gen.make_layer(wl, 0, "cpu")
+    qs.append(q)
+    ks.append(k)
+    per_step = min(args.cpu_seconds, 150.0 / max(1, args.steps + args.warmup))   # whole run ~ 2.5 min
+    for _ in range(args.warmup):
+        cpu_baseline(wl, qs, ks, budget_s=per_step / 4)
+    vals = []
+    t0 = time.perf_counter()
+    last = None
+    for _ in range(args.steps):
+        last = cpu_baseline(wl, qs, ks, budget_s=per_step)
+        vals.append(last["value"])
+    wall = time.perf_counter() - t0
+    value = statistics.mean(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws_n,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(wall / max(1, args.steps) * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "B": wl.B, "T_total": wl.T_total, "layers": wl.n_layers,
+                   "n_reuse": wl.n_reuse, "w": wl.w, "c": wl.c, "L_max": wl.L_max},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": last["cores"], "kind": "oracle",
+                         "sample": last["sample"]},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--workload", choices=sorted(configs.ALL), default="llama_model")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -284,7 +284,7 @@ def make_layer(wl: Workload, layer: int, device, spans=None, with_q=None):
     q = gen_q_window(wl, layer, device)
     k = gen_kv_raw(wl, layer, TENSOR_K, device)
     v = gen_kv_raw(wl, layer, TENSOR_V, device)
-    if any(len(s) for s in spans):
+    if wl.w > 0 and any(len(s) for s in spans):         # needles follow the window queries
         vec = torch.from_numpy(needle_vectors(wl, q)).to(TORCH_DTYPE[wl.dtype]).to(device)
         cu = wl.cu_seqlens
         for b, seq_spans in enumerate(spans):
