@@ -48,6 +48,7 @@ def _load():
         "chunkkv_compress_layers": [P, i32, i32, pp, pp, pp, pp, pp, vp, vp, vp, vp, sz, vp],
         "chunkkv_status_check": [vp, vp, ctypes.POINTER(i32)],
         "chunkkv_score_path": [P],
+        "chunkkv_score_noalloc": [P, vp, vp, vp, vp],
     }
     for name, args in sigs.items():
         fn = getattr(lib, name)

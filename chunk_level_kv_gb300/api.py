@@ -94,6 +94,17 @@ def chunkkv_score(p: Params, q_win, k, chunk_scores, ws) -> None:
                                               _ptr(ws), ws.numel() * ws.element_size(), _stream(k.device)))
 
 
+def chunkkv_score_noalloc(p: Params, q_win, k, chunk_scores) -> None:
+    """chunkkv_score without a workspace: for callers that cannot allocate device memory.
+
+    The scratch lives in one fixed-size device array inside the library (shared
+    by every call, so calls must not overlap on the GPU); shapes that need more
+    raise ChunkKVError with CHUNKKV_ERR_WORKSPACE_TOO_SMALL.
+    """
+    _check("chunkkv_score_noalloc", LIB.chunkkv_score_noalloc(ctypes.byref(p), _ptr(q_win), _ptr(k),
+                                                              _ptr(chunk_scores), _stream(k.device)))
+
+
 def chunkkv_select(p: Params, chunk_scores, indices, counts) -> None:
     _check("chunkkv_select", LIB.chunkkv_select(ctypes.byref(p), _ptr(chunk_scores), _ptr(indices),
                                                 _ptr(counts), _stream(counts.device)))
@@ -165,6 +176,6 @@ def compress_layers(q_win, k, v, cu_seqlens, *, Hq: int, Hkv: int, w: int, c: in
 
 __all__ = [
     "ChunkKVError", "CompressResult", "Params", "chunkkv_compress_layers", "chunkkv_gather",
-    "chunkkv_out_capacity", "chunkkv_score", "chunkkv_score_path", "chunkkv_select", "chunkkv_status_check",
+    "chunkkv_out_capacity", "chunkkv_score", "chunkkv_score_noalloc", "chunkkv_score_path", "chunkkv_select", "chunkkv_status_check",
     "chunkkv_workspace_size", "compress_layers", "make_params", "params_for", "MAX_GATHER_LAYERS",
 ]

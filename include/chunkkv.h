@@ -20,8 +20,9 @@
  *
  * Conventions for every call
  *  - Device pointers point to GPU global memory owned by the caller; the
- *    library never allocates or frees device memory and keeps no per-call
- *    state between calls.  Host arrays (cu_seqlens, pointer tables) are read
+ *    library never allocates or frees device memory while it runs and keeps
+ *    no per-call state between calls (its one fixed device array is the
+ *    scratch of chunkkv_score_noalloc, described there).  Host arrays (cu_seqlens, pointer tables) are read
  *    during the call only.
  *  - Every call is asynchronous on the given stream (0 = legacy default).
  *  - Arguments are checked on the host before anything is launched; a bad
@@ -152,6 +153,30 @@ chunkkv_status chunkkv_compress_layers(const chunkkv_params* p, int32_t n_layers
                                        const void* const* v, void* const* k_out, void* const* v_out,
                                        int32_t* indices, int32_t* counts, float* chunk_scores,
                                        void* ws, size_t ws_bytes, chunkkv_stream_t stream);
+
+/*
+ * Window scores for callers that cannot allocate device memory.  The ChunkKV
+ * notes have no counterpart for this call; it exists for code that must not
+ * call cudaMalloc when it scores (code running inside a memory pool or arena
+ * that owns all device memory, allocator callbacks, runtimes with a memory
+ * budget fixed at start-up) and has no workspace to lend.
+ * It computes exactly what chunkkv_score computes, with the portable scoring
+ * kernel, and takes no workspace: its scratch is one device array of
+ * CHUNKKV_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads
+ * the library holds until the process exits.  It allocates nothing.
+ *  - Shapes whose scratch would exceed that array return
+ *    CHUNKKV_ERR_WORKSPACE_TOO_SMALL before anything is launched (about
+ *    4 * w * G * Hkv * sum_b T_b / c bytes are needed; e.g. T = 32768 tokens with
+ *    w*G = 128 rows and 8 KV heads fits).
+ *  - All calls share the array and it keeps the last call's contents; a call
+ *    reads only what it wrote itself, so nothing has to be cleared.  Calls whose
+ *    kernels can overlap on the GPU (other streams, other threads) race on it.
+ *  - The first call on each device looks up the array's device address with
+ *    that device current; make it before any stream capture begins.
+ */
+#define CHUNKKV_NOALLOC_SCRATCH_BYTES (16u << 20)
+chunkkv_status chunkkv_score_noalloc(const chunkkv_params* p, const void* q_win, const void* k,
+                                     float* chunk_scores, chunkkv_stream_t stream);
 
 /*
  * Synchronises the stream, then reads and clears the device-side error word of
