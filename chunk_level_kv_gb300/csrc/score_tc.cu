@@ -1,16 +1,603 @@
-// Tensor-core window scoring (tcgen05 + TMA + TMEM) for bf16 keys.
+// Tensor-core window scoring (tcgen05 + TMA + TMEM) for bf16 keys, head dim 128.
+//
+// ChunkKV §4.1 Algorithm 1 steps 1-3 with the probabilities of Kara §2 Eq. (1),
+// in the single-pass unit decomposition described in score.cu: each work item
+// is one (scoring unit, 128-row M tile of the window rows).  Per item the CTA
+//   - loads the item's 128 packed window rows (Q) once by TMA,
+//   - streams the unit's keys in tiles of 80 through shared memory by TMA,
+//   - computes S = Q K^T (128 x 80, fp32) with tcgen05.mma into TMEM,
+//   - lets each of 128 softmax threads own one window row: it reads its row of
+//     S from TMEM, forms 2^(s*log2(e)/sqrt(d) - R) with R the row maximum of the
+//     item's first tile, and sums those per chunk (chunk boundaries are compile
+//     time constants for each of the C / gcd(80, C) tile phases), writing one
+//     fp32 bin per (chunk, row) and the row's (R, sum) at the end of the item.
+// A row whose values would outgrow the first-tile reference by more than 2^64
+// switches to the new maximum and rescales what it already wrote.
+//
+// Warp roles (256 threads): warp 0 = TMA producer, warp 1 = TMEM owner and MMA
+// issuer, warps 4-7 = softmax (warp 4+i reads TMEM lanes 32i..32i+31), warps 2-3
+// idle.  Two CTAs fit on one SM (104 KB shared memory, 256 TMEM columns each).
+// Every wait is bounded: a wait that runs out records an error code in the
+// workspace error word, raises a CTA-wide abort flag and the CTA drains and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "common.cuh"
 
 namespace chunkkv {
+namespace tc {
 
-bool tc_supported(const Plan& pl) { (void)pl; return false; }
+constexpr int kN = 80;                         // keys per tile (MMA N)
+constexpr int kD = 128;                        // head dimension
+constexpr int kStagesK = 2;                    // K tiles in shared memory
+constexpr int kStagesQ = 2;                    // Q tiles in shared memory
+constexpr int kStagesT = 3;                    // accumulator stages in TMEM (3 x 80 columns)
+constexpr int kTmemCols = 256;
+constexpr int kThreads = 256;
+constexpr int kPanelQ = 128 * 128;             // one 64-element (128 B) panel of 128 rows
+constexpr int kPanelK = kN * 128;              // one 128 B panel of 80 key rows
+constexpr int kQBytes = 2 * kPanelQ;           // 32 KB per Q tile
+constexpr int kKBytes = 2 * kPanelK;           // 20 KB per K tile
+constexpr int kSmemBytes = 1024 + kStagesQ * kQBytes + kStagesK * kKBytes + 256;
+constexpr uint32_t kIdesc = (1u << 4)                         // D = fp32
+                          | (1u << 7) | (1u << 10)           // A = B = bf16
+                          | ((uint32_t)(kN >> 3) << 17)      // N
+                          | ((uint32_t)(128 >> 4) << 24);    // M
+constexpr float kBig = 18446744073709551616.0f;              // 2^64: rescale threshold
 
-void tc_plan(Plan& pl) { pl.use_tc = 0; pl.tc_mt = 0; }
+struct TcGeom {
+  int32_t Hkv, wG, MT, cpu, ku, n_items;
+  float alpha;                       // log2(e) / sqrt(d)
+  long long timeout;                 // clock64 cycles per wait
+};
 
-cudaError_t launch_score_tc(const Plan& pl, const ScoreGeom& g, const SeqTable& st, const void* q,
-                            const void* k, float* rl, float* bins, void* qpack, int32_t* err,
-                            cudaStream_t s) {
-  (void)pl; (void)g; (void)st; (void)q; (void)k; (void)rl; (void)bins; (void)qpack; (void)err; (void)s;
+// ---------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
+      ::"r"(dst), "l"((uint64_t)map), "r"(bar), "r"(c0), "r"(c1) : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
+                                            int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
+      "[%2];" ::"r"(dst), "l"((uint64_t)map), "r"(bar), "r"(c0), "r"(c1), "r"(c2) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}"
+      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(acc) : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row groups 1024 B apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;                 // leading byte offset (not used by swizzled K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;       // stride byte offset
+  d |= (uint64_t)1 << 46;                 // descriptor version
+  d |= (uint64_t)2 << 61;                 // 128-byte swizzle
+  return d;
+}
+
+// 16 consecutive fp32 TMEM columns of this thread's lane (32x32b shape, x16).  The
+// registers may only be read after tmem_wait16, which takes them as read-write
+// operands so that no use can be scheduled before tcgen05.wait::ld.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait16(uint32_t (&r)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15])
+               :
+               : "memory");
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__host__ __device__ constexpr int gcd_c(int a, int b) { return b == 0 ? a : gcd_c(b, a % b); }
+
+// Shared state of a CTA for bounded waits.
+struct Ctl {
+  int32_t* err;
+  volatile int* abort;
+  long long timeout;
+};
+
+__device__ __forceinline__ bool wait_bar(const Ctl& ctl, uint32_t bar, uint32_t parity, int code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*ctl.abort) return false;
+    if (clock64() - t0 > ctl.timeout) {
+      atomicCAS(ctl.err, 0, code);
+      *ctl.abort = 1;
+      return false;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- softmax side
+// Per-row state of the item being processed.
+struct RowState {
+  float negR;      // -(reference exponent)
+  float l;         // sum of 2^(t - R) over the item's keys so far
+  float carry;     // partial sum of a chunk that continues into the next tile
+  bool over;       // some chunk exceeded kBig (rescale needed)
+};
+
+// Segment SEG (columns 16*SEG .. 16*SEG+15) of a tile whose column 0 has phase PH
+// inside its chunk.  bin points at bins[(gu*cpu + q)*wG + row], q being the
+// unit-local chunk that holds the tile's column 0.
+template <int C, int PH, int SEG, bool MASK>
+__device__ __forceinline__ void tile_seg(const uint32_t (&r)[16], float alpha, RowState& s, float* bin, int wG,
+                                         int valid, bool write) {
+  float acc = s.carry;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int col = SEG * 16 + i;
+    float e = ex2(fmaf(__uint_as_float(r[i]), alpha, s.negR));
+    if (MASK) e = (col < valid) ? e : 0.f;
+    acc += e;
+    if ((PH + col + 1) % C == 0) {
+      const int chunk = (PH + col + 1) / C - 1;
+      s.over |= !(acc <= kBig);
+      if (write) bin[(size_t)chunk * wG] = acc;
+      s.l += acc;
+      acc = 0.f;
+    }
+  }
+  s.carry = acc;
+}
+
+// One 80-column tile: five 16-column TMEM loads, each issued while the previous
+// segment is being processed.
+template <int C, int PH, bool MASK>
+__device__ __forceinline__ void tile_phase(uint32_t taddr, float alpha, RowState& s, float* bin, int wG, int valid,
+                                           bool write) {
+  uint32_t a[16], b[16];
+  tmem_ld16(taddr, a);
+  tmem_wait16(a);
+  tmem_ld16(taddr + 16, b);
+  tile_seg<C, PH, 0, MASK>(a, alpha, s, bin, wG, valid, write);
+  tmem_wait16(b);
+  tmem_ld16(taddr + 32, a);
+  tile_seg<C, PH, 1, MASK>(b, alpha, s, bin, wG, valid, write);
+  tmem_wait16(a);
+  tmem_ld16(taddr + 48, b);
+  tile_seg<C, PH, 2, MASK>(a, alpha, s, bin, wG, valid, write);
+  tmem_wait16(b);
+  tmem_ld16(taddr + 64, a);
+  tile_seg<C, PH, 3, MASK>(b, alpha, s, bin, wG, valid, write);
+  tmem_wait16(a);
+  tile_seg<C, PH, 4, MASK>(a, alpha, s, bin, wG, valid, write);
+}
+
+template <int C, int PH = 0>
+__device__ __forceinline__ void tile_dispatch(int ph, bool mask, uint32_t taddr, float alpha, RowState& s, float* bin,
+                                              int wG, int valid, bool write) {
+  if constexpr (PH < C) {
+    if (ph == PH) {
+      if (mask)
+        tile_phase<C, PH, true>(taddr, alpha, s, bin, wG, valid, write);
+      else
+        tile_phase<C, PH, false>(taddr, alpha, s, bin, wG, valid, write);
+    } else {
+      tile_dispatch<C, PH + gcd_c(kN, C)>(ph, mask, taddr, alpha, s, bin, wG, valid, write);
+    }
+  }
+}
+
+// Row maximum of the first `valid` columns of a tile (raw dot products).
+__device__ __forceinline__ float tile_max(uint32_t taddr, int valid) {
+  float m = -INFINITY;
+  uint32_t r[16];
+#pragma unroll
+  for (int sg = 0; sg < kN / 16; ++sg) {
+    tmem_ld16(taddr + 16 * sg, r);
+    tmem_wait16(r);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) m = (16 * sg + i < valid) ? fmaxf(m, __uint_as_float(r[i])) : m;
+  }
+  return m;
+}
+
+// ---------------------------------------------------------------- the kernel
+template <int C>
+__global__ void __launch_bounds__(kThreads, 2)
+score_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k, TcGeom g,
+                const __grid_constant__ SeqTable st, float* __restrict__ rl, float* __restrict__ bins,
+                int32_t* __restrict__ err) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* sQ = smem;                                          // kStagesQ x 32 KB
+  uint8_t* sK = smem + kStagesQ * kQBytes;                     // kStagesK x 20 KB
+  uint64_t* bars = (uint64_t*)(sK + kStagesK * kKBytes);
+  uint64_t* q_full = bars;                                     // [kStagesQ]
+  uint64_t* q_empty = bars + kStagesQ;                         // [kStagesQ]
+  uint64_t* k_full = bars + 2 * kStagesQ;                      // [kStagesK]
+  uint64_t* k_empty = k_full + kStagesK;                       // [kStagesK]
+  uint64_t* t_full = k_empty + kStagesK;                       // [kStagesT]
+  uint64_t* t_empty = t_full + kStagesT;                       // [kStagesT]
+  uint32_t* tmem_slot = (uint32_t*)(t_empty + kStagesT);
+  volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStagesQ; ++i) { mbar_init(smem_u32(&q_full[i]), 1); mbar_init(smem_u32(&q_empty[i]), 1); }
+    for (int i = 0; i < kStagesK; ++i) { mbar_init(smem_u32(&k_full[i]), 1); mbar_init(smem_u32(&k_empty[i]), 1); }
+    for (int i = 0; i < kStagesT; ++i) { mbar_init(smem_u32(&t_full[i]), 1); mbar_init(smem_u32(&t_empty[i]), 128); }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmap_q) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmap_k) : "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(kTmemCols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Ctl ctl{err, abort_flag, g.timeout};
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t kc = 0, qc = 0;
+      for (int item = blockIdx.x; item < g.n_items && !*abort_flag; item += gridDim.x) {
+        const int unit = item / g.MT, mt = item - unit * g.MT;
+        int b, h, u;
+        decode_unit(st, g.Hkv, unit, b, h, u);
+        const int T = st.cu[b + 1] - st.cu[b];
+        const int k0 = u * g.ku;
+        const int nk = min(g.ku, T - k0);
+        const int ntile = (nk + kN - 1) / kN;
+        const int qs = qc % kStagesQ;
+        if (!wait_bar(ctl, smem_u32(&q_empty[qs]), ((qc / kStagesQ) & 1) ^ 1, kDevTimeoutTmaProducer)) break;
+        const uint32_t qbar = smem_u32(&q_full[qs]);
+        mbar_expect_tx(qbar, kQBytes);
+        const int qrow = ((b * g.Hkv + h) * g.MT + mt) * 128;
+        tma_load_2d(smem_u32(sQ + qs * kQBytes), &tmap_q, qbar, 0, qrow);
+        tma_load_2d(smem_u32(sQ + qs * kQBytes + kPanelQ), &tmap_q, qbar, 64, qrow);
+        ++qc;
+        const int tok0 = st.cu[b] + k0;
+        for (int t = 0; t < ntile; ++t) {
+          const int ks = kc % kStagesK;
+          if (!wait_bar(ctl, smem_u32(&k_empty[ks]), ((kc / kStagesK) & 1) ^ 1, kDevTimeoutTmaProducer)) break;
+          const uint32_t kbar = smem_u32(&k_full[ks]);
+          mbar_expect_tx(kbar, kKBytes);
+          tma_load_3d(smem_u32(sK + ks * kKBytes), &tmap_k, kbar, 0, h, tok0 + t * kN);
+          tma_load_3d(smem_u32(sK + ks * kKBytes + kPanelK), &tmap_k, kbar, 64, h, tok0 + t * kN);
+          ++kc;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t kc = 0, qc = 0, tc = 0;
+      for (int item = blockIdx.x; item < g.n_items && !*abort_flag; item += gridDim.x) {
+        const int unit = item / g.MT;
+        int b, h, u;
+        decode_unit(st, g.Hkv, unit, b, h, u);
+        const int T = st.cu[b + 1] - st.cu[b];
+        const int nk = min(g.ku, T - u * g.ku);
+        const int ntile = (nk + kN - 1) / kN;
+        const int qs = qc % kStagesQ;
+        if (!wait_bar(ctl, smem_u32(&q_full[qs]), (qc / kStagesQ) & 1, kDevTimeoutMma)) break;
+        tc_fence_after();
+        const uint32_t qaddr = smem_u32(sQ + qs * kQBytes);
+        bool ok = true;
+        for (int t = 0; t < ntile; ++t) {
+          const int ks = kc % kStagesK, ts = tc % kStagesT;
+          if (!wait_bar(ctl, smem_u32(&k_full[ks]), (kc / kStagesK) & 1, kDevTimeoutMma) ||
+              !wait_bar(ctl, smem_u32(&t_empty[ts]), ((tc / kStagesT) & 1) ^ 1, kDevTimeoutMma)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t kaddr = smem_u32(sK + ks * kKBytes);
+          const uint32_t d = tmem + ts * kN;
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk) {
+            const uint32_t off = (kk & 3) * 32;                  // 16 bf16 = 32 B inside the swizzle atom
+            const uint64_t ad = sw128_desc(qaddr + (kk >> 2) * kPanelQ + off);
+            const uint64_t bd = sw128_desc(kaddr + (kk >> 2) * kPanelK + off);
+            tc_mma(d, ad, bd, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(smem_u32(&k_empty[ks]));
+          tc_commit(smem_u32(&t_full[ts]));
+          ++kc;
+          ++tc;
+        }
+        if (!ok) break;
+        tc_commit(smem_u32(&q_empty[qs]));
+        ++qc;
+      }
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------ softmax: one window row per thread
+    const int rloc = (warp - 4) * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)((warp - 4) * 32) << 16);
+    uint32_t tc = 0;
+    for (int item = blockIdx.x; item < g.n_items && !*abort_flag; item += gridDim.x) {
+      const int unit = item / g.MT, mt = item - unit * g.MT;
+      int b, h, u;
+      decode_unit(st, g.Hkv, unit, b, h, u);
+      const int T = st.cu[b + 1] - st.cu[b];
+      const int nk = min(g.ku, T - u * g.ku);
+      const int ntile = (nk + kN - 1) / kN;
+      const int row = mt * 128 + rloc;
+      const bool write = row < g.wG;
+      const bool warp_live = mt * 128 + (warp - 4) * 32 < g.wG;     // whole warp of padding rows: no work
+      float* ubins = bins + (size_t)unit * g.cpu * g.wG + row;
+      RowState s{0.f, 0.f, 0.f, false};
+      float R = 0.f;
+      bool ok = true;
+      for (int t = 0; t < ntile; ++t) {
+        const int ts = tc % kStagesT;
+        if (!wait_bar(ctl, smem_u32(&t_full[ts]), (tc / kStagesT) & 1, kDevTimeoutEpilogue)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (warp_live) {
+          const uint32_t taddr = lane_base + ts * kN;
+          const int valid = min(kN, nk - t * kN);
+          if (t == 0) {
+            R = tile_max(taddr, valid) * g.alpha;
+            s.negR = -R;
+          }
+          const int ph = (t * kN) % C;
+          const int q = (t * kN) / C;
+          const RowState before = s;
+          tile_dispatch<C>(ph, valid < kN, taddr, g.alpha, s, ubins + (size_t)q * g.wG, g.wG, valid, write);
+          if (__any_sync(0xffffffffu, s.over)) {
+            // a value outgrew the reference: those rows move their reference to this
+            // tile's maximum, rescale what they already hold and redo the tile (the
+            // whole warp takes part because the TMEM loads are warp-collective)
+            const float tm = tile_max(taddr, valid) * g.alpha;
+            const float R2 = s.over ? fmaxf(R, tm) : R;
+            const float f = ex2(R - R2);
+            if (s.over && write)
+              for (int ch = 0; ch < q; ++ch) ubins[(size_t)ch * g.wG] *= f;
+            s = before;
+            s.l *= f;
+            s.carry *= f;
+            R = R2;
+            s.negR = -R2;
+            tile_dispatch<C>(ph, valid < kN, taddr, g.alpha, s, ubins + (size_t)q * g.wG, g.wG, valid, write);
+            s.over = false;
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(smem_u32(&t_empty[ts]));
+        ++tc;
+      }
+      if (!ok) break;
+      if (warp_live && write) {
+        // the item ended inside a chunk (last, partial chunk of the sequence)
+        if ((ntile * kN) % C != 0) {
+          const int ch = (ntile * kN) / C;
+          if (ch < g.cpu) ubins[(size_t)ch * g.wG] = s.carry;
+          s.l += s.carry;
+        }
+        rl[((size_t)unit * 2 + 0) * g.wG + row] = R;
+        rl[((size_t)unit * 2 + 1) * g.wG + row] = s.l;
+      }
+    }
+  }
+
+  // ------------------------------------------------ teardown
+  if (*abort_flag) {
+    // let copies and MMAs already in flight land before the shared memory and TMEM go away
+    const long long t0 = clock64();
+    while (clock64() - t0 < 200000) {
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+}
+
+// Packed window rows: qp[((b*Hkv + h)*MT + mt)*128 + r][e] = Q_w[b, r % w, h*G + r / w, e] for
+// rows r < w*G of the group, zero for the padding rows up to MT*128.
+__global__ void pack_q_kernel(const __nv_bfloat16* __restrict__ q, ScoreGeom g, int MT, int B,
+                              __nv_bfloat16* __restrict__ qp) {
+  const int rows_per_head = MT * 128;
+  const int64_t total_vec = (int64_t)B * g.Hkv * rows_per_head * (kD / 8);
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total_vec; i += (int64_t)gridDim.x * blockDim.x) {
+    const int vi = (int)(i % (kD / 8));
+    const int64_t row = i / (kD / 8);
+    const int r = (int)(row % rows_per_head);
+    const int64_t bh = row / rows_per_head;
+    const int h = (int)(bh % g.Hkv), b = (int)(bh / g.Hkv);
+    uint4 val = make_uint4(0, 0, 0, 0);
+    if (r < g.wG) {
+      const int gm = r / g.w, qi = r % g.w;
+      val = *(const uint4*)(q + (int64_t)b * g.q_stride_b + (int64_t)qi * g.q_stride_w +
+                            (int64_t)(h * g.G + gm) * g.q_stride_h + vi * 8);
+    }
+    *(uint4*)(qp + row * kD + vi * 8) = val;
+  }
+}
+
+// ---------------------------------------------------------------- host side
+using EncodeFn = PFN_cuTensorMapEncodeTiled_v12000;
+
+EncodeFn encode_fn() {
+  static EncodeFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &qr) ==
+            cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      fn = (EncodeFn)p;
+  });
+  return fn;
+}
+
+struct DeviceInfo {
+  int sms = 0;
+  bool attr_set[32] = {};
+};
+
+DeviceInfo& device_info(int dev) {
+  static DeviceInfo info[64];
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  DeviceInfo& d = info[dev & 63];
+  if (d.sms == 0) cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+  return d;
+}
+
+template <int C>
+cudaError_t launch_c(const TcGeom& tg, const CUtensorMap& mq, const CUtensorMap& mk, const SeqTable& st, float* rl,
+                     float* bins, int32_t* err, int slot, cudaStream_t s) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  DeviceInfo& di = device_info(dev);
+  if (!di.attr_set[slot]) {
+    e = cudaFuncSetAttribute(score_tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    di.attr_set[slot] = true;
+  }
+  const int grid = std::min(tg.n_items, 2 * di.sms);
+  score_tc_kernel<C><<<grid, kThreads, kSmemBytes, s>>>(mq, mk, tg, st, rl, bins, err);
+  return cudaGetLastError();
+}
+
+constexpr int kSupportedC[] = {3, 4, 5, 8, 10, 16, 20, 30};
+
+int c_slot(int c) {
+  for (int i = 0; i < (int)(sizeof(kSupportedC) / sizeof(int)); ++i)
+    if (kSupportedC[i] == c) return i;
+  return -1;
+}
+
+int lcm_i(int a, int b) { return a / gcd_c(a, b) * b; }
+
+}  // namespace tc
+
+bool tc_supported(const Plan& pl) {
+  return pl.elt == 2 && pl.d == tc::kD && pl.wG > 0 && tc::c_slot(pl.c) >= 0 && tc::encode_fn() != nullptr;
+}
+
+void tc_plan(Plan& pl) {
+  pl.use_tc = 0;
+  pl.tc_mt = 0;
+  if (!(pl.elt == 2 && pl.d == tc::kD && pl.wG > 0 && tc::c_slot(pl.c) >= 0)) return;
+  // Units of lcm(80, c) * m keys: whole tiles and whole chunks.  m is chosen so that
+  // the items (units x M tiles) fill the two-CTA-per-SM persistent grid evenly, with
+  // about 8 tiles (640 keys) per unit as the default size.
+  const int base = tc::lcm_i(tc::kN, pl.c);
+  const int MT = (pl.wG + 127) / 128;
+  int m = std::max(1, 640 / base);
+  pl.use_tc = 1;
+  pl.tc_mt = MT;
+  pl.cpu = base * m / pl.c;
+}
+
+cudaError_t launch_score_tc(const Plan& pl, const ScoreGeom& g, const SeqTable& st, const void* q, const void* k,
+                            float* rl, float* bins, void* qpack, int32_t* err, cudaStream_t s) {
+  tc::EncodeFn enc = tc::encode_fn();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  const int MT = pl.tc_mt;
+  const int T_total = st.cu[st.B];
+  if (g.n_units == 0 || T_total == 0) return cudaSuccess;
+  // pack the window rows of every (sequence, KV head) into zero-padded 128-row tiles
+  {
+    const int64_t total_vec = (int64_t)pl.B * pl.Hkv * MT * 128 * (tc::kD / 8);
+    const int blocks = (int)std::min<int64_t>((total_vec + 255) / 256, 4096);
+    tc::pack_q_kernel<<<blocks, 256, 0, s>>>((const __nv_bfloat16*)q, g, MT, pl.B, (__nv_bfloat16*)qpack);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  CUtensorMap mq, mk;
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)tc::kD, (cuuint64_t)pl.B * pl.Hkv * MT * 128};
+    cuuint64_t strides[1] = {(cuuint64_t)tc::kD * 2};
+    cuuint32_t box[2] = {64, 128};
+    cuuint32_t es[2] = {1, 1};
+    if (enc(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, qpack, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)tc::kD, (cuuint64_t)pl.Hkv, (cuuint64_t)T_total};
+    cuuint64_t strides[2] = {(cuuint64_t)g.kv_stride_h * 2, (cuuint64_t)g.kv_stride_t * 2};
+    cuuint32_t box[3] = {64, 1, tc::kN};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (enc(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(k), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  tc::TcGeom tg;
+  tg.Hkv = pl.Hkv;
+  tg.wG = pl.wG;
+  tg.MT = MT;
+  tg.cpu = pl.cpu;
+  tg.ku = pl.ku;
+  tg.n_items = g.n_units * MT;
+  tg.alpha = g.alpha;
+  tg.timeout = 4000000000LL;     // about two seconds of clock64 cycles per wait
+  switch (pl.c) {
+    case 3: return tc::launch_c<3>(tg, mq, mk, st, rl, bins, err, 0, s);
+    case 4: return tc::launch_c<4>(tg, mq, mk, st, rl, bins, err, 1, s);
+    case 5: return tc::launch_c<5>(tg, mq, mk, st, rl, bins, err, 2, s);
+    case 8: return tc::launch_c<8>(tg, mq, mk, st, rl, bins, err, 3, s);
+    case 10: return tc::launch_c<10>(tg, mq, mk, st, rl, bins, err, 4, s);
+    case 16: return tc::launch_c<16>(tg, mq, mk, st, rl, bins, err, 5, s);
+    case 20: return tc::launch_c<20>(tg, mq, mk, st, rl, bins, err, 6, s);
+    case 30: return tc::launch_c<30>(tg, mq, mk, st, rl, bins, err, 7, s);
+  }
   return cudaErrorNotSupported;
 }
 

@@ -23,7 +23,7 @@ def f64(t) -> np.ndarray:
 
 
 def check_scores(got: np.ndarray, want: np.ndarray, what: str = "") -> None:
-    got = np.asarray(got, dtype=np.float64)[: len(want)]
+    got = np.asarray(got[: len(want)], dtype=np.float64)
     bad = np.abs(got - want) > ATOL + RTOL * np.abs(want)
     if bad.any():
         i = int(np.argmax(bad))

@@ -215,3 +215,14 @@ def mistral_inputs():
     wl = configs.mistral_ragged()
     qs, ks, vs, spans = gen.make_all_layers(wl, DEV)
     return wl, qs, ks, vs, spans
+
+
+def test_tensor_core_path_is_selected_for_bf16_d128(ckv):
+    # the shapes of the LLaMA / Mistral / Qwen workloads run the tcgen05 kernel
+    for wl in (configs.llama_layer(), configs.llama_model(), configs.qwen_128k(),
+               configs.mistral_ragged(c=3), configs.mistral_ragged(c=30)):
+        p, keep = ckv.make_params(cu_seqlens=wl.cu_seqlens, Hq=wl.Hq, Hkv=wl.Hkv, d=wl.d, w=wl.w, c=wl.c,
+                                  L_max=wl.L_max, dtype=torch.bfloat16)
+        assert ckv.chunkkv_score_path(p) == 1, wl.name
+    p, keep = ckv.make_params(cu_seqlens=[0, 512], Hq=4, Hkv=2, d=64, w=8, c=10, L_max=128, dtype=torch.float32)
+    assert ckv.chunkkv_score_path(p) == 0
