@@ -117,6 +117,8 @@ def run_gpu(args):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     wl = configs.ALL[args.workload]()
+    if args.layers:
+        wl = wl.with_params(n_layers=args.layers, name=f"{wl.name}_first{args.layers}L")
     qs, ks, vs, _ = gen.make_all_layers(wl, dev)
     p, keep = ckv.params_for(next(q for q in qs if q is not None), ks[0], wl.cu_seqlens, Hkv=wl.Hkv, w=wl.w,
                              c=wl.c, L_max=wl.L_max)
@@ -186,7 +188,9 @@ def run_gpu(args):
     path = ckv.chunkkv_score_path(p)
     roof_peak = peaks["hbm_gbs"]
     achieved = score_bytes / (score_avg * 1e-3) / 1e9
-    launches_per_step = groups * 4          # score, finalize, select, gather per reuse group
+    # per reuse group: scoring, log-sum-exp, finalize, select, gather (+ one Q pack per step on the
+    # tensor-core path)
+    launches_per_step = groups * 5 + (1 if path == 1 else 0)
 
     # ---- end to end through the C-ABI with host buffers (pinned), copies inside the timed region
     e2e = None
@@ -333,6 +337,7 @@ def main():
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--workload", choices=sorted(configs.ALL), default="llama_model")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--layers", type=int, default=0, help="keep only the first N layers (profiling)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

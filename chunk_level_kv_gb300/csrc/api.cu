@@ -10,9 +10,10 @@ namespace chunkkv {
 
 bool tc_supported(const Plan& pl);                                  // score_tc.cu
 void tc_plan(Plan& pl);                                             // score_tc.cu
-cudaError_t launch_score_tc(const Plan& pl, const ScoreGeom& g, const SeqTable& st, const void* q,
-                            const void* k, float* rl, float* bins, void* qpack, int32_t* err,
-                            cudaStream_t s);
+cudaError_t launch_pack_q(const Plan& pl, const ScoreGeom& g, const void* const* q_layers, int n_layers,
+                          void* qpack, cudaStream_t s);
+cudaError_t launch_score_tc(const Plan& pl, const ScoreGeom& g, const SeqTable& st, const void* k, float* rl,
+                            float* bins, const void* qpack, int32_t* err, cudaStream_t s);
 
 namespace {
 
@@ -76,6 +77,31 @@ chunkkv_status make_plan(const chunkkv_params* p, int n_layers, int n_reuse, Pla
   pl.use_tc = 0;
   pl.cpu = std::max(1, 512 / p->c);
   tc_plan(pl);                                    // may switch to the tensor-core geometry
+  if (pl.use_tc) {
+    // Unit length for the persistent tensor-core grid: the multiple m of the
+    // base unit that minimises (waves of work items) x (tiles per item) on a
+    // two-CTA-per-SM GB300 (304 slots); ties go to longer units.
+    const int slots = 2 * 152;
+    const int64_t per_unit_items = (int64_t)p->Hkv * pl.tc_mt;
+    const int base_tiles = pl.tc_base_chunks * p->c / 80;
+    int64_t best_cost = INT64_MAX;
+    for (int m = 1; m <= 64; ++m) {
+      const int cpu = pl.tc_base_chunks * m;
+      int64_t items = 0;
+      for (int b = 0; b < p->B; ++b) {
+        const int T = p->cu_seqlens[b + 1] - p->cu_seqlens[b];
+        const int64_t C = ((int64_t)T + p->c - 1) / p->c;
+        items += (C + cpu - 1) / cpu * per_unit_items;
+      }
+      if (items == 0) break;
+      const int64_t cost = (items + slots - 1) / slots * (int64_t)m * base_tiles;
+      if (cost <= best_cost) {
+        best_cost = cost;
+        pl.cpu = cpu;
+      }
+      if (items <= per_unit_items) break;          // one unit per sequence already
+    }
+  }
   pl.ku = pl.cpu * p->c;
   int64_t units = 0;
   if (st) st->B = p->B;
@@ -94,15 +120,23 @@ chunkkv_status make_plan(const chunkkv_params* p, int n_layers, int n_reuse, Pla
   pl.n_units = (int32_t)(units * p->Hkv);
   const size_t rl = align_up((size_t)pl.n_units * 2 * pl.wG * sizeof(float));
   const size_t bins = align_up((size_t)pl.n_units * pl.cpu * pl.wG * sizeof(float));
-  const size_t scores = align_up((size_t)p->B * p->Hkv * C_max * sizeof(float));
-  const size_t qpack = pl.use_tc ? align_up((size_t)p->B * p->Hkv * pl.tc_mt * 128 * p->d * 2) : 0;
+  const size_t lse = align_up((size_t)p->B * p->Hkv * pl.wG * sizeof(float));
+  pl.n_groups = n_layers > 0 ? (n_layers + n_reuse - 1) / n_reuse : 1;
+  // Workspace: [header | one scratch slot per reuse group | packed window rows
+  // per group (tensor-core path) | chunk scores per group].  Every group has its
+  // own slot, so the scoring of all groups can run back to back before the
+  // (batched) log-sum-exp, finalisation, selection and gather.
   pl.off_rl = 0;
   pl.off_bins = rl;
-  pl.off_scores = rl + bins;
-  pl.off_qpack = rl + bins + scores;
-  pl.slot_bytes = rl + bins + scores + qpack;
+  pl.off_lse = rl + bins;
+  pl.slot_bytes = rl + bins + lse;
+  pl.qpack_group_bytes = pl.use_tc ? align_up((size_t)p->B * p->Hkv * pl.tc_mt * 128 * p->d * 2) : 0;
+  pl.scores_group_bytes = align_up((size_t)p->B * p->Hkv * C_max * sizeof(float));
   pl.header_bytes = kHeaderBytes;
-  (void)n_layers;
+  pl.off_slots = 0;
+  pl.off_qpack = pl.slot_bytes * pl.n_groups;
+  pl.off_scores = pl.off_qpack + pl.qpack_group_bytes * pl.n_groups;
+  pl.total_bytes = pl.header_bytes + pl.off_scores + pl.scores_group_bytes * pl.n_groups;
   return CHUNKKV_OK;
 }
 
@@ -125,24 +159,31 @@ ScoreGeom score_geom(const chunkkv_params* p, const Plan& pl) {
   g.q_stride_h = p->q_stride_h;
   g.kv_stride_t = p->kv_stride_t;
   g.kv_stride_h = p->kv_stride_h;
+  g.rl_gs = g.bins_gs = g.lse_gs = (int64_t)(pl.slot_bytes / sizeof(float));
+  g.scores_gs = (int64_t)(pl.scores_group_bytes / sizeof(float));
   return g;
 }
 
 chunkkv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? CHUNKKV_OK : CHUNKKV_ERR_CUDA; }
 
-// Scoring of one layer into `scores` through workspace slot `slot`.
-cudaError_t run_score(const chunkkv_params* p, const Plan& pl, const SeqTable& st, const void* q,
-                      const void* k, float* scores, char* ws, char* slot, cudaStream_t s) {
-  const ScoreGeom g = score_geom(p, pl);
+// Scoring kernel of one reuse group (its layer's window rows already packed at
+// qpack on the tensor-core path) into the group's scratch slot.
+cudaError_t run_score_group(const Plan& pl, const ScoreGeom& g, const SeqTable& st, const void* q, const void* k,
+                            char* slot, const void* qpack, int32_t* err, cudaStream_t s) {
   float* rl = (float*)(slot + pl.off_rl);
   float* bins = (float*)(slot + pl.off_bins);
-  cudaError_t e;
-  if (pl.use_tc)
-    e = launch_score_tc(pl, g, st, q, k, rl, bins, slot + pl.off_qpack, (int32_t*)ws, s);
-  else
-    e = launch_score_simt(pl, g, st, q, k, rl, bins, s);
+  return pl.use_tc ? launch_score_tc(pl, g, st, k, rl, bins, qpack, err, s)
+                   : launch_score_simt(pl, g, st, q, k, rl, bins, s);
+}
+
+// Log-sum-exp and finalisation of n_groups consecutive slots into their chunk scores.
+cudaError_t run_post_score(const Plan& pl, const ScoreGeom& g, const SeqTable& st, char* slots, float* scores,
+                           int n_groups, cudaStream_t s) {
+  float* rl = (float*)(slots + pl.off_rl);
+  float* lse = (float*)(slots + pl.off_lse);
+  cudaError_t e = launch_lse(g, st, rl, lse, n_groups, s);
   if (e != cudaSuccess) return e;
-  return launch_finalize(pl, g, st, rl, bins, scores, s);
+  return launch_finalize(pl, g, st, rl, (const float*)(slots + pl.off_bins), lse, scores, n_groups, s);
 }
 
 SelectGeom select_geom(const chunkkv_params* p, const Plan& pl) {
@@ -153,6 +194,9 @@ SelectGeom select_geom(const chunkkv_params* p, const Plan& pl) {
   sg.L_max = p->L_max;
   sg.C_max = pl.C_max;
   sg.n_cap = pl.n_cap;
+  sg.scores_gs = (int64_t)pl.B * pl.Hkv * pl.C_max;
+  sg.idx_gs = (int64_t)pl.B * pl.Hkv * pl.n_cap;
+  sg.cnt_gs = (int64_t)pl.B * pl.Hkv;
   return sg;
 }
 
@@ -164,18 +208,25 @@ GatherGeom gather_geom(const chunkkv_params* p, const Plan& pl) {
   gg.n_cap = pl.n_cap;
   gg.kv_stride_t = p->kv_stride_t;
   gg.kv_stride_h = p->kv_stride_h;
+  gg.n_reuse = 1;
+  gg.l0 = 0;
+  gg.idx_gs = (int64_t)pl.B * pl.Hkv * pl.n_cap;
+  gg.cnt_gs = (int64_t)pl.B * pl.Hkv;
   return gg;
 }
 
-cudaError_t run_gather(const chunkkv_params* p, const Plan& pl, const SeqTable& st, int n_layers,
+// Gather of n_layers layers; layer l uses index group l / n_reuse.
+cudaError_t run_gather(const chunkkv_params* p, const Plan& pl, const SeqTable& st, int n_layers, int n_reuse,
                        const void* const* k, const void* const* v, void* const* ko, void* const* vo,
                        const int32_t* indices, const int32_t* counts, cudaStream_t s) {
-  const GatherGeom gg = gather_geom(p, pl);
+  GatherGeom gg = gather_geom(p, pl);
+  gg.n_reuse = n_reuse;
   const int nbh = pl.B * pl.Hkv;
   const int per_launch = std::max(1, std::min(CHUNKKV_MAX_GATHER_LAYERS, 65535 / std::max(1, nbh)));
   for (int l0 = 0; l0 < n_layers; l0 += per_launch) {
     GatherArgs ga;
     ga.n_layers = std::min(per_launch, n_layers - l0);
+    gg.l0 = l0;
     for (int i = 0; i < ga.n_layers; ++i) {
       ga.k[i] = k[l0 + i];
       ga.v[i] = v[l0 + i];
@@ -222,7 +273,7 @@ chunkkv_status chunkkv_workspace_size(const chunkkv_params* p, int32_t n_layers,
   Plan pl;
   chunkkv_status s = make_plan(p, n_layers, n_reuse, pl, nullptr);
   if (s != CHUNKKV_OK) return s;
-  *bytes = pl.header_bytes + pl.slot_bytes;
+  *bytes = pl.total_bytes;
   return CHUNKKV_OK;
 }
 
@@ -242,10 +293,21 @@ chunkkv_status chunkkv_score(const chunkkv_params* p, const void* q_win, const v
   if ((pl.wG > 0 && (!q_win || !aligned16(q_win))) || !k || !chunk_scores || !ws || !aligned16(k) ||
       !aligned16(ws))
     return CHUNKKV_ERR_INVALID_ARG;
-  if (ws_bytes < pl.header_bytes + pl.slot_bytes) return CHUNKKV_ERR_WORKSPACE_TOO_SMALL;
+  if (ws_bytes < pl.total_bytes) return CHUNKKV_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t cs = (cudaStream_t)stream;
   char* w = (char*)ws;
-  return cuda_status(run_score(p, pl, st, q_win, k, chunk_scores, w, w + pl.header_bytes,
-                               (cudaStream_t)stream));
+  char* base = w + pl.header_bytes;
+  char* slot = base + pl.off_slots;
+  char* qpack = base + pl.off_qpack;
+  ScoreGeom g = score_geom(p, pl);
+  cudaError_t e = cudaSuccess;
+  if (pl.use_tc && pl.wG > 0) {
+    const void* ql[1] = {q_win};
+    e = launch_pack_q(pl, g, ql, 1, qpack, cs);
+  }
+  if (e == cudaSuccess) e = run_score_group(pl, g, st, q_win, k, slot, qpack, (int32_t*)w, cs);
+  if (e == cudaSuccess) e = run_post_score(pl, g, st, slot, chunk_scores, 1, cs);
+  return cuda_status(e);
 }
 
 chunkkv_status chunkkv_select(const chunkkv_params* p, const float* chunk_scores, int32_t* indices,
@@ -257,7 +319,7 @@ chunkkv_status chunkkv_select(const chunkkv_params* p, const float* chunk_scores
   if (pl.B * pl.Hkv == 0) return CHUNKKV_OK;
   if (!counts || (pl.C_max > 0 && !chunk_scores) || (pl.n_cap > 0 && !indices))
     return CHUNKKV_ERR_INVALID_ARG;
-  return cuda_status(launch_select(pl, select_geom(p, pl), st, chunk_scores, indices, counts,
+  return cuda_status(launch_select(pl, select_geom(p, pl), st, chunk_scores, indices, counts, 1,
                                    (cudaStream_t)stream));
 }
 
@@ -272,10 +334,11 @@ chunkkv_status chunkkv_gather(const chunkkv_params* p, int32_t n_layers, const i
   if (pl.B * pl.Hkv == 0 || pl.n_cap == 0) return CHUNKKV_OK;
   if (!indices || !counts || !k || !v || !k_out || !v_out) return CHUNKKV_ERR_INVALID_ARG;
   for (int l = 0; l < n_layers; ++l)
-    if (!aligned16(k[l]) || !aligned16(v[l]) || !aligned16(k_out[l]) || !aligned16(v_out[l]) || !k[l] ||
-        !v[l] || !k_out[l] || !v_out[l])
+    if (!k[l] || !v[l] || !k_out[l] || !v_out[l] || !aligned16(k[l]) || !aligned16(v[l]) ||
+        !aligned16(k_out[l]) || !aligned16(v_out[l]))
       return CHUNKKV_ERR_INVALID_ARG;
-  return cuda_status(run_gather(p, pl, st, n_layers, k, v, k_out, v_out, indices, counts,
+  // every layer of this call shares the one index list: group (l / n_layers) = 0
+  return cuda_status(run_gather(p, pl, st, n_layers, n_layers, k, v, k_out, v_out, indices, counts,
                                 (cudaStream_t)stream));
 }
 
@@ -300,27 +363,42 @@ chunkkv_status chunkkv_compress_layers(const chunkkv_params* p, int32_t n_layers
         !aligned16(k_out[l]) || !aligned16(v_out[l]))
       return CHUNKKV_ERR_INVALID_ARG;
   }
-  if (ws_bytes < pl.header_bytes + pl.slot_bytes) return CHUNKKV_ERR_WORKSPACE_TOO_SMALL;
+  if (ws_bytes < pl.total_bytes) return CHUNKKV_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t cs = (cudaStream_t)stream;
   char* w = (char*)ws;
-  char* slot = w + pl.header_bytes;
-  const size_t per_group_scores = (size_t)pl.B * pl.Hkv * pl.C_max;
-  const size_t per_group_idx = (size_t)pl.B * pl.Hkv * pl.n_cap;
-  const size_t per_group_cnt = (size_t)pl.B * pl.Hkv;
-  const SelectGeom sg = select_geom(p, pl);
-  for (int l0 = 0; l0 < n_layers; l0 += n_reuse) {
-    const int grp = l0 / n_reuse;
-    const int nl = std::min(n_reuse, n_layers - l0);
-    float* sc = chunk_scores ? chunk_scores + grp * per_group_scores : (float*)(slot + pl.off_scores);
-    int32_t* ix = indices ? indices + grp * per_group_idx : nullptr;
-    int32_t* ct = counts + grp * per_group_cnt;
-    cudaError_t e = run_score(p, pl, st, q_win[l0], k[l0], sc, w, slot, cs);
-    if (e == cudaSuccess) e = launch_select(pl, sg, st, sc, ix, ct, cs);
-    if (e == cudaSuccess)
-      e = run_gather(p, pl, st, nl, k + l0, v + l0, k_out + l0, v_out + l0, ix, ct, cs);
-    if (e != cudaSuccess) return CHUNKKV_ERR_CUDA;
+  char* base = w + pl.header_bytes;
+  const int n_groups = pl.n_groups;
+  ScoreGeom g = score_geom(p, pl);
+  float* scores = chunk_scores ? chunk_scores : (float*)(base + pl.off_scores);
+  if (chunk_scores) g.scores_gs = (int64_t)pl.B * pl.Hkv * pl.C_max;
+  // One stream, every launch chained by programmatic dependent launch:
+  //  1. the window rows of every scoring layer packed in one launch (tensor-core path);
+  //  2. the scoring kernel of each reuse group, back to back, each into its own slot;
+  //  3. log-sum-exp and finalisation of all groups in one launch each;
+  //  4. top-k selection and index build of every (group, sequence, head) in one launch;
+  //  5. the gather of every layer (layer l with index group l / n_reuse).
+  cudaError_t e = cudaSuccess;
+  if (pl.use_tc && pl.wG > 0) {
+    static thread_local const void* qsel[CHUNKKV_MAX_GATHER_LAYERS];
+    for (int g0 = 0; g0 < n_groups && e == cudaSuccess; g0 += CHUNKKV_MAX_GATHER_LAYERS) {
+      const int n = std::min(CHUNKKV_MAX_GATHER_LAYERS, n_groups - g0);
+      for (int i = 0; i < n; ++i) qsel[i] = q_win[(g0 + i) * n_reuse];
+      e = launch_pack_q(pl, g, qsel, n, base + pl.off_qpack + g0 * pl.qpack_group_bytes, cs);
+    }
   }
-  return CHUNKKV_OK;
+  for (int grp = 0; grp < n_groups && e == cudaSuccess; ++grp) {
+    const int l0 = grp * n_reuse;
+    e = run_score_group(pl, g, st, q_win[l0], k[l0], base + pl.off_slots + grp * pl.slot_bytes,
+                        base + pl.off_qpack + grp * pl.qpack_group_bytes, (int32_t*)w, cs);
+  }
+  if (e == cudaSuccess) e = run_post_score(pl, g, st, base + pl.off_slots, scores, n_groups, cs);
+  if (e == cudaSuccess) {
+    SelectGeom sg = select_geom(p, pl);
+    sg.scores_gs = g.scores_gs;
+    e = launch_select(pl, sg, st, scores, indices, counts, n_groups, cs);
+  }
+  if (e == cudaSuccess) e = run_gather(p, pl, st, n_layers, n_reuse, k, v, k_out, v_out, indices, counts, cs);
+  return cuda_status(e);
 }
 
 chunkkv_status chunkkv_status_check(void* ws, chunkkv_stream_t stream, int32_t* device_code) {

@@ -6,7 +6,7 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
-#include "../../include/chunkkv.h"
+#include "chunkkv.h"
 
 namespace chunkkv {
 
@@ -34,11 +34,15 @@ struct ScoreGeom {
   float alpha;        // log2(e) / sqrt(d): logits are handled as base-2 exponents
   int64_t q_stride_b, q_stride_w, q_stride_h;
   int64_t kv_stride_t, kv_stride_h;
+  // Distance (in floats) between the buffers of consecutive reuse groups, for the
+  // kernels that handle every group of a call in one launch (blockIdx.z = group).
+  int64_t rl_gs, bins_gs, lse_gs, scores_gs;
 };
 
-// Selection / index-build geometry.
+// Selection / index-build geometry (blockIdx.y = reuse group).
 struct SelectGeom {
   int32_t Hkv, c, w, L_max, C_max, n_cap;
+  int64_t scores_gs, idx_gs, cnt_gs;            // per-group strides in elements
 };
 
 // Layers moved by one gather launch.
@@ -52,7 +56,9 @@ struct GatherArgs {
 
 struct GatherGeom {
   int32_t Hkv, d, elt, n_cap;
+  int32_t n_reuse, l0;                          // layer l0 + i of a launch uses group (l0 + i) / n_reuse
   int64_t kv_stride_t, kv_stride_h;
+  int64_t idx_gs, cnt_gs;                       // per-group strides of indices / counts
 };
 
 // Device error codes written to the first word of the workspace.
@@ -61,6 +67,7 @@ enum DeviceError : int32_t {
   kDevTimeoutTmaProducer = 0x101,
   kDevTimeoutMma = 0x102,
   kDevTimeoutEpilogue = 0x103,
+  kDevMisalignedSmem = 0x201,
 };
 
 // Decode a global unit id into (b, h, u).
@@ -76,10 +83,36 @@ __device__ __forceinline__ void decode_unit(const SeqTable& st, int Hkv, int gu,
   u = ul - st.uoff[b];
 }
 
+// Programmatic dependent launch.  Every kernel of the library is launched with
+// programmatic stream serialisation: it calls pdl_wait() before it touches
+// memory that the previous kernel in the stream writes or reads, and
+// pdl_trigger() once its own work is done, so the next kernel's launch and
+// prologue overlap this kernel's drain but never take resources this kernel
+// still needs.  Both are no-ops when a kernel is launched without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ float to_float(float x) { return x; }
 __device__ __forceinline__ float to_float(__nv_bfloat16 x) { return __bfloat162float(x); }
 
 // ----------------------------------------------------------------- host side
+
+// Launch with programmatic stream serialisation (see pdl_wait / pdl_trigger).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
 
 // Workspace plan shared by the C-ABI entry points and the launchers.
 struct Plan {
@@ -88,18 +121,26 @@ struct Plan {
   int32_t cpu, ku, n_units;
   int32_t use_tc;                 // tensor-core scoring kernel
   int32_t tc_mt;                  // 128-row M tiles of the window rows (tensor-core path)
-  size_t slot_bytes;              // one scoring slot
-  size_t off_rl, off_bins, off_scores, off_qpack;   // inside a slot
+  int32_t tc_base_chunks;         // chunks in the smallest whole-tile unit (tensor-core path)
+  int32_t n_groups;               // reuse groups of the call (scoring layers)
+  size_t slot_bytes;              // one group's scratch: rl, bins, lse
+  size_t off_rl, off_bins, off_lse;                 // inside a slot
+  size_t off_slots, off_qpack, off_scores;          // regions of the workspace (after the header)
+  size_t scores_group_bytes;                        // one group's chunk scores (scores region holds all)
+  size_t qpack_group_bytes;                         // one layer's packed window rows (tensor-core path)
   size_t header_bytes;
+  size_t total_bytes;
 };
 
 // Launchers (defined in the kernel translation units).
 cudaError_t launch_score_simt(const Plan& pl, const ScoreGeom& g, const SeqTable& st, const void* q,
                               const void* k, float* rl, float* bins, cudaStream_t s);
 cudaError_t launch_finalize(const Plan& pl, const ScoreGeom& g, const SeqTable& st, float* rl,
-                            const float* bins, float* scores, cudaStream_t s);
+                            const float* bins, const float* lse, float* scores, int n_groups, cudaStream_t s);
+cudaError_t launch_lse(const ScoreGeom& g, const SeqTable& st, const float* rl, float* lse, int n_groups,
+                       cudaStream_t s);
 cudaError_t launch_select(const Plan& pl, const SelectGeom& sg, const SeqTable& st, const float* scores,
-                          int32_t* indices, int32_t* counts, cudaStream_t s);
+                          int32_t* indices, int32_t* counts, int n_groups, cudaStream_t s);
 cudaError_t launch_gather(const Plan& pl, const GatherGeom& gg, const SeqTable& st, const GatherArgs& ga,
                           const int32_t* indices, const int32_t* counts, cudaStream_t s);
 

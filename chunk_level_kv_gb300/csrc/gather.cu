@@ -35,6 +35,10 @@ gather_kernel(GatherGeom gg, const __grid_constant__ SeqTable st, const __grid_c
   const int layer = y / nbh;
   const int bh = y - layer * nbh;
   const int b = bh / gg.Hkv, h = bh - b * gg.Hkv;
+  const int grp = (gg.l0 + layer) / gg.n_reuse;          // the index list this layer uses
+  indices += grp * gg.idx_gs;
+  counts += grp * gg.cnt_gs;
+  pdl_wait();
   const int cnt = min(max(counts[bh], 0), gg.n_cap);     // never beyond the output rows
   const int T = st.cu[b + 1] - st.cu[b];
   const int vpr_shift = __ffs(gg.d * gg.elt / 16) - 1;        // vectors per row (a power of two)
@@ -72,6 +76,7 @@ gather_kernel(GatherGeom gg, const __grid_constant__ SeqTable st, const __grid_c
       }
     }
   }
+  pdl_trigger();
 }
 
 // Portable variant for row sizes that are not a power-of-two number of vectors.
@@ -82,6 +87,10 @@ gather_any_kernel(GatherGeom gg, const __grid_constant__ SeqTable st, const __gr
   const int layer = blockIdx.y / nbh;
   const int bh = blockIdx.y - layer * nbh;
   const int b = bh / gg.Hkv, h = bh - b * gg.Hkv;
+  const int grp = (gg.l0 + layer) / gg.n_reuse;
+  indices += grp * gg.idx_gs;
+  counts += grp * gg.cnt_gs;
+  pdl_wait();
   const int vpr = gg.d * gg.elt / 16;
   const int T = st.cu[b + 1] - st.cu[b];
   const int total = T > 0 ? min(max(counts[bh], 0), gg.n_cap) * vpr : 0;
@@ -96,6 +105,7 @@ gather_any_kernel(GatherGeom gg, const __grid_constant__ SeqTable st, const __gr
     ko[slot] = ld_stream((const uint4*)((const char*)ga.k[layer] + off) + vi);
     vo[slot] = ld_stream((const uint4*)((const char*)ga.v[layer] + off) + vi);
   }
+  pdl_trigger();
 }
 
 cudaError_t launch_gather(const Plan& pl, const GatherGeom& gg, const SeqTable& st, const GatherArgs& ga,
@@ -109,11 +119,8 @@ cudaError_t launch_gather(const Plan& pl, const GatherGeom& gg, const SeqTable& 
   int gx = (int)((slots + per_block - 1) / per_block);
   if (gx < 1) gx = 1;
   dim3 grid(gx, nbh * ga.n_layers);
-  if (pow2)
-    gather_kernel<<<grid, kGatherThreads, 0, s>>>(gg, st, ga, indices, counts);
-  else
-    gather_any_kernel<<<grid, kGatherThreads, 0, s>>>(gg, st, ga, indices, counts);
-  return cudaGetLastError();
+  if (pow2) return launch_pdl(gather_kernel, grid, dim3(kGatherThreads), 0, s, gg, st, ga, indices, counts);
+  return launch_pdl(gather_any_kernel, grid, dim3(kGatherThreads), 0, s, gg, st, ga, indices, counts);
 }
 
 }  // namespace chunkkv

@@ -43,6 +43,7 @@ score_simt_kernel(const E* __restrict__ q, const E* __restrict__ k, ScoreGeom g,
   const int nk = min(g.ku, T - k0);
   const E* kbase = k + (int64_t)(st.cu[b] + k0) * g.kv_stride_t + (int64_t)h * g.kv_stride_h;
   const int tid = threadIdx.x;
+  pdl_wait();
 
   for (int rb = 0; rb < g.wG; rb += kSimtRows) {
     __syncthreads();
@@ -114,6 +115,7 @@ score_simt_kernel(const E* __restrict__ q, const E* __restrict__ k, ScoreGeom g,
       rl[((int64_t)gu * 2 + 1) * g.wG + r] = l;
     }
   }
+  pdl_trigger();
 }
 
 cudaError_t launch_score_simt(const Plan& pl, const ScoreGeom& g, const SeqTable& st, const void* q,
@@ -125,14 +127,16 @@ cudaError_t launch_score_simt(const Plan& pl, const ScoreGeom& g, const SeqTable
     e = cudaFuncSetAttribute(score_simt_kernel<__nv_bfloat16>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    score_simt_kernel<__nv_bfloat16><<<g.n_units, kSimtRows, smem, s>>>(
-        (const __nv_bfloat16*)q, (const __nv_bfloat16*)k, g, st, rl, bins);
+    e = launch_pdl(score_simt_kernel<__nv_bfloat16>, dim3(g.n_units), dim3(kSimtRows), smem, s,
+                   (const __nv_bfloat16*)q, (const __nv_bfloat16*)k, g, st, rl, bins);
+    if (e != cudaSuccess) return e;
   } else {
     e = cudaFuncSetAttribute(score_simt_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
     if (e != cudaSuccess) return e;
-    score_simt_kernel<float><<<g.n_units, kSimtRows, smem, s>>>((const float*)q, (const float*)k, g,
-                                                               st, rl, bins);
+    e = launch_pdl(score_simt_kernel<float>, dim3(g.n_units), dim3(kSimtRows), smem, s, (const float*)q,
+                   (const float*)k, g, st, rl, bins);
+    if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }
@@ -142,70 +146,161 @@ cudaError_t launch_score_simt(const Plan& pl, const ScoreGeom& g, const SeqTable
 // same (sequence, head); the unit's bins are then weighted by 2^(R_r - lse_r)
 // and summed over rows, one warp per chunk (coalesced over rows).
 constexpr int kFinThreads = 256;
+constexpr int kFinChunks = 32;                  // chunks per CTA: blockIdx.y tiles a unit
 
 __global__ void __launch_bounds__(kFinThreads)
 finalize_kernel(ScoreGeom g, const __grid_constant__ SeqTable st, const float* __restrict__ rl,
-                const float* __restrict__ bins, float* __restrict__ scores) {
+                const float* __restrict__ bins, const float* __restrict__ lse_rows, int lse_stride,
+                float* __restrict__ scores) {
   extern __shared__ float wts[];                // [wG]
   int b, h, u;
   const int gu = blockIdx.x;
+  const int cb = blockIdx.y * kFinChunks;       // this CTA's block of the unit's chunks
+  rl += blockIdx.z * g.rl_gs;                   // this CTA's reuse group
+  bins += blockIdx.z * g.bins_gs;
+  if (lse_rows != nullptr) lse_rows += blockIdx.z * g.lse_gs;
+  scores += blockIdx.z * g.scores_gs;
+  pdl_wait();
   decode_unit(st, g.Hkv, gu, b, h, u);
   const int T = st.cu[b + 1] - st.cu[b];
   const int C = (T + g.c - 1) / g.c;
+  if (min(g.cpu, C - u * g.cpu) <= cb) return;  // no chunk of this unit in this block
   const int U = st.uoff[b + 1] - st.uoff[b];
   const int64_t stride_u = (int64_t)g.Hkv * 2 * g.wG;          // between units of one head
   const float* rl_head = rl + ((int64_t)st.uoff[b] * g.Hkv + h) * 2 * g.wG;
 
   for (int r = threadIdx.x; r < g.wG; r += blockDim.x) {
-    float M = -INFINITY;
-    for (int v = 0; v < U; ++v) M = fmaxf(M, rl_head[v * stride_u + r]);
-    float S = 0.f;
-    for (int v = 0; v < U; ++v) S += rl_head[v * stride_u + g.wG + r] * exp2f(rl_head[v * stride_u + r] - M);
-    const float lse = M + log2f(S);
+    float lse;
+    if (lse_rows != nullptr) {                      // formed by the scoring kernel
+      lse = lse_rows[((int64_t)b * g.Hkv + h) * lse_stride + r];
+    } else {
+      float M = -INFINITY;
+      for (int v = 0; v < U; ++v) M = fmaxf(M, rl_head[v * stride_u + r]);
+      float S = 0.f;
+      for (int v = 0; v < U; ++v) S += rl_head[v * stride_u + g.wG + r] * exp2f(rl_head[v * stride_u + r] - M);
+      lse = M + log2f(S);
+    }
     wts[r] = exp2f(rl[(int64_t)gu * 2 * g.wG + r] - lse);
   }
   __syncthreads();
 
-  const int nc = min(g.cpu, C - u * g.cpu);
+  const int nc = min(min(g.cpu, C - u * g.cpu) - cb, kFinChunks);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const float* ub = bins + (int64_t)gu * g.cpu * g.wG;
-  float* out = scores + ((int64_t)b * g.Hkv + h) * g.C_max + (int64_t)u * g.cpu;
-  for (int ch = warp; ch < nc; ch += kFinThreads / 32) {
-    float acc = 0.f;
-    for (int r = lane; r < g.wG; r += 32) acc = fmaf(ub[(int64_t)ch * g.wG + r], wts[r], acc);
+  const float* ub = bins + ((int64_t)gu * g.cpu + cb) * g.wG;
+  float* out = scores + ((int64_t)b * g.Hkv + h) * g.C_max + (int64_t)u * g.cpu + cb;
+  // each warp sums four chunks at a time: four independent load streams per lane
+  constexpr int kW = kFinThreads / 32;
+  for (int ch0 = warp * 4; ch0 < nc; ch0 += kW * 4) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    const int m = min(4, nc - ch0);
+    for (int r = lane; r < g.wG; r += 32) {
+      const float wr = wts[r];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) out[ch] = acc;
+      for (int i = 0; i < 4; ++i)
+        if (i < m) acc[i] = fmaf(__ldcs(ub + (int64_t)(ch0 + i) * g.wG + r), wr, acc[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float a = acc[i];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+      if (lane == 0 && i < m) out[ch0 + i] = a;
+    }
   }
+  pdl_trigger();
+}
+
+// Row log-sum-exp (base 2) of every (sequence, head) from the per-unit (R, l)
+// pairs: lse_r = M + log2(sum_u l_u 2^(R_u - M)), M = max_u R_u.  One CTA per
+// (sequence, head, 32 rows): lane = row (128-byte loads), the 32 warps take every
+// 32nd unit, four units per step with their loads issued together, and the
+// partial (M, S) pairs are merged through shared memory.
+constexpr int kLseThreads = 1024;
+
+__device__ __forceinline__ void lse_merge(float& M, float& S, float Mv, float Sv) {
+  if (Sv == 0.f) return;
+  const float Mn = fmaxf(M, Mv);
+  S = S * exp2f(M - Mn) + Sv * exp2f(Mv - Mn);
+  M = Mn;
+}
+
+__global__ void __launch_bounds__(kLseThreads)
+lse_kernel(ScoreGeom g, const __grid_constant__ SeqTable st, const float* __restrict__ rl,
+           float* __restrict__ lse) {
+  constexpr int W = kLseThreads / 32;
+  __shared__ float shM[W][32], shS[W][32];
+  const int bh = blockIdx.x;
+  const int b = bh / g.Hkv, h = bh - b * g.Hkv;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int r = blockIdx.y * 32 + lane;
+  const int U = st.uoff[b + 1] - st.uoff[b];
+  rl += blockIdx.z * g.rl_gs;                   // this CTA's reuse group
+  lse += blockIdx.z * g.lse_gs;
+  pdl_wait();
+  const int64_t ustride = (int64_t)g.Hkv * 2 * g.wG;
+  const float* base = rl + ((int64_t)st.uoff[b] * g.Hkv + h) * 2 * g.wG + r;
+  float M = -INFINITY, S = 0.f;
+  if (r < g.wG) {
+    int v = warp;
+    for (; v + 3 * W < U; v += 4 * W) {
+      float Rv[4], lv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        Rv[i] = base[(v + i * W) * ustride];
+        lv[i] = base[(v + i * W) * ustride + g.wG];
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) lse_merge(M, S, Rv[i], lv[i]);
+    }
+    for (; v < U; v += W) lse_merge(M, S, base[v * ustride], base[v * ustride + g.wG]);
+  }
+  shM[warp][lane] = M;
+  shS[warp][lane] = S;
+  __syncthreads();
+  if (warp == 0 && r < g.wG) {
+    float Mt = -INFINITY, St = 0.f;
+    for (int w2 = 0; w2 < W; ++w2) lse_merge(Mt, St, shM[w2][lane], shS[w2][lane]);
+    lse[(int64_t)bh * g.wG + r] = Mt + log2f(St);
+  }
+  pdl_trigger();
+}
+
+cudaError_t launch_lse(const ScoreGeom& g, const SeqTable& st, const float* rl, float* lse, int n_groups,
+                       cudaStream_t s) {
+  if (g.n_units == 0 || g.wG == 0 || n_groups == 0) return cudaSuccess;
+  dim3 grid(st.B * g.Hkv, (g.wG + 31) / 32, n_groups);
+  return launch_pdl(lse_kernel, grid, dim3(kLseThreads), 0, s, g, st, rl, lse);
 }
 
 // Scores of a head with no window rows are all zero (no attention mass).
 __global__ void zero_scores_kernel(ScoreGeom g, const __grid_constant__ SeqTable st, float* scores) {
   int b, h, u;
+  scores += blockIdx.z * g.scores_gs;
+  pdl_wait();
   decode_unit(st, g.Hkv, blockIdx.x, b, h, u);
   const int T = st.cu[b + 1] - st.cu[b];
   const int C = (T + g.c - 1) / g.c;
   const int nc = min(g.cpu, C - u * g.cpu);
   float* out = scores + ((int64_t)b * g.Hkv + h) * g.C_max + (int64_t)u * g.cpu;
   for (int ch = threadIdx.x; ch < nc; ch += blockDim.x) out[ch] = 0.f;
+  pdl_trigger();
 }
 
 cudaError_t launch_finalize(const Plan& pl, const ScoreGeom& g, const SeqTable& st, float* rl,
-                            const float* bins, float* scores, cudaStream_t s) {
+                            const float* bins, const float* lse, float* scores, int n_groups, cudaStream_t s) {
   (void)pl;
-  if (g.n_units == 0) return cudaSuccess;
-  if (g.wG == 0) {
-    zero_scores_kernel<<<g.n_units, 128, 0, s>>>(g, st, scores);
-    return cudaGetLastError();
-  }
+  if (g.n_units == 0 || n_groups == 0) return cudaSuccess;
+  if (g.wG == 0)
+    return launch_pdl(zero_scores_kernel, dim3(g.n_units, 1, n_groups), dim3(128), 0, s, g, st, scores);
   const size_t smem = (size_t)g.wG * sizeof(float);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(finalize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
   }
-  finalize_kernel<<<g.n_units, kFinThreads, smem, s>>>(g, st, rl, bins, scores);
-  return cudaGetLastError();
+  dim3 grid(g.n_units, (g.cpu + kFinChunks - 1) / kFinChunks, n_groups);
+  return launch_pdl(finalize_kernel, grid, dim3(kFinThreads), smem, s, g, st, (const float*)rl, bins, lse,
+                    (int)g.wG, scores);
 }
 
 }  // namespace chunkkv

@@ -115,10 +115,11 @@ extern "C" chunkkv_status chunkkv_score_noalloc(const chunkkv_params* p, const v
   g.q_stride_h = p->q_stride_h;
   g.kv_stride_t = p->kv_stride_t;
   g.kv_stride_h = p->kv_stride_h;
+  g.rl_gs = g.bins_gs = g.lse_gs = g.scores_gs = 0;      // a single group
   float* rl = (float*)base;
   float* bins = (float*)((char*)base + rl_bytes);
   cudaStream_t cs = (cudaStream_t)stream;
   cudaError_t e = launch_score_simt(pl, g, st, q_win, k, rl, bins, cs);
-  if (e == cudaSuccess) e = launch_finalize(pl, g, st, rl, bins, chunk_scores, cs);
+  if (e == cudaSuccess) e = launch_finalize(pl, g, st, rl, bins, nullptr, chunk_scores, 1, cs);
   return e == cudaSuccess ? CHUNKKV_OK : CHUNKKV_ERR_CUDA;
 }

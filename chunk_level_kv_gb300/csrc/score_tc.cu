@@ -31,16 +31,19 @@ namespace tc {
 
 constexpr int kN = 80;                         // keys per tile (MMA N)
 constexpr int kD = 128;                        // head dimension
-constexpr int kStagesK = 2;                    // K tiles in shared memory
-constexpr int kStagesQ = 2;                    // Q tiles in shared memory
+constexpr int kStagesK = 4;                    // K tiles in shared memory
+constexpr int kStagesQ = 1;                    // Q tile in shared memory (reused across items)
 constexpr int kStagesT = 3;                    // accumulator stages in TMEM (3 x 80 columns)
 constexpr int kTmemCols = 256;
-constexpr int kThreads = 256;
+constexpr int kThreads = 192;                  // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
 constexpr int kPanelQ = 128 * 128;             // one 64-element (128 B) panel of 128 rows
 constexpr int kPanelK = kN * 128;              // one 128 B panel of 80 key rows
 constexpr int kQBytes = 2 * kPanelQ;           // 32 KB per Q tile
 constexpr int kKBytes = 2 * kPanelK;           // 20 KB per K tile
-constexpr int kSmemBytes = 1024 + kStagesQ * kQBytes + kStagesK * kKBytes + 256;
+// The dynamic shared window starts 1024-byte aligned (no static shared memory);
+// the kernel checks this and reports an error instead of computing on a
+// misaligned swizzle pattern.
+constexpr int kSmemBytes = kStagesQ * kQBytes + kStagesK * kKBytes + 256;
 constexpr uint32_t kIdesc = (1u << 4)                         // D = fp32
                           | (1u << 7) | (1u << 10)           // A = B = bf16
                           | ((uint32_t)(kN >> 3) << 17)      // N
@@ -83,6 +86,29 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
       "[%2];" ::"r"(dst), "l"((uint64_t)map), "r"(bar), "r"(c0), "r"(c1), "r"(c2) : "memory");
+}
+
+// Same as tma_load_3d with an L2 eviction-priority policy (createpolicy) attached.
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
+                                                 int c2, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1, {%3, %4, %5}], [%2], %6;"
+      ::"r"(dst), "l"((uint64_t)map), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "l"(policy) : "memory");
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+// A bin store that asks L2 to keep the line: the finalisation reads it back soon.
+__device__ __forceinline__ void st_keep(float* ptr, float v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(ptr), "f"(v), "l"(policy) : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -157,70 +183,85 @@ __device__ __forceinline__ bool wait_bar(const Ctl& ctl, uint32_t bar, uint32_t 
 // ---------------------------------------------------------------- softmax side
 // Per-row state of the item being processed.
 struct RowState {
-  float negR;      // -(reference exponent)
+  float2 negR;     // -(reference exponent), twice (packed operand)
+  float2 carry;    // partial sum (two lanes) of a chunk that continues into the next tile
   float l;         // sum of 2^(t - R) over the item's keys so far
-  float carry;     // partial sum of a chunk that continues into the next tile
-  bool over;       // some chunk exceeded kBig (rescale needed)
 };
 
 // Segment SEG (columns 16*SEG .. 16*SEG+15) of a tile whose column 0 has phase PH
-// inside its chunk.  bin points at bins[(gu*cpu + q)*wG + row], q being the
-// unit-local chunk that holds the tile's column 0.
+// inside its chunk.  Columns are taken in pairs: one packed FMA forms both base-2
+// exponents, two MUFU ex2 evaluate them and one packed add accumulates them; the
+// pair's two lanes are folded when a chunk ends (compile-time positions).  bin
+// points at bins[(gu*cpu + q)*wG + row], q being the unit-local chunk that holds
+// the tile's column 0.
 template <int C, int PH, int SEG, bool MASK>
-__device__ __forceinline__ void tile_seg(const uint32_t (&r)[16], float alpha, RowState& s, float* bin, int wG,
-                                         int valid, bool write) {
-  float acc = s.carry;
+__device__ __forceinline__ void tile_seg(const uint32_t (&r)[16], float2 alpha2, RowState& s, float* bin, int wG,
+                                         int valid, bool write, uint64_t pol) {
+  static_assert(C >= 2, "pairs hold at most one chunk end");
+  float2 acc = s.carry;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const int col = SEG * 16 + i;
-    float e = ex2(fmaf(__uint_as_float(r[i]), alpha, s.negR));
-    if (MASK) e = (col < valid) ? e : 0.f;
-    acc += e;
-    if ((PH + col + 1) % C == 0) {
-      const int chunk = (PH + col + 1) / C - 1;
-      s.over |= !(acc <= kBig);
-      if (write) bin[(size_t)chunk * wG] = acc;
-      s.l += acc;
-      acc = 0.f;
+  for (int p = 0; p < 8; ++p) {
+    const int c0 = SEG * 16 + 2 * p;
+    const float2 x = make_float2(__uint_as_float(r[2 * p]), __uint_as_float(r[2 * p + 1]));
+    const float2 t = __ffma2_rn(x, alpha2, s.negR);
+    float2 e = make_float2(ex2(t.x), ex2(t.y));
+    if (MASK) {
+      e.x = (c0 < valid) ? e.x : 0.f;
+      e.y = (c0 + 1 < valid) ? e.y : 0.f;
+    }
+    if ((PH + c0 + 1) % C == 0) {               // a chunk ends at the pair's first column
+      const float bsum = (acc.x + acc.y) + e.x;
+      if (write) st_keep(bin + (size_t)((PH + c0 + 1) / C - 1) * wG, bsum, pol);
+      s.l += bsum;
+      acc = make_float2(0.f, e.y);
+    } else if ((PH + c0 + 2) % C == 0) {        // a chunk ends at the pair's second column
+      acc = __fadd2_rn(acc, e);
+      const float bsum = acc.x + acc.y;
+      if (write) st_keep(bin + (size_t)((PH + c0 + 2) / C - 1) * wG, bsum, pol);
+      s.l += bsum;
+      acc = make_float2(0.f, 0.f);
+    } else {
+      acc = __fadd2_rn(acc, e);
     }
   }
   s.carry = acc;
 }
 
-// One 80-column tile: five 16-column TMEM loads, each issued while the previous
-// segment is being processed.
+// One 80-column tile: the whole row segment is loaded from TMEM first (five
+// x16 loads, one wait), so the 40 column pairs are independent work that the
+// scheduler can interleave freely.
 template <int C, int PH, bool MASK>
-__device__ __forceinline__ void tile_phase(uint32_t taddr, float alpha, RowState& s, float* bin, int wG, int valid,
-                                           bool write) {
-  uint32_t a[16], b[16];
+__device__ __forceinline__ void tile_phase(uint32_t taddr, float2 alpha, RowState& s, float* bin, int wG, int valid,
+                                           bool write, uint64_t pol) {
+  uint32_t a[16], b[16], c[16], d[16], e[16];
   tmem_ld16(taddr, a);
-  tmem_wait16(a);
   tmem_ld16(taddr + 16, b);
-  tile_seg<C, PH, 0, MASK>(a, alpha, s, bin, wG, valid, write);
-  tmem_wait16(b);
-  tmem_ld16(taddr + 32, a);
-  tile_seg<C, PH, 1, MASK>(b, alpha, s, bin, wG, valid, write);
+  tmem_ld16(taddr + 32, c);
+  tmem_ld16(taddr + 48, d);
+  tmem_ld16(taddr + 64, e);
   tmem_wait16(a);
-  tmem_ld16(taddr + 48, b);
-  tile_seg<C, PH, 2, MASK>(a, alpha, s, bin, wG, valid, write);
   tmem_wait16(b);
-  tmem_ld16(taddr + 64, a);
-  tile_seg<C, PH, 3, MASK>(b, alpha, s, bin, wG, valid, write);
-  tmem_wait16(a);
-  tile_seg<C, PH, 4, MASK>(a, alpha, s, bin, wG, valid, write);
+  tmem_wait16(c);
+  tmem_wait16(d);
+  tmem_wait16(e);
+  tile_seg<C, PH, 0, MASK>(a, alpha, s, bin, wG, valid, write, pol);
+  tile_seg<C, PH, 1, MASK>(b, alpha, s, bin, wG, valid, write, pol);
+  tile_seg<C, PH, 2, MASK>(c, alpha, s, bin, wG, valid, write, pol);
+  tile_seg<C, PH, 3, MASK>(d, alpha, s, bin, wG, valid, write, pol);
+  tile_seg<C, PH, 4, MASK>(e, alpha, s, bin, wG, valid, write, pol);
 }
 
 template <int C, int PH = 0>
-__device__ __forceinline__ void tile_dispatch(int ph, bool mask, uint32_t taddr, float alpha, RowState& s, float* bin,
-                                              int wG, int valid, bool write) {
+__device__ __forceinline__ void tile_dispatch(int ph, bool mask, uint32_t taddr, float2 alpha, RowState& s, float* bin,
+                                              int wG, int valid, bool write, uint64_t pol) {
   if constexpr (PH < C) {
     if (ph == PH) {
       if (mask)
-        tile_phase<C, PH, true>(taddr, alpha, s, bin, wG, valid, write);
+        tile_phase<C, PH, true>(taddr, alpha, s, bin, wG, valid, write, pol);
       else
-        tile_phase<C, PH, false>(taddr, alpha, s, bin, wG, valid, write);
+        tile_phase<C, PH, false>(taddr, alpha, s, bin, wG, valid, write, pol);
     } else {
-      tile_dispatch<C, PH + gcd_c(kN, C)>(ph, mask, taddr, alpha, s, bin, wG, valid, write);
+      tile_dispatch<C, PH + gcd_c(kN, C)>(ph, mask, taddr, alpha, s, bin, wG, valid, write, pol);
     }
   }
 }
@@ -246,7 +287,11 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 const __grid_constant__ SeqTable st, float* __restrict__ rl, float* __restrict__ bins,
                 int32_t* __restrict__ err) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* smem = smem_raw;
+  if (smem_u32(smem_raw) & 1023u) {                         // swizzled tiles need 1024-byte alignment
+    if (threadIdx.x == 0) atomicCAS(err, 0, (int)kDevMisalignedSmem);
+    return;
+  }
   uint8_t* sQ = smem;                                          // kStagesQ x 32 KB
   uint8_t* sK = smem + kStagesQ * kQBytes;                     // kStagesK x 20 KB
   uint64_t* bars = (uint64_t*)(sK + kStagesK * kKBytes);
@@ -284,6 +329,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
       uint32_t kc = 0, qc = 0;
+      int qkey = -1;                                   // (sequence, head, M tile) of the loaded Q
+      const uint64_t kpol = policy_evict_first();      // keys are streamed once per M tile
       for (int item = blockIdx.x; item < g.n_items && !*abort_flag; item += gridDim.x) {
         const int unit = item / g.MT, mt = item - unit * g.MT;
         int b, h, u;
@@ -292,22 +339,25 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         const int k0 = u * g.ku;
         const int nk = min(g.ku, T - k0);
         const int ntile = (nk + kN - 1) / kN;
-        const int qs = qc % kStagesQ;
-        if (!wait_bar(ctl, smem_u32(&q_empty[qs]), ((qc / kStagesQ) & 1) ^ 1, kDevTimeoutTmaProducer)) break;
-        const uint32_t qbar = smem_u32(&q_full[qs]);
-        mbar_expect_tx(qbar, kQBytes);
-        const int qrow = ((b * g.Hkv + h) * g.MT + mt) * 128;
-        tma_load_2d(smem_u32(sQ + qs * kQBytes), &tmap_q, qbar, 0, qrow);
-        tma_load_2d(smem_u32(sQ + qs * kQBytes + kPanelQ), &tmap_q, qbar, 64, qrow);
-        ++qc;
+        const int key = (b * g.Hkv + h) * g.MT + mt;
+        if (key != qkey) {
+          // a new window-row tile: wait until the MMAs that read the old one are done
+          if (!wait_bar(ctl, smem_u32(&q_empty[0]), (qc & 1) ^ 1, kDevTimeoutTmaProducer)) break;
+          const uint32_t qbar = smem_u32(&q_full[0]);
+          mbar_expect_tx(qbar, kQBytes);
+          tma_load_2d(smem_u32(sQ), &tmap_q, qbar, 0, key * 128);
+          tma_load_2d(smem_u32(sQ + kPanelQ), &tmap_q, qbar, 64, key * 128);
+          ++qc;
+          qkey = key;
+        }
         const int tok0 = st.cu[b] + k0;
         for (int t = 0; t < ntile; ++t) {
           const int ks = kc % kStagesK;
           if (!wait_bar(ctl, smem_u32(&k_empty[ks]), ((kc / kStagesK) & 1) ^ 1, kDevTimeoutTmaProducer)) break;
           const uint32_t kbar = smem_u32(&k_full[ks]);
           mbar_expect_tx(kbar, kKBytes);
-          tma_load_3d(smem_u32(sK + ks * kKBytes), &tmap_k, kbar, 0, h, tok0 + t * kN);
-          tma_load_3d(smem_u32(sK + ks * kKBytes + kPanelK), &tmap_k, kbar, 64, h, tok0 + t * kN);
+          tma_load_3d_hint(smem_u32(sK + ks * kKBytes), &tmap_k, kbar, 0, h, tok0 + t * kN, kpol);
+          tma_load_3d_hint(smem_u32(sK + ks * kKBytes + kPanelK), &tmap_k, kbar, 64, h, tok0 + t * kN, kpol);
           ++kc;
         }
       }
@@ -316,17 +366,23 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
       uint32_t kc = 0, qc = 0, tc = 0;
+      int qkey = -1;
+      const uint32_t qaddr = smem_u32(sQ);
       for (int item = blockIdx.x; item < g.n_items && !*abort_flag; item += gridDim.x) {
-        const int unit = item / g.MT;
+        const int unit = item / g.MT, mt = item - unit * g.MT;
         int b, h, u;
         decode_unit(st, g.Hkv, unit, b, h, u);
         const int T = st.cu[b + 1] - st.cu[b];
         const int nk = min(g.ku, T - u * g.ku);
         const int ntile = (nk + kN - 1) / kN;
-        const int qs = qc % kStagesQ;
-        if (!wait_bar(ctl, smem_u32(&q_full[qs]), (qc / kStagesQ) & 1, kDevTimeoutMma)) break;
-        tc_fence_after();
-        const uint32_t qaddr = smem_u32(sQ + qs * kQBytes);
+        const int key = (b * g.Hkv + h) * g.MT + mt;
+        if (key != qkey) {
+          if (qkey >= 0) tc_commit(smem_u32(&q_empty[0]));     // old Q free once its MMAs finish
+          if (!wait_bar(ctl, smem_u32(&q_full[0]), qc & 1, kDevTimeoutMma)) break;
+          tc_fence_after();
+          ++qc;
+          qkey = key;
+        }
         bool ok = true;
         for (int t = 0; t < ntile; ++t) {
           const int ks = kc % kStagesK, ts = tc % kStagesT;
@@ -351,14 +407,16 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
           ++tc;
         }
         if (!ok) break;
-        tc_commit(smem_u32(&q_empty[qs]));
-        ++qc;
       }
     }
-  } else if (warp >= 4) {
+  } else {
     // ------------------------------------------------ softmax: one window row per thread
-    const int rloc = (warp - 4) * 32 + lane;
-    const uint32_t lane_base = tmem + ((uint32_t)((warp - 4) * 32) << 16);
+    // warps 2..5 cover the four TMEM lane groups (a warp reads lanes 32*(warp%4)..+31)
+    const int lg = warp & 3;
+    const int rloc = lg * 32 + lane;
+    const uint64_t bpol = policy_evict_last();       // bins are read back by the finalisation
+    pdl_wait();                                      // previous kernel of the stream done (and its writes visible)
+    const uint32_t lane_base = tmem + ((uint32_t)(lg * 32) << 16);
     uint32_t tc = 0;
     for (int item = blockIdx.x; item < g.n_items && !*abort_flag; item += gridDim.x) {
       const int unit = item / g.MT, mt = item - unit * g.MT;
@@ -369,9 +427,10 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
       const int ntile = (nk + kN - 1) / kN;
       const int row = mt * 128 + rloc;
       const bool write = row < g.wG;
-      const bool warp_live = mt * 128 + (warp - 4) * 32 < g.wG;     // whole warp of padding rows: no work
+      const bool warp_live = mt * 128 + lg * 32 < g.wG;            // whole warp of padding rows: no work
       float* ubins = bins + (size_t)unit * g.cpu * g.wG + row;
-      RowState s{0.f, 0.f, 0.f, false};
+      RowState s{make_float2(0.f, 0.f), make_float2(0.f, 0.f), 0.f};
+      const float2 alpha2 = make_float2(g.alpha, g.alpha);
       float R = 0.f;
       bool ok = true;
       for (int t = 0; t < ntile; ++t) {
@@ -386,28 +445,30 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
           const int valid = min(kN, nk - t * kN);
           if (t == 0) {
             R = tile_max(taddr, valid) * g.alpha;
-            s.negR = -R;
+            s.negR = make_float2(-R, -R);
           }
           const int ph = (t * kN) % C;
           const int q = (t * kN) / C;
           const RowState before = s;
-          tile_dispatch<C>(ph, valid < kN, taddr, g.alpha, s, ubins + (size_t)q * g.wG, g.wG, valid, write);
-          if (__any_sync(0xffffffffu, s.over)) {
-            // a value outgrew the reference: those rows move their reference to this
-            // tile's maximum, rescale what they already hold and redo the tile (the
-            // whole warp takes part because the TMEM loads are warp-collective)
+          tile_dispatch<C>(ph, valid < kN, taddr, alpha2, s, ubins + (size_t)q * g.wG, g.wG, valid, write, bpol);
+          // every bin is at most the row sum: one test per tile catches any value
+          // that outgrew the reference (and inf / NaN)
+          const bool over = !(s.l <= kBig);
+          if (__any_sync(0xffffffffu, over)) {
+            // those rows move their reference to this tile's maximum, rescale what
+            // they already hold and redo the tile (the whole warp takes part because
+            // the TMEM loads are warp-collective)
             const float tm = tile_max(taddr, valid) * g.alpha;
-            const float R2 = s.over ? fmaxf(R, tm) : R;
+            const float R2 = over ? fmaxf(R, tm) : R;
             const float f = ex2(R - R2);
-            if (s.over && write)
+            if (over && write)
               for (int ch = 0; ch < q; ++ch) ubins[(size_t)ch * g.wG] *= f;
             s = before;
             s.l *= f;
-            s.carry *= f;
+            s.carry = make_float2(s.carry.x * f, s.carry.y * f);
             R = R2;
-            s.negR = -R2;
-            tile_dispatch<C>(ph, valid < kN, taddr, g.alpha, s, ubins + (size_t)q * g.wG, g.wG, valid, write);
-            s.over = false;
+            s.negR = make_float2(-R2, -R2);
+            tile_dispatch<C>(ph, valid < kN, taddr, alpha2, s, ubins + (size_t)q * g.wG, g.wG, valid, write, bpol);
           }
         }
         tc_fence_before();
@@ -418,9 +479,10 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
       if (warp_live && write) {
         // the item ended inside a chunk (last, partial chunk of the sequence)
         if ((ntile * kN) % C != 0) {
+          const float cs = s.carry.x + s.carry.y;
           const int ch = (ntile * kN) / C;
-          if (ch < g.cpu) ubins[(size_t)ch * g.wG] = s.carry;
-          s.l += s.carry;
+          if (ch < g.cpu) ubins[(size_t)ch * g.wG] = cs;
+          s.l += cs;
         }
         rl[((size_t)unit * 2 + 0) * g.wG + row] = R;
         rl[((size_t)unit * 2 + 1) * g.wG + row] = s.l;
@@ -429,6 +491,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
   }
 
   // ------------------------------------------------ teardown
+  pdl_trigger();
   if (*abort_flag) {
     // let copies and MMAs already in flight land before the shared memory and TMEM go away
     const long long t0 = clock64();
@@ -443,9 +506,19 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
 }
 
 // Packed window rows: qp[((b*Hkv + h)*MT + mt)*128 + r][e] = Q_w[b, r % w, h*G + r / w, e] for
-// rows r < w*G of the group, zero for the padding rows up to MT*128.
-__global__ void pack_q_kernel(const __nv_bfloat16* __restrict__ q, ScoreGeom g, int MT, int B,
-                              __nv_bfloat16* __restrict__ qp) {
+// rows r < w*G of the group, zero for the padding rows up to MT*128.  blockIdx.y
+// selects one of up to kMaxPackLayers layers (their packed tiles follow each other).
+constexpr int kMaxPackLayers = 64;
+struct PackArgs {
+  int32_t n;
+  const __nv_bfloat16* q[kMaxPackLayers];
+};
+
+__global__ void pack_q_kernel(const __grid_constant__ PackArgs pa, ScoreGeom g, int MT, int B,
+                              __nv_bfloat16* __restrict__ qp_base, int64_t layer_elems) {
+  const __nv_bfloat16* q = pa.q[blockIdx.y];
+  __nv_bfloat16* qp = qp_base + blockIdx.y * layer_elems;
+  pdl_wait();
   const int rows_per_head = MT * 128;
   const int64_t total_vec = (int64_t)B * g.Hkv * rows_per_head * (kD / 8);
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total_vec; i += (int64_t)gridDim.x * blockDim.x) {
@@ -462,6 +535,7 @@ __global__ void pack_q_kernel(const __nv_bfloat16* __restrict__ q, ScoreGeom g, 
     }
     *(uint4*)(qp + row * kD + vi * 8) = val;
   }
+  pdl_trigger();
 }
 
 // ---------------------------------------------------------------- host side
@@ -507,9 +581,14 @@ cudaError_t launch_c(const TcGeom& tg, const CUtensorMap& mq, const CUtensorMap&
     if (e != cudaSuccess) return e;
     di.attr_set[slot] = true;
   }
-  const int grid = std::min(tg.n_items, 2 * di.sms);
-  score_tc_kernel<C><<<grid, kThreads, kSmemBytes, s>>>(mq, mk, tg, st, rl, bins, err);
-  return cudaGetLastError();
+  // A grid that is a multiple of Hkv * MT keeps each CTA on one (sequence, head,
+  // M tile) from item to item, so its window-row tile stays loaded.
+  int grid = 2 * di.sms;
+  const int period = tg.Hkv * tg.MT;
+  if (grid >= period) grid -= grid % period;
+  grid = std::min(tg.n_items, grid);
+  return launch_pdl(score_tc_kernel<C>, dim3(grid), dim3(kThreads), (size_t)kSmemBytes, s, mq, mk, tg, st, rl,
+                    bins, err);
 }
 
 constexpr int kSupportedC[] = {3, 4, 5, 8, 10, 16, 20, 30};
@@ -531,40 +610,49 @@ bool tc_supported(const Plan& pl) {
 void tc_plan(Plan& pl) {
   pl.use_tc = 0;
   pl.tc_mt = 0;
+  pl.tc_base_chunks = 0;
   if (!(pl.elt == 2 && pl.d == tc::kD && pl.wG > 0 && tc::c_slot(pl.c) >= 0)) return;
-  // Units of lcm(80, c) * m keys: whole tiles and whole chunks.  m is chosen so that
-  // the items (units x M tiles) fill the two-CTA-per-SM persistent grid evenly, with
-  // about 8 tiles (640 keys) per unit as the default size.
-  const int base = tc::lcm_i(tc::kN, pl.c);
-  const int MT = (pl.wG + 127) / 128;
-  int m = std::max(1, 640 / base);
+  // Units are whole tiles and whole chunks: multiples of lcm(80, c) keys.  The
+  // multiplier is chosen by the planner (balance over the persistent grid).
   pl.use_tc = 1;
-  pl.tc_mt = MT;
-  pl.cpu = base * m / pl.c;
+  pl.tc_mt = (pl.wG + 127) / 128;
+  pl.tc_base_chunks = tc::lcm_i(tc::kN, pl.c) / pl.c;
+  pl.cpu = pl.tc_base_chunks * std::max(1, 640 / tc::lcm_i(tc::kN, pl.c));
 }
 
-cudaError_t launch_score_tc(const Plan& pl, const ScoreGeom& g, const SeqTable& st, const void* q, const void* k,
-                            float* rl, float* bins, void* qpack, int32_t* err, cudaStream_t s) {
+cudaError_t launch_pack_q(const Plan& pl, const ScoreGeom& g, const void* const* q_layers, int n_layers,
+                          void* qpack, cudaStream_t s) {
+  const int MT = pl.tc_mt;
+  const int64_t layer_elems = (int64_t)pl.B * pl.Hkv * MT * 128 * tc::kD;
+  for (int l0 = 0; l0 < n_layers; l0 += tc::kMaxPackLayers) {
+    tc::PackArgs pa;
+    pa.n = std::min(tc::kMaxPackLayers, n_layers - l0);
+    for (int i = 0; i < pa.n; ++i) pa.q[i] = (const __nv_bfloat16*)q_layers[l0 + i];
+    const int64_t total_vec = layer_elems / 8;
+    dim3 grid((unsigned)std::min<int64_t>((total_vec + 255) / 256, 2048), pa.n);
+    cudaError_t e = launch_pdl(tc::pack_q_kernel, grid, dim3(256), 0, s, pa, g, MT, pl.B,
+                               (__nv_bfloat16*)qpack + l0 * layer_elems, layer_elems);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+// Scores one layer whose window rows are already packed at qpack (launch_pack_q).
+cudaError_t launch_score_tc(const Plan& pl, const ScoreGeom& g, const SeqTable& st, const void* k, float* rl,
+                            float* bins, const void* qpack, int32_t* err, cudaStream_t s) {
   tc::EncodeFn enc = tc::encode_fn();
   if (enc == nullptr) return cudaErrorNotSupported;
   const int MT = pl.tc_mt;
   const int T_total = st.cu[st.B];
   if (g.n_units == 0 || T_total == 0) return cudaSuccess;
-  // pack the window rows of every (sequence, KV head) into zero-padded 128-row tiles
-  {
-    const int64_t total_vec = (int64_t)pl.B * pl.Hkv * MT * 128 * (tc::kD / 8);
-    const int blocks = (int)std::min<int64_t>((total_vec + 255) / 256, 4096);
-    tc::pack_q_kernel<<<blocks, 256, 0, s>>>((const __nv_bfloat16*)q, g, MT, pl.B, (__nv_bfloat16*)qpack);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
   CUtensorMap mq, mk;
   {
     cuuint64_t dims[2] = {(cuuint64_t)tc::kD, (cuuint64_t)pl.B * pl.Hkv * MT * 128};
     cuuint64_t strides[1] = {(cuuint64_t)tc::kD * 2};
     cuuint32_t box[2] = {64, 128};
     cuuint32_t es[2] = {1, 1};
-    if (enc(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, qpack, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+    if (enc(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(qpack), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;

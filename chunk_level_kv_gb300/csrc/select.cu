@@ -47,8 +47,10 @@ select_kernel(SelectGeom sg, const __grid_constant__ SeqTable st, const float* _
   const int c = sg.c;
   const int C = (T + c - 1) / c;
   const int k = min(sg.L_max / c, C);
-  const float* A = scores + (int64_t)bh * sg.C_max;
-  int32_t* out = indices + (int64_t)bh * sg.n_cap;
+  const float* A = scores + blockIdx.y * sg.scores_gs + (int64_t)bh * sg.C_max;
+  int32_t* out = indices + blockIdx.y * sg.idx_gs + (int64_t)bh * sg.n_cap;
+  counts += blockIdx.y * sg.cnt_gs;
+  pdl_wait();
 
   // ---- 1. threshold key (k-th largest) and how many chunks equal to it are kept
   uint32_t thr = 0;
@@ -126,14 +128,154 @@ select_kernel(SelectGeom sg, const __grid_constant__ SeqTable st, const float* _
   const int rec0 = tail0 + strad;
   for (int t = tid; t < T - Rs; t += blockDim.x) out[rec0 + t] = Rs + t;
   if (tid == 0) counts[bh] = rec0 + (T - Rs);
+  pdl_trigger();
+}
+
+// Register-resident variant for C <= 1024 * ITEMS: thread t holds the order keys
+// of chunks t*ITEMS .. t*ITEMS+ITEMS-1 through the whole selection.  The
+// threshold is found in three radix passes of 11, 11 and 10 bits over 2048-bin
+// shared histograms: the first digit (exponent and leading mantissa bits) spreads
+// similar-magnitude scores over many bins, so the shared atomics rarely collide,
+// and the later passes only count the few keys that still match the prefix.  The
+// ordered expansion needs two block scans.
+constexpr int kSelBins = 2048;
+constexpr int kSelRegThreads = 1024;
+
+template <int ITEMS>
+__global__ void __launch_bounds__(kSelRegThreads)
+select_reg_kernel(SelectGeom sg, const __grid_constant__ SeqTable st, const float* __restrict__ scores,
+                  int32_t* __restrict__ indices, int32_t* __restrict__ counts) {
+  using Scan = cub::BlockScan<int, kSelRegThreads>;
+  constexpr int BPT = kSelBins / kSelRegThreads;           // histogram bins per thread in the scan
+  __shared__ typename Scan::TempStorage scan_tmp;
+  __shared__ int hist[kSelBins];
+  __shared__ uint32_t sh_prefix;
+  __shared__ int sh_remaining, sh_straddle;
+
+  const int bh = blockIdx.x;
+  const int b = bh / sg.Hkv;
+  const int tid = threadIdx.x;
+  const int T = st.cu[b + 1] - st.cu[b];
+  const int c = sg.c;
+  const int C = (T + c - 1) / c;
+  const int k = min(sg.L_max / c, C);
+  const float* A = scores + blockIdx.y * sg.scores_gs + (int64_t)bh * sg.C_max;
+  int32_t* out = indices + blockIdx.y * sg.idx_gs + (int64_t)bh * sg.n_cap;
+  counts += blockIdx.y * sg.cnt_gs;
+  const int i0 = tid * ITEMS;
+  pdl_wait();
+
+  uint32_t key[ITEMS];
+#pragma unroll
+  for (int j = 0; j < ITEMS; ++j) key[j] = (i0 + j < C) ? order_key(__ldcg(A + i0 + j)) : 0u;
+
+  // ---- threshold: the k-th largest key, and how many keys equal to it are kept
+  uint32_t thr = 0;
+  int need_eq = 0;
+  if (k > 0 && k < C) {
+    uint32_t prefix = 0, mask = 0;
+    int remaining = k;
+#pragma unroll 1
+    for (int pass = 0; pass < 3; ++pass) {
+      const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+      const uint32_t dmask = pass == 2 ? 1023u : 2047u;
+      for (int i = tid; i < kSelBins; i += blockDim.x) hist[i] = 0;
+      __syncthreads();
+#pragma unroll
+      for (int j = 0; j < ITEMS; ++j)
+        if ((i0 + j < C) && ((key[j] & mask) == prefix)) atomicAdd(&hist[(key[j] >> shift) & dmask], 1);
+      __syncthreads();
+      // descending digits: thread t holds bins 2047 - BPT*t - i
+      int cnt[BPT], tot = 0;
+#pragma unroll
+      for (int i = 0; i < BPT; ++i) {
+        cnt[i] = hist[kSelBins - 1 - (BPT * tid + i)];
+        tot += cnt[i];
+      }
+      int excl;
+      Scan(scan_tmp).ExclusiveSum(tot, excl);
+#pragma unroll
+      for (int i = 0; i < BPT; ++i) {
+        if (excl < remaining && excl + cnt[i] >= remaining) {
+          sh_prefix = prefix | ((uint32_t)(kSelBins - 1 - (BPT * tid + i)) << shift);
+          sh_remaining = remaining - excl;
+        }
+        excl += cnt[i];
+      }
+      __syncthreads();
+      prefix = sh_prefix;
+      remaining = sh_remaining;
+      mask |= dmask << shift;
+    }
+    thr = prefix;
+    need_eq = remaining;
+  }
+
+  // ---- keep flags: above the threshold, or equal to it and among the first need_eq in index order
+  uint32_t keep = 0, eq = 0;
+  int n_eq = 0;
+#pragma unroll
+  for (int j = 0; j < ITEMS; ++j) {
+    if (i0 + j < C && k > 0) {
+      if (k >= C) {
+        keep |= 1u << j;
+      } else {
+        if (key[j] > thr) keep |= 1u << j;
+        if (key[j] == thr) { eq |= 1u << j; ++n_eq; }
+      }
+    }
+  }
+  if (tid == 0) sh_straddle = 0;
+  int eq_base;
+  Scan(scan_tmp).ExclusiveSum(n_eq, eq_base);
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < ITEMS; ++j)
+    if ((eq >> j) & 1u) {
+      if (eq_base < need_eq) keep |= 1u << j;
+      ++eq_base;
+    }
+
+  // ---- expansion: whole kept chunks below Rs = max(0, T - w) land at rank * c, in order
+  const int Rs = max(0, T - sg.w);
+  const int sc = Rs / c;
+  const int part = Rs - sc * c;
+  int n_low = 0;
+#pragma unroll
+  for (int j = 0; j < ITEMS; ++j) n_low += ((keep >> j) & 1u) && (i0 + j < sc);
+  int rank, low_tot;
+  Scan(scan_tmp).ExclusiveSum(n_low, rank, low_tot);
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < ITEMS; ++j) {
+    const int i = i0 + j;
+    if (((keep >> j) & 1u) && i < sc) {
+      int32_t* o = out + (int64_t)rank * c;
+      for (int t = 0; t < c; ++t) o[t] = i * c + t;
+      ++rank;
+    }
+    if (i == sc && part > 0 && ((keep >> j) & 1u)) sh_straddle = 1;
+  }
+  __syncthreads();
+  const int tail0 = low_tot * c;
+  const int strad = sh_straddle ? part : 0;
+  for (int t = tid; t < strad; t += blockDim.x) out[tail0 + t] = sc * c + t;
+  const int rec0 = tail0 + strad;
+  for (int t = tid; t < T - Rs; t += blockDim.x) out[rec0 + t] = Rs + t;
+  if (tid == 0) counts[bh] = rec0 + (T - Rs);
+  pdl_trigger();
 }
 
 cudaError_t launch_select(const Plan& pl, const SelectGeom& sg, const SeqTable& st, const float* scores,
-                          int32_t* indices, int32_t* counts, cudaStream_t s) {
+                          int32_t* indices, int32_t* counts, int n_groups, cudaStream_t s) {
   const int n = pl.B * pl.Hkv;
-  if (n == 0) return cudaSuccess;
-  select_kernel<<<n, kSelThreads, 0, s>>>(sg, st, scores, indices, counts);
-  return cudaGetLastError();
+  if (n == 0 || n_groups == 0) return cudaSuccess;
+  const dim3 grid(n, n_groups);
+  if (pl.C_max <= kSelRegThreads * 4)
+    return launch_pdl(select_reg_kernel<4>, grid, dim3(kSelRegThreads), 0, s, sg, st, scores, indices, counts);
+  if (pl.C_max <= kSelRegThreads * 16)
+    return launch_pdl(select_reg_kernel<16>, grid, dim3(kSelRegThreads), 0, s, sg, st, scores, indices, counts);
+  return launch_pdl(select_kernel, grid, dim3(kSelThreads), 0, s, sg, st, scores, indices, counts);
 }
 
 }  // namespace chunkkv
