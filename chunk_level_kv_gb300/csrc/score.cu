@@ -146,7 +146,7 @@ cudaError_t launch_score_simt(const Plan& pl, const ScoreGeom& g, const SeqTable
 // same (sequence, head); the unit's bins are then weighted by 2^(R_r - lse_r)
 // and summed over rows, one warp per chunk (coalesced over rows).
 constexpr int kFinThreads = 256;
-constexpr int kFinChunks = 32;                  // chunks per CTA: blockIdx.y tiles a unit
+constexpr int kFinChunks = 128;                 // chunks per CTA: blockIdx.y tiles a unit
 
 __global__ void __launch_bounds__(kFinThreads)
 finalize_kernel(ScoreGeom g, const __grid_constant__ SeqTable st, const float* __restrict__ rl,
@@ -188,19 +188,25 @@ finalize_kernel(ScoreGeom g, const __grid_constant__ SeqTable st, const float* _
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const float* ub = bins + ((int64_t)gu * g.cpu + cb) * g.wG;
   float* out = scores + ((int64_t)b * g.Hkv + h) * g.C_max + (int64_t)u * g.cpu + cb;
-  // each warp sums four chunks at a time: four independent load streams per lane
+  // each warp sums eight chunks at a time: eight independent load streams per lane
   constexpr int kW = kFinThreads / 32;
-  for (int ch0 = warp * 4; ch0 < nc; ch0 += kW * 4) {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    const int m = min(4, nc - ch0);
+  constexpr int kG = 8;
+  for (int ch0 = warp * kG; ch0 < nc; ch0 += kW * kG) {
+    float acc[kG];
+#pragma unroll
+    for (int i = 0; i < kG; ++i) acc[i] = 0.f;
+    const int m = min(kG, nc - ch0);
+    const float* cbase = ub + (int64_t)ch0 * g.wG;
     for (int r = lane; r < g.wG; r += 32) {
       const float wr = wts[r];
+      float v[kG];
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        if (i < m) acc[i] = fmaf(__ldcs(ub + (int64_t)(ch0 + i) * g.wG + r), wr, acc[i]);
+      for (int i = 0; i < kG; ++i) v[i] = i < m ? __ldcs(cbase + (int64_t)i * g.wG + r) : 0.f;
+#pragma unroll
+      for (int i = 0; i < kG; ++i) acc[i] = fmaf(v[i], wr, acc[i]);
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < kG; ++i) {
       float a = acc[i];
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
