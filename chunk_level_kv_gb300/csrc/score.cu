@@ -197,13 +197,28 @@ finalize_kernel(ScoreGeom g, const __grid_constant__ SeqTable st, const float* _
     for (int i = 0; i < kG; ++i) acc[i] = 0.f;
     const int m = min(kG, nc - ch0);
     const float* cbase = ub + (int64_t)ch0 * g.wG;
-    for (int r = lane; r < g.wG; r += 32) {
-      const float wr = wts[r];
-      float v[kG];
+    if ((g.wG & 3) == 0) {
+      // four consecutive rows per lane: 16-byte loads, kG of them in flight
+      for (int r = 4 * lane; r < g.wG; r += 128) {
+        const float4 w4 = *reinterpret_cast<const float4*>(wts + r);
+        float4 v[kG];
 #pragma unroll
-      for (int i = 0; i < kG; ++i) v[i] = i < m ? __ldcs(cbase + (int64_t)i * g.wG + r) : 0.f;
+        for (int i = 0; i < kG; ++i)
+          v[i] = i < m ? __ldcs(reinterpret_cast<const float4*>(cbase + (int64_t)i * g.wG + r))
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int i = 0; i < kG; ++i) acc[i] = fmaf(v[i], wr, acc[i]);
+        for (int i = 0; i < kG; ++i)
+          acc[i] = fmaf(v[i].x, w4.x, fmaf(v[i].y, w4.y, fmaf(v[i].z, w4.z, fmaf(v[i].w, w4.w, acc[i]))));
+      }
+    } else {
+      for (int r = lane; r < g.wG; r += 32) {
+        const float wr = wts[r];
+        float v[kG];
+#pragma unroll
+        for (int i = 0; i < kG; ++i) v[i] = i < m ? __ldcs(cbase + (int64_t)i * g.wG + r) : 0.f;
+#pragma unroll
+        for (int i = 0; i < kG; ++i) acc[i] = fmaf(v[i], wr, acc[i]);
+      }
     }
 #pragma unroll
     for (int i = 0; i < kG; ++i) {
@@ -221,7 +236,7 @@ finalize_kernel(ScoreGeom g, const __grid_constant__ SeqTable st, const float* _
 // (sequence, head, 32 rows): lane = row (128-byte loads), the 32 warps take every
 // 32nd unit, four units per step with their loads issued together, and the
 // partial (M, S) pairs are merged through shared memory.
-constexpr int kLseThreads = 1024;
+constexpr int kLseThreads = 256;
 
 __device__ __forceinline__ void lse_merge(float& M, float& S, float Mv, float Sv) {
   if (Sv == 0.f) return;
