@@ -3,6 +3,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <vector>
 
 #include "common.cuh"
 
@@ -12,8 +13,9 @@ bool tc_supported(const Plan& pl);                                  // score_tc.
 void tc_plan(Plan& pl);                                             // score_tc.cu
 cudaError_t launch_pack_q(const Plan& pl, const ScoreGeom& g, const void* const* q_layers, int n_layers,
                           void* qpack, cudaStream_t s);
-cudaError_t launch_score_tc(const Plan& pl, const ScoreGeom& g, const SeqTable& st, const void* k, float* rl,
-                            float* bins, const void* qpack, int32_t* err, cudaStream_t s);
+cudaError_t launch_score_tc(const Plan& pl, const ScoreGeom& g, const SeqTable& st, const void* const* k_groups,
+                            int n_groups, int64_t slot_gs, float* rl, float* bins, const void* qpack, int32_t* err,
+                            cudaStream_t s);
 
 namespace {
 
@@ -166,14 +168,21 @@ ScoreGeom score_geom(const chunkkv_params* p, const Plan& pl) {
 
 chunkkv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? CHUNKKV_OK : CHUNKKV_ERR_CUDA; }
 
-// Scoring kernel of one reuse group (its layer's window rows already packed at
-// qpack on the tensor-core path) into the group's scratch slot.
-cudaError_t run_score_group(const Plan& pl, const ScoreGeom& g, const SeqTable& st, const void* q, const void* k,
-                            char* slot, const void* qpack, int32_t* err, cudaStream_t s) {
-  float* rl = (float*)(slot + pl.off_rl);
-  float* bins = (float*)(slot + pl.off_bins);
-  return pl.use_tc ? launch_score_tc(pl, g, st, k, rl, bins, qpack, err, s)
-                   : launch_score_simt(pl, g, st, q, k, rl, bins, s);
+// Scoring of n_groups reuse groups into consecutive scratch slots from `slots`.
+// q and k hold each group's scoring layer; on the tensor-core path the window
+// rows are already packed from qpack and one persistent launch covers all groups.
+cudaError_t run_score_groups(const Plan& pl, const ScoreGeom& g, const SeqTable& st, const void* const* q,
+                             const void* const* k, int n_groups, char* slots, const void* qpack, int32_t* err,
+                             cudaStream_t s) {
+  float* rl = (float*)(slots + pl.off_rl);
+  float* bins = (float*)(slots + pl.off_bins);
+  const int64_t slot_gs = (int64_t)(pl.slot_bytes / sizeof(float));
+  if (pl.use_tc) return launch_score_tc(pl, g, st, k, n_groups, slot_gs, rl, bins, qpack, err, s);
+  for (int i = 0; i < n_groups; ++i) {
+    cudaError_t e = launch_score_simt(pl, g, st, q[i], k[i], rl + i * slot_gs, bins + i * slot_gs, s);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 // Log-sum-exp and finalisation of n_groups consecutive slots into their chunk scores.
@@ -305,7 +314,7 @@ chunkkv_status chunkkv_score(const chunkkv_params* p, const void* q_win, const v
     const void* ql[1] = {q_win};
     e = launch_pack_q(pl, g, ql, 1, qpack, cs);
   }
-  if (e == cudaSuccess) e = run_score_group(pl, g, st, q_win, k, slot, qpack, (int32_t*)w, cs);
+  if (e == cudaSuccess) e = run_score_groups(pl, g, st, &q_win, &k, 1, slot, qpack, (int32_t*)w, cs);
   if (e == cudaSuccess) e = run_post_score(pl, g, st, slot, chunk_scores, 1, cs);
   return cuda_status(e);
 }
@@ -378,19 +387,16 @@ chunkkv_status chunkkv_compress_layers(const chunkkv_params* p, int32_t n_layers
   //  4. top-k selection and index build of every (group, sequence, head) in one launch;
   //  5. the gather of every layer (layer l with index group l / n_reuse).
   cudaError_t e = cudaSuccess;
-  if (pl.use_tc && pl.wG > 0) {
-    static thread_local const void* qsel[CHUNKKV_MAX_GATHER_LAYERS];
-    for (int g0 = 0; g0 < n_groups && e == cudaSuccess; g0 += CHUNKKV_MAX_GATHER_LAYERS) {
-      const int n = std::min(CHUNKKV_MAX_GATHER_LAYERS, n_groups - g0);
-      for (int i = 0; i < n; ++i) qsel[i] = q_win[(g0 + i) * n_reuse];
-      e = launch_pack_q(pl, g, qsel, n, base + pl.off_qpack + g0 * pl.qpack_group_bytes, cs);
-    }
+  static thread_local std::vector<const void*> qsel, ksel;
+  qsel.resize(n_groups);
+  ksel.resize(n_groups);
+  for (int i = 0; i < n_groups; ++i) {
+    qsel[i] = q_win[i * n_reuse];
+    ksel[i] = k[i * n_reuse];
   }
-  for (int grp = 0; grp < n_groups && e == cudaSuccess; ++grp) {
-    const int l0 = grp * n_reuse;
-    e = run_score_group(pl, g, st, q_win[l0], k[l0], base + pl.off_slots + grp * pl.slot_bytes,
-                        base + pl.off_qpack + grp * pl.qpack_group_bytes, (int32_t*)w, cs);
-  }
+  if (pl.use_tc && pl.wG > 0) e = launch_pack_q(pl, g, qsel.data(), n_groups, base + pl.off_qpack, cs);
+  if (e == cudaSuccess)
+    e = run_score_groups(pl, g, st, qsel.data(), ksel.data(), n_groups, base + pl.off_slots, base + pl.off_qpack, (int32_t*)w, cs);
   if (e == cudaSuccess) e = run_post_score(pl, g, st, base + pl.off_slots, scores, n_groups, cs);
   if (e == cudaSuccess) {
     SelectGeom sg = select_geom(p, pl);

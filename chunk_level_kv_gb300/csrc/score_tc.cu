@@ -50,11 +50,46 @@ constexpr uint32_t kIdesc = (1u << 4)                         // D = fp32
                           | ((uint32_t)(128 >> 4) << 24);    // M
 constexpr float kBig = 18446744073709551616.0f;              // 2^64: rescale threshold
 
+// One launch scores up to kMaxGroups reuse groups (one layer each): items are
+// enumerated group by group, each group with its own key tensor map and its own
+// scratch slot (rl, bins at a fixed stride from the first group's).
+constexpr int kMaxGroups = 32;
+
 struct TcGeom {
-  int32_t Hkv, wG, MT, cpu, ku, n_items;
+  int32_t B, Hkv, wG, MT, cpu, ku;
+  int32_t items_pg;                  // work items per group: units x M tiles
+  int32_t n_items;                   // items_pg x groups of this launch
+  int64_t slot_gs;                   // floats between the scratch slots of consecutive groups
   float alpha;                       // log2(e) / sqrt(d)
   long long timeout;                 // clock64 cycles per wait
 };
+
+struct TcMaps {
+  CUtensorMap q;                     // packed window rows of every group of the launch, [rows, 128]
+  CUtensorMap k[kMaxGroups];         // keys of each group's layer, [T_total, Hkv, 128]
+};
+
+// Where work item `item` of a launch lives.
+struct Item {
+  int grp, unit, mt, b, h, u, nk, ntile, key;
+  int64_t tok0;                      // first key row of the unit in the packed varlen key array
+};
+
+__device__ __forceinline__ Item decode_item(const TcGeom& g, const SeqTable& st, int item) {
+  Item it;
+  it.grp = item / g.items_pg;
+  const int local = item - it.grp * g.items_pg;
+  it.unit = local / g.MT;
+  it.mt = local - it.unit * g.MT;
+  decode_unit(st, g.Hkv, it.unit, it.b, it.h, it.u);
+  const int T = st.cu[it.b + 1] - st.cu[it.b];
+  const int k0 = it.u * g.ku;
+  it.nk = min(g.ku, T - k0);
+  it.ntile = (it.nk + kN - 1) / kN;
+  it.key = ((it.grp * g.B + it.b) * g.Hkv + it.h) * g.MT + it.mt;   // packed row tile of its window rows
+  it.tok0 = (int64_t)st.cu[it.b] + k0;
+  return it;
+}
 
 // ---------------------------------------------------------------- PTX wrappers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -283,9 +318,8 @@ __device__ __forceinline__ float tile_max(uint32_t taddr, int valid) {
 // ---------------------------------------------------------------- the kernel
 template <int C>
 __global__ void __launch_bounds__(kThreads, 2)
-score_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k, TcGeom g,
-                const __grid_constant__ SeqTable st, float* __restrict__ rl, float* __restrict__ bins,
-                int32_t* __restrict__ err) {
+score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_constant__ SeqTable st,
+                float* __restrict__ rl, float* __restrict__ bins, int32_t* __restrict__ err) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw;
   if (smem_u32(smem_raw) & 1023u) {                         // swizzled tiles need 1024-byte alignment
@@ -311,8 +345,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     for (int i = 0; i < kStagesT; ++i) { mbar_init(smem_u32(&t_full[i]), 1); mbar_init(smem_u32(&t_empty[i]), 128); }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmap_q) : "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmap_k) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&maps.q) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&maps.k[0]) : "memory");
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -329,36 +363,46 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
       uint32_t kc = 0, qc = 0;
-      int qkey = -1;                                   // (sequence, head, M tile) of the loaded Q
+      int qkey = -1;                                   // (group, sequence, head, M tile) of the loaded Q
       const uint64_t kpol = policy_evict_first();      // keys are streamed once per M tile
-      for (int item = blockIdx.x; item < g.n_items && !*abort_flag; item += gridDim.x) {
-        const int unit = item / g.MT, mt = item - unit * g.MT;
-        int b, h, u;
-        decode_unit(st, g.Hkv, unit, b, h, u);
-        const int T = st.cu[b + 1] - st.cu[b];
-        const int k0 = u * g.ku;
-        const int nk = min(g.ku, T - k0);
-        const int ntile = (nk + kN - 1) / kN;
-        const int key = (b * g.Hkv + h) * g.MT + mt;
-        if (key != qkey) {
-          // a new window-row tile: wait until the MMAs that read the old one are done
+      bool ok = true;
+      for (int item = blockIdx.x; item < g.n_items && ok && !*abort_flag; item += gridDim.x) {
+        const Item it = decode_item(g, st, item);
+        const CUtensorMap* kmap = &maps.k[it.grp];
+        // A new window-row tile is loaded only after the first K tiles of the item
+        // are on their way: the MMAs of the previous item still need the old tile,
+        // and its reload then overlaps the softmax of the previous item's last tiles.
+        const int pre = it.key != qkey ? min(it.ntile, kStagesK) : 0;
+        for (int t = 0; t < it.ntile && ok; ++t) {
+          if (t == pre && it.key != qkey) {
+            if (!wait_bar(ctl, smem_u32(&q_empty[0]), (qc & 1) ^ 1, kDevTimeoutTmaProducer)) { ok = false; break; }
+            const uint32_t qbar = smem_u32(&q_full[0]);
+            mbar_expect_tx(qbar, kQBytes);
+            tma_load_2d(smem_u32(sQ), &maps.q, qbar, 0, it.key * 128);
+            tma_load_2d(smem_u32(sQ + kPanelQ), &maps.q, qbar, 64, it.key * 128);
+            ++qc;
+            qkey = it.key;
+          }
+          const int ks = kc % kStagesK;
+          if (!wait_bar(ctl, smem_u32(&k_empty[ks]), ((kc / kStagesK) & 1) ^ 1, kDevTimeoutTmaProducer)) {
+            ok = false;
+            break;
+          }
+          const uint32_t kbar = smem_u32(&k_full[ks]);
+          mbar_expect_tx(kbar, kKBytes);
+          const int tok = (int)(it.tok0 + t * kN);
+          tma_load_3d_hint(smem_u32(sK + ks * kKBytes), kmap, kbar, 0, it.h, tok, kpol);
+          tma_load_3d_hint(smem_u32(sK + ks * kKBytes + kPanelK), kmap, kbar, 64, it.h, tok, kpol);
+          ++kc;
+        }
+        if (ok && it.key != qkey) {          // an item shorter than the prefetch: its Q comes last
           if (!wait_bar(ctl, smem_u32(&q_empty[0]), (qc & 1) ^ 1, kDevTimeoutTmaProducer)) break;
           const uint32_t qbar = smem_u32(&q_full[0]);
           mbar_expect_tx(qbar, kQBytes);
-          tma_load_2d(smem_u32(sQ), &tmap_q, qbar, 0, key * 128);
-          tma_load_2d(smem_u32(sQ + kPanelQ), &tmap_q, qbar, 64, key * 128);
+          tma_load_2d(smem_u32(sQ), &maps.q, qbar, 0, it.key * 128);
+          tma_load_2d(smem_u32(sQ + kPanelQ), &maps.q, qbar, 64, it.key * 128);
           ++qc;
-          qkey = key;
-        }
-        const int tok0 = st.cu[b] + k0;
-        for (int t = 0; t < ntile; ++t) {
-          const int ks = kc % kStagesK;
-          if (!wait_bar(ctl, smem_u32(&k_empty[ks]), ((kc / kStagesK) & 1) ^ 1, kDevTimeoutTmaProducer)) break;
-          const uint32_t kbar = smem_u32(&k_full[ks]);
-          mbar_expect_tx(kbar, kKBytes);
-          tma_load_3d_hint(smem_u32(sK + ks * kKBytes), &tmap_k, kbar, 0, h, tok0 + t * kN, kpol);
-          tma_load_3d_hint(smem_u32(sK + ks * kKBytes + kPanelK), &tmap_k, kbar, 64, h, tok0 + t * kN, kpol);
-          ++kc;
+          qkey = it.key;
         }
       }
     }
@@ -369,13 +413,9 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
       int qkey = -1;
       const uint32_t qaddr = smem_u32(sQ);
       for (int item = blockIdx.x; item < g.n_items && !*abort_flag; item += gridDim.x) {
-        const int unit = item / g.MT, mt = item - unit * g.MT;
-        int b, h, u;
-        decode_unit(st, g.Hkv, unit, b, h, u);
-        const int T = st.cu[b + 1] - st.cu[b];
-        const int nk = min(g.ku, T - u * g.ku);
-        const int ntile = (nk + kN - 1) / kN;
-        const int key = (b * g.Hkv + h) * g.MT + mt;
+        const Item it = decode_item(g, st, item);
+        const int ntile = it.ntile;
+        const int key = it.key;
         if (key != qkey) {
           if (qkey >= 0) tc_commit(smem_u32(&q_empty[0]));     // old Q free once its MMAs finish
           if (!wait_bar(ctl, smem_u32(&q_full[0]), qc & 1, kDevTimeoutMma)) break;
@@ -419,16 +459,13 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     const uint32_t lane_base = tmem + ((uint32_t)(lg * 32) << 16);
     uint32_t tc = 0;
     for (int item = blockIdx.x; item < g.n_items && !*abort_flag; item += gridDim.x) {
-      const int unit = item / g.MT, mt = item - unit * g.MT;
-      int b, h, u;
-      decode_unit(st, g.Hkv, unit, b, h, u);
-      const int T = st.cu[b + 1] - st.cu[b];
-      const int nk = min(g.ku, T - u * g.ku);
-      const int ntile = (nk + kN - 1) / kN;
-      const int row = mt * 128 + rloc;
+      const Item it = decode_item(g, st, item);
+      const int nk = it.nk, ntile = it.ntile;
+      const int row = it.mt * 128 + rloc;
       const bool write = row < g.wG;
-      const bool warp_live = mt * 128 + lg * 32 < g.wG;            // whole warp of padding rows: no work
-      float* ubins = bins + (size_t)unit * g.cpu * g.wG + row;
+      const bool warp_live = it.mt * 128 + lg * 32 < g.wG;         // whole warp of padding rows: no work
+      float* ubins = bins + it.grp * g.slot_gs + (size_t)it.unit * g.cpu * g.wG + row;
+      float* url = rl + it.grp * g.slot_gs + (size_t)it.unit * 2 * g.wG + row;
       RowState s{make_float2(0.f, 0.f), make_float2(0.f, 0.f), 0.f};
       const float2 alpha2 = make_float2(g.alpha, g.alpha);
       float R = 0.f;
@@ -484,8 +521,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
           if (ch < g.cpu) ubins[(size_t)ch * g.wG] = cs;
           s.l += cs;
         }
-        rl[((size_t)unit * 2 + 0) * g.wG + row] = R;
-        rl[((size_t)unit * 2 + 1) * g.wG + row] = s.l;
+        url[0] = R;
+        url[g.wG] = s.l;
       }
     }
   }
@@ -570,8 +607,8 @@ DeviceInfo& device_info(int dev) {
 }
 
 template <int C>
-cudaError_t launch_c(const TcGeom& tg, const CUtensorMap& mq, const CUtensorMap& mk, const SeqTable& st, float* rl,
-                     float* bins, int32_t* err, int slot, cudaStream_t s) {
+cudaError_t launch_c(const TcGeom& tg, const TcMaps& maps, const SeqTable& st, float* rl, float* bins, int32_t* err,
+                     int slot, cudaStream_t s) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -581,14 +618,15 @@ cudaError_t launch_c(const TcGeom& tg, const CUtensorMap& mq, const CUtensorMap&
     if (e != cudaSuccess) return e;
     di.attr_set[slot] = true;
   }
-  // A grid that is a multiple of Hkv * MT keeps each CTA on one (sequence, head,
-  // M tile) from item to item, so its window-row tile stays loaded.
+  // A grid that is a multiple of Hkv * MT keeps each CTA on one (head, M tile)
+  // from item to item (items of a group are a multiple of Hkv * MT too), so the
+  // window-row tile changes only with the sequence or the group.
   int grid = 2 * di.sms;
   const int period = tg.Hkv * tg.MT;
   if (grid >= period) grid -= grid % period;
   grid = std::min(tg.n_items, grid);
-  return launch_pdl(score_tc_kernel<C>, dim3(grid), dim3(kThreads), (size_t)kSmemBytes, s, mq, mk, tg, st, rl,
-                    bins, err);
+  return launch_pdl(score_tc_kernel<C>, dim3(grid), dim3(kThreads), (size_t)kSmemBytes, s, maps, tg, st, rl, bins,
+                    err);
 }
 
 constexpr int kSupportedC[] = {3, 4, 5, 8, 10, 16, 20, 30};
@@ -637,56 +675,71 @@ cudaError_t launch_pack_q(const Plan& pl, const ScoreGeom& g, const void* const*
   return cudaSuccess;
 }
 
-// Scores one layer whose window rows are already packed at qpack (launch_pack_q).
-cudaError_t launch_score_tc(const Plan& pl, const ScoreGeom& g, const SeqTable& st, const void* k, float* rl,
-                            float* bins, const void* qpack, int32_t* err, cudaStream_t s) {
+// Scores n_groups layers (one per reuse group) in one persistent launch.  Their
+// window rows are packed back to back from qpack (launch_pack_q); group i reads
+// keys k_groups[i] and writes the scratch slot at rl + i * slot_gs and
+// bins + i * slot_gs (slot_gs in floats).
+cudaError_t launch_score_tc(const Plan& pl, const ScoreGeom& g, const SeqTable& st, const void* const* k_groups,
+                            int n_groups, int64_t slot_gs, float* rl, float* bins, const void* qpack, int32_t* err,
+                            cudaStream_t s) {
   tc::EncodeFn enc = tc::encode_fn();
   if (enc == nullptr) return cudaErrorNotSupported;
   const int MT = pl.tc_mt;
   const int T_total = st.cu[st.B];
-  if (g.n_units == 0 || T_total == 0) return cudaSuccess;
-  CUtensorMap mq, mk;
-  {
-    cuuint64_t dims[2] = {(cuuint64_t)tc::kD, (cuuint64_t)pl.B * pl.Hkv * MT * 128};
-    cuuint64_t strides[1] = {(cuuint64_t)tc::kD * 2};
-    cuuint32_t box[2] = {64, 128};
-    cuuint32_t es[2] = {1, 1};
-    if (enc(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(qpack), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
+  if (g.n_units == 0 || T_total == 0 || n_groups == 0) return cudaSuccess;
+  const int64_t rows_pg = (int64_t)pl.B * pl.Hkv * MT * 128;
+  for (int g0 = 0; g0 < n_groups; g0 += tc::kMaxGroups) {
+    const int n = std::min(tc::kMaxGroups, n_groups - g0);
+    static thread_local tc::TcMaps maps;
+    {
+      cuuint64_t dims[2] = {(cuuint64_t)tc::kD, (cuuint64_t)(rows_pg * n)};
+      cuuint64_t strides[1] = {(cuuint64_t)tc::kD * 2};
+      cuuint32_t box[2] = {64, 128};
+      cuuint32_t es[2] = {1, 1};
+      const void* qg = (const char*)qpack + g0 * rows_pg * tc::kD * 2;
+      if (enc(&maps.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(qg), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    }
+    for (int i = 0; i < n; ++i) {
+      cuuint64_t dims[3] = {(cuuint64_t)tc::kD, (cuuint64_t)pl.Hkv, (cuuint64_t)T_total};
+      cuuint64_t strides[2] = {(cuuint64_t)g.kv_stride_h * 2, (cuuint64_t)g.kv_stride_t * 2};
+      cuuint32_t box[3] = {64, 1, tc::kN};
+      cuuint32_t es[3] = {1, 1, 1};
+      if (enc(&maps.k[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(k_groups[g0 + i]), dims, strides,
+              box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    }
+    tc::TcGeom tg;
+    tg.B = pl.B;
+    tg.Hkv = pl.Hkv;
+    tg.wG = pl.wG;
+    tg.MT = MT;
+    tg.cpu = pl.cpu;
+    tg.ku = pl.ku;
+    tg.items_pg = g.n_units * MT;
+    tg.n_items = tg.items_pg * n;
+    tg.slot_gs = slot_gs;
+    tg.alpha = g.alpha;
+    tg.timeout = 4000000000LL;     // about two seconds of clock64 cycles per wait
+    float* rlg = rl + g0 * slot_gs;
+    float* bg = bins + g0 * slot_gs;
+    cudaError_t e = cudaErrorNotSupported;
+    switch (pl.c) {
+      case 3: e = tc::launch_c<3>(tg, maps, st, rlg, bg, err, 0, s); break;
+      case 4: e = tc::launch_c<4>(tg, maps, st, rlg, bg, err, 1, s); break;
+      case 5: e = tc::launch_c<5>(tg, maps, st, rlg, bg, err, 2, s); break;
+      case 8: e = tc::launch_c<8>(tg, maps, st, rlg, bg, err, 3, s); break;
+      case 10: e = tc::launch_c<10>(tg, maps, st, rlg, bg, err, 4, s); break;
+      case 16: e = tc::launch_c<16>(tg, maps, st, rlg, bg, err, 5, s); break;
+      case 20: e = tc::launch_c<20>(tg, maps, st, rlg, bg, err, 6, s); break;
+      case 30: e = tc::launch_c<30>(tg, maps, st, rlg, bg, err, 7, s); break;
+    }
+    if (e != cudaSuccess) return e;
   }
-  {
-    cuuint64_t dims[3] = {(cuuint64_t)tc::kD, (cuuint64_t)pl.Hkv, (cuuint64_t)T_total};
-    cuuint64_t strides[2] = {(cuuint64_t)g.kv_stride_h * 2, (cuuint64_t)g.kv_stride_t * 2};
-    cuuint32_t box[3] = {64, 1, tc::kN};
-    cuuint32_t es[3] = {1, 1, 1};
-    if (enc(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(k), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
-  tc::TcGeom tg;
-  tg.Hkv = pl.Hkv;
-  tg.wG = pl.wG;
-  tg.MT = MT;
-  tg.cpu = pl.cpu;
-  tg.ku = pl.ku;
-  tg.n_items = g.n_units * MT;
-  tg.alpha = g.alpha;
-  tg.timeout = 4000000000LL;     // about two seconds of clock64 cycles per wait
-  switch (pl.c) {
-    case 3: return tc::launch_c<3>(tg, mq, mk, st, rl, bins, err, 0, s);
-    case 4: return tc::launch_c<4>(tg, mq, mk, st, rl, bins, err, 1, s);
-    case 5: return tc::launch_c<5>(tg, mq, mk, st, rl, bins, err, 2, s);
-    case 8: return tc::launch_c<8>(tg, mq, mk, st, rl, bins, err, 3, s);
-    case 10: return tc::launch_c<10>(tg, mq, mk, st, rl, bins, err, 4, s);
-    case 16: return tc::launch_c<16>(tg, mq, mk, st, rl, bins, err, 5, s);
-    case 20: return tc::launch_c<20>(tg, mq, mk, st, rl, bins, err, 6, s);
-    case 30: return tc::launch_c<30>(tg, mq, mk, st, rl, bins, err, 7, s);
-  }
-  return cudaErrorNotSupported;
+  return cudaSuccess;
 }
 
 }  // namespace chunkkv
