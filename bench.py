@@ -148,6 +148,7 @@ def run_gpu(args):
     torch.cuda.synchronize()
     sampler.start()
     time.sleep(0.3)
+    launches0 = ckv.chunkkv_launch_count()
     times = []
     for _ in range(args.steps):
         if flush is not None:
@@ -158,6 +159,7 @@ def run_gpu(args):
         e1.record(stream)
         times.append((e0, e1))
     torch.cuda.synchronize()
+    launches = ckv.chunkkv_launch_count() - launches0        # library kernels in the timed region
     clocks = sampler.stop()
     ms = [a.elapsed_time(b) for a, b in times]
     ckv.chunkkv_status_check(ws)
@@ -188,9 +190,6 @@ def run_gpu(args):
     path = ckv.chunkkv_score_path(p)
     roof_peak = peaks["hbm_gbs"]
     achieved = score_bytes / (score_avg * 1e-3) / 1e9
-    # per reuse group: scoring, log-sum-exp, finalize, select, gather (+ one Q pack per step on the
-    # tensor-core path)
-    launches_per_step = groups * 5 + (1 if path == 1 else 0)
 
     # ---- end to end through the C-ABI with host buffers (pinned), copies inside the timed region
     e2e = None
@@ -260,7 +259,7 @@ def run_gpu(args):
                      "peak_source": f"{peak_src} hbm_gbs", "avg_launch_ms": round(score_avg, 5)},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": int(launches),
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)

@@ -56,6 +56,8 @@ def _load():
         fn.restype = ctypes.c_int32
     lib.chunkkv_status_string.argtypes = [ctypes.c_int32]
     lib.chunkkv_status_string.restype = ctypes.c_char_p
+    lib.chunkkv_launch_count.argtypes = []
+    lib.chunkkv_launch_count.restype = ctypes.c_uint64
     return lib
 
 

@@ -89,6 +89,10 @@ def chunkkv_score_path(p: Params) -> int:
     return int(LIB.chunkkv_score_path(ctypes.byref(p)))
 
 
+def chunkkv_launch_count() -> int:
+    return int(LIB.chunkkv_launch_count())
+
+
 def chunkkv_score(p: Params, q_win, k, chunk_scores, ws) -> None:
     _check("chunkkv_score", LIB.chunkkv_score(ctypes.byref(p), _ptr(q_win), _ptr(k), _ptr(chunk_scores),
                                               _ptr(ws), ws.numel() * ws.element_size(), _stream(k.device)))

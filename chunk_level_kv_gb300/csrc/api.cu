@@ -9,6 +9,8 @@
 
 namespace chunkkv {
 
+std::atomic<unsigned long long> g_launch_count{0};
+
 bool tc_supported(const Plan& pl);                                  // score_tc.cu
 void tc_plan(Plan& pl);                                             // score_tc.cu
 cudaError_t launch_pack_q(const Plan& pl, const ScoreGeom& g, const void* const* q_layers, int n_layers,
@@ -85,7 +87,7 @@ chunkkv_status make_plan(const chunkkv_params* p, int n_layers, int n_reuse, Pla
     // two-CTA-per-SM GB300 (304 slots); ties go to longer units.
     const int slots = 2 * 152;
     const int64_t per_unit_items = (int64_t)p->Hkv * pl.tc_mt;
-    const int base_tiles = pl.tc_base_chunks * p->c / 80;
+    const int base_tiles = pl.tc_base_chunks * p->c / pl.tc_tile_n;
     int64_t best_cost = INT64_MAX;
     for (int m = 1; m <= 64; ++m) {
       const int cpu = pl.tc_base_chunks * m;
@@ -406,6 +408,8 @@ chunkkv_status chunkkv_compress_layers(const chunkkv_params* p, int32_t n_layers
   if (e == cudaSuccess) e = run_gather(p, pl, st, n_layers, n_reuse, k, v, k_out, v_out, indices, counts, cs);
   return cuda_status(e);
 }
+
+uint64_t chunkkv_launch_count(void) { return chunkkv::g_launch_count.load(std::memory_order_relaxed); }
 
 chunkkv_status chunkkv_status_check(void* ws, chunkkv_stream_t stream, int32_t* device_code) {
   if (ws == nullptr) return CHUNKKV_ERR_INVALID_ARG;

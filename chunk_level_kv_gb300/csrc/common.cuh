@@ -6,6 +6,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "chunkkv.h"
 
 namespace chunkkv {
@@ -98,6 +100,9 @@ __device__ __forceinline__ float to_float(__nv_bfloat16 x) { return __bfloat162f
 // ----------------------------------------------------------------- host side
 
 // Launch with programmatic stream serialisation (see pdl_wait / pdl_trigger).
+// Kernels launched through launch_pdl by this process (chunkkv_launch_count).
+extern std::atomic<unsigned long long> g_launch_count;
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
                        Args... args) {
@@ -111,7 +116,9 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, args...);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+  if (e == cudaSuccess) g_launch_count.fetch_add(1, std::memory_order_relaxed);
+  return e;
 }
 
 // Workspace plan shared by the C-ABI entry points and the launchers.
@@ -122,6 +129,7 @@ struct Plan {
   int32_t use_tc;                 // tensor-core scoring kernel
   int32_t tc_mt;                  // 128-row M tiles of the window rows (tensor-core path)
   int32_t tc_base_chunks;         // chunks in the smallest whole-tile unit (tensor-core path)
+  int32_t tc_tile_n;              // keys per tile of the tensor-core kernel
   int32_t n_groups;               // reuse groups of the call (scoring layers)
   size_t slot_bytes;              // one group's scratch: rl, bins, lse
   size_t off_rl, off_bins, off_lse;                 // inside a slot

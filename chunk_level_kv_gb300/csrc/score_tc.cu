@@ -2,10 +2,13 @@
 //
 // ChunkKV §4.1 Algorithm 1 steps 1-3 with the probabilities of Kara §2 Eq. (1),
 // in the single-pass unit decomposition described in score.cu: each work item
-// is one (scoring unit, 128-row M tile of the window rows).  Per item the CTA
-//   - loads the item's 128 packed window rows (Q) once by TMA,
+// is one (reuse group, scoring unit, 128-row M tile of the window rows), and one
+// persistent launch covers the items of every reuse group.  Per item the CTA
+//   - has the item's 128 packed window rows (Q) loaded by TMA and copied into
+//     TMEM (only when the tile differs from the previous item's),
 //   - streams the unit's keys in tiles of 80 through shared memory by TMA,
-//   - computes S = Q K^T (128 x 80, fp32) with tcgen05.mma into TMEM,
+//   - computes S = Q K^T (128 x 80, fp32) with tcgen05.mma (A in TMEM, B in
+//     shared memory) into one of two TMEM accumulator stages,
 //   - lets each of 128 softmax threads own one window row: it reads its row of
 //     S from TMEM, forms 2^(s*log2(e)/sqrt(d) - R) with R the row maximum of the
 //     item's first tile, and sums those per chunk (chunk boundaries are compile
@@ -14,11 +17,11 @@
 // A row whose values would outgrow the first-tile reference by more than 2^64
 // switches to the new maximum and rescales what it already wrote.
 //
-// Warp roles (256 threads): warp 0 = TMA producer, warp 1 = TMEM owner and MMA
-// issuer, warps 4-7 = softmax (warp 4+i reads TMEM lanes 32i..32i+31), warps 2-3
-// idle.  Two CTAs fit on one SM (104 KB shared memory, 256 TMEM columns each).
-// Every wait is bounded: a wait that runs out records an error code in the
-// workspace error word, raises a CTA-wide abort flag and the CTA drains and exits.
+// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = TMEM owner and MMA
+// issuer, warps 2-5 = softmax (warp w reads TMEM lanes 32*(w%4) .. +31).  Two
+// CTAs fit on one SM (112 KB shared memory, 256 TMEM columns each).  Every wait
+// is bounded: a wait that runs out records an error code in the workspace error
+// word, raises a CTA-wide abort flag and the CTA drains and exits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -31,10 +34,18 @@ namespace tc {
 
 constexpr int kN = 80;                         // keys per tile (MMA N)
 constexpr int kD = 128;                        // head dimension
-constexpr int kStagesK = 4;                    // K tiles in shared memory
+constexpr int kStagesK = (115712 - 2 * 128 * 128 - 256) / (2 * kN * 128) < 6
+                             ? (115712 - 2 * 128 * 128 - 256) / (2 * kN * 128) : 6;   // K tiles in shared memory (two CTAs per SM)
 constexpr int kStagesQ = 1;                    // Q tile in shared memory (reused across items)
-constexpr int kStagesT = 3;                    // accumulator stages in TMEM (3 x 80 columns)
+// The window-row tile lives in TMEM (columns 0..63, copied from shared memory
+// once per tile change) and feeds the MMAs as operand A, so that the tensor
+// core reads only the key tile from shared memory (with both operands there an
+// M=128, N=80 MMA asks for more shared-memory bandwidth than an SM has).  The
+// accumulators take the columns after it.
+constexpr int kQCols = 64;                     // 128 rows x 128 bf16 = 64 32-bit columns
+constexpr int kStagesT = (256 - kQCols) / kN < 3 ? (256 - kQCols) / kN : 3;   // accumulator stages in TMEM
 constexpr int kTmemCols = 256;
+static_assert(kStagesT >= 2 && kQCols + kStagesT * kN <= kTmemCols, "TMEM budget");
 constexpr int kThreads = 192;                  // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
 constexpr int kPanelQ = 128 * 128;             // one 64-element (128 B) panel of 128 rows
 constexpr int kPanelK = kN * 128;              // one 128 B panel of 80 key rows
@@ -103,11 +114,16 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
+// Test for the completion of the phase with the given parity; a thread whose
+// phase is still open is suspended in hardware until the phase completes or
+// kSuspendNs nanoseconds pass, instead of spinning on the issue slots that the
+// softmax warps of its SM sub-partition need.
+constexpr uint32_t kSuspendNs = 1000000;
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok) : "r"(bar), "r"(parity), "r"(kSuspendNs) : "memory");
   return ok != 0;
 }
 
@@ -151,10 +167,15 @@ __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t acc) {
+// D (+)= A B^T with A (128 x 16 bf16) in TMEM at a_tmem (row m in lane m, element pairs per column).
+__device__ __forceinline__ void tc_mma_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t acc) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}"
-      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(acc) : "memory");
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(kIdesc), "r"(acc) : "memory");
+}
+// 128 rows x 32 bytes from shared memory (matrix descriptor) into 128 lanes x 8 TMEM columns.
+__device__ __forceinline__ void tc_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row groups 1024 B apart.
@@ -262,28 +283,27 @@ __device__ __forceinline__ void tile_seg(const uint32_t (&r)[16], float2 alpha2,
   s.carry = acc;
 }
 
-// One 80-column tile: the whole row segment is loaded from TMEM first (five
-// x16 loads, one wait), so the 40 column pairs are independent work that the
-// scheduler can interleave freely.
+template <int C, int PH, int SEG, bool MASK>
+__device__ __forceinline__ void tile_segs(const uint32_t (&r)[kN / 16][16], float2 alpha, RowState& s, float* bin,
+                                          int wG, int valid, bool write, uint64_t pol) {
+  if constexpr (SEG < kN / 16) {
+    tile_seg<C, PH, SEG, MASK>(r[SEG], alpha, s, bin, wG, valid, write, pol);
+    tile_segs<C, PH, SEG + 1, MASK>(r, alpha, s, bin, wG, valid, write, pol);
+  }
+}
+
+// One tile of kN columns: the whole row segment is loaded from TMEM first
+// (kN/16 x16 loads, one wait), so the column pairs are independent work that
+// the scheduler can interleave freely.
 template <int C, int PH, bool MASK>
 __device__ __forceinline__ void tile_phase(uint32_t taddr, float2 alpha, RowState& s, float* bin, int wG, int valid,
                                            bool write, uint64_t pol) {
-  uint32_t a[16], b[16], c[16], d[16], e[16];
-  tmem_ld16(taddr, a);
-  tmem_ld16(taddr + 16, b);
-  tmem_ld16(taddr + 32, c);
-  tmem_ld16(taddr + 48, d);
-  tmem_ld16(taddr + 64, e);
-  tmem_wait16(a);
-  tmem_wait16(b);
-  tmem_wait16(c);
-  tmem_wait16(d);
-  tmem_wait16(e);
-  tile_seg<C, PH, 0, MASK>(a, alpha, s, bin, wG, valid, write, pol);
-  tile_seg<C, PH, 1, MASK>(b, alpha, s, bin, wG, valid, write, pol);
-  tile_seg<C, PH, 2, MASK>(c, alpha, s, bin, wG, valid, write, pol);
-  tile_seg<C, PH, 3, MASK>(d, alpha, s, bin, wG, valid, write, pol);
-  tile_seg<C, PH, 4, MASK>(e, alpha, s, bin, wG, valid, write, pol);
+  uint32_t r[kN / 16][16];
+#pragma unroll
+  for (int sg = 0; sg < kN / 16; ++sg) tmem_ld16(taddr + 16 * sg, r[sg]);
+#pragma unroll
+  for (int sg = 0; sg < kN / 16; ++sg) tmem_wait16(r[sg]);
+  tile_segs<C, PH, 0, MASK>(r, alpha, s, bin, wG, valid, write, pol);
 }
 
 template <int C, int PH = 0>
@@ -335,7 +355,8 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
   uint64_t* k_empty = k_full + kStagesK;                       // [kStagesK]
   uint64_t* t_full = k_empty + kStagesK;                       // [kStagesT]
   uint64_t* t_empty = t_full + kStagesT;                       // [kStagesT]
-  uint32_t* tmem_slot = (uint32_t*)(t_empty + kStagesT);
+  uint64_t* qt_done = t_empty + kStagesT;                      // [1] MMAs of the old TMEM window tile / its copy done
+  uint32_t* tmem_slot = (uint32_t*)(qt_done + 1);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -343,6 +364,7 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
     for (int i = 0; i < kStagesQ; ++i) { mbar_init(smem_u32(&q_full[i]), 1); mbar_init(smem_u32(&q_empty[i]), 1); }
     for (int i = 0; i < kStagesK; ++i) { mbar_init(smem_u32(&k_full[i]), 1); mbar_init(smem_u32(&k_empty[i]), 1); }
     for (int i = 0; i < kStagesT; ++i) { mbar_init(smem_u32(&t_full[i]), 1); mbar_init(smem_u32(&t_empty[i]), 128); }
+    mbar_init(smem_u32(&qt_done[0]), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&maps.q) : "memory");
@@ -409,7 +431,7 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
-      uint32_t kc = 0, qc = 0, tc = 0;
+      uint32_t kc = 0, qc = 0, tc = 0, qtc = 0;
       int qkey = -1;
       const uint32_t qaddr = smem_u32(sQ);
       for (int item = blockIdx.x; item < g.n_items && !*abort_flag; item += gridDim.x) {
@@ -417,8 +439,21 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
         const int ntile = it.ntile;
         const int key = it.key;
         if (key != qkey) {
-          if (qkey >= 0) tc_commit(smem_u32(&q_empty[0]));     // old Q free once its MMAs finish
+          // the TMEM tile is overwritten only after the MMAs that read it are done
+          if (qkey >= 0) {
+            tc_commit(smem_u32(&qt_done[0]));
+            if (!wait_bar(ctl, smem_u32(&qt_done[0]), qtc & 1, kDevTimeoutMma)) break;
+            ++qtc;
+          }
           if (!wait_bar(ctl, smem_u32(&q_full[0]), qc & 1, kDevTimeoutMma)) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk)      // 16 elements (32 B of each row) per copy
+            tc_cp_128x256b(tmem + kk * 8, sw128_desc(qaddr + (kk >> 2) * kPanelQ + (kk & 3) * 32));
+          tc_commit(smem_u32(&q_empty[0]));                    // shared-memory tile free once copied
+          tc_commit(smem_u32(&qt_done[0]));
+          if (!wait_bar(ctl, smem_u32(&qt_done[0]), qtc & 1, kDevTimeoutMma)) break;
+          ++qtc;
           tc_fence_after();
           ++qc;
           qkey = key;
@@ -433,13 +468,12 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
           }
           tc_fence_after();
           const uint32_t kaddr = smem_u32(sK + ks * kKBytes);
-          const uint32_t d = tmem + ts * kN;
+          const uint32_t d = tmem + kQCols + ts * kN;
 #pragma unroll
           for (int kk = 0; kk < kD / 16; ++kk) {
             const uint32_t off = (kk & 3) * 32;                  // 16 bf16 = 32 B inside the swizzle atom
-            const uint64_t ad = sw128_desc(qaddr + (kk >> 2) * kPanelQ + off);
             const uint64_t bd = sw128_desc(kaddr + (kk >> 2) * kPanelK + off);
-            tc_mma(d, ad, bd, kk > 0 ? 1u : 0u);
+            tc_mma_ta(d, tmem + kk * 8, bd, kk > 0 ? 1u : 0u);
           }
           tc_commit(smem_u32(&k_empty[ks]));
           tc_commit(smem_u32(&t_full[ts]));
@@ -478,7 +512,7 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
         }
         tc_fence_after();
         if (warp_live) {
-          const uint32_t taddr = lane_base + ts * kN;
+          const uint32_t taddr = lane_base + kQCols + ts * kN;
           const int valid = min(kN, nk - t * kN);
           if (t == 0) {
             R = tile_max(taddr, valid) * g.alpha;
@@ -655,6 +689,7 @@ void tc_plan(Plan& pl) {
   pl.use_tc = 1;
   pl.tc_mt = (pl.wG + 127) / 128;
   pl.tc_base_chunks = tc::lcm_i(tc::kN, pl.c) / pl.c;
+  pl.tc_tile_n = tc::kN;
   pl.cpu = pl.tc_base_chunks * std::max(1, 640 / tc::lcm_i(tc::kN, pl.c));
 }
 

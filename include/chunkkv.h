@@ -192,6 +192,14 @@ const char* chunkkv_status_string(chunkkv_status s);
 /* Which scoring kernel chunkkv_score would use for these shapes: 0 = SIMT, 1 = tensor-core. */
 int32_t chunkkv_score_path(const chunkkv_params* p);
 
+/*
+ * Number of CUDA kernels this process has launched through the library so far
+ * (every entry point, every device and host thread; a relaxed atomic counter
+ * that only grows).  The difference of two readings around a region counts the
+ * library's kernel launches in it.  Never fails.
+ */
+uint64_t chunkkv_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -75,6 +75,9 @@ def test_tiny_fp32_exact(ckv):
     (4500, 30, 64, 28, 4, 900),      # c = 30, G = 7, window rows 448
     (1777, 1, 8, 4, 2, 100),         # token-level selection (c = 1)
     (640, 7, 5, 6, 2, 70),           # odd chunk, odd window
+    (5000, 10, 48, 40, 8, 500),      # window rows 240: two M tiles in one CTA, the second partly padding
+    (2500, 5, 40, 32, 4, 300),       # window rows 320: three M tiles, the last CTA's second tile all padding
+    (3333, 16, 64, 16, 2, 512),      # window rows 512: four full M tiles, c = 16
 ])
 def test_bf16_shapes(ckv, T, c, w, Hq, Hkv, L_max):
     wl = configs.llama_layer().with_params(seqlens=(T,), c=c, w=w, Hq=Hq, Hkv=Hkv, L_max=L_max,
@@ -103,11 +106,27 @@ def test_degenerate_parameters(ckv, kw):
         assert n == 1234 and torch.equal(out.indices[0, 0, 0, :n].cpu(), torch.arange(1234, dtype=torch.int32))
 
 
-def test_layer_reuse_groups(ckv):
-    wl = configs.llama_model().with_params(seqlens=(2048,), n_layers=5, n_reuse=2, L_max=409,
-                                           name="reuse5")
+@pytest.mark.parametrize("Hq,Hkv,w", [(32, 8, 32), (28, 4, 64)])
+def test_layer_reuse_groups(ckv, Hq, Hkv, w):
+    # one scoring launch covers the three reuse groups (one and two M tiles per CTA)
+    wl = configs.llama_model().with_params(seqlens=(2048,), n_layers=5, n_reuse=2, L_max=409, Hq=Hq, Hkv=Hkv,
+                                           w=w, name=f"reuse5_G{Hq // Hkv}_w{w}")
     out, _ = run_and_check(ckv, wl)
     assert out.indices.shape[0] == 3
+
+
+def test_one_launch_per_phase(ckv):
+    # pack, score (all reuse groups), log-sum-exp, finalize, select, gather (all layers)
+    wl = configs.llama_model().with_params(seqlens=(3000,), n_layers=6, n_reuse=2, L_max=600, name="phases")
+    qs, ks, vs, _ = gen.make_all_layers(wl, DEV)
+    ckv.compress_layers(qs, ks, vs, wl.cu_seqlens, Hq=wl.Hq, Hkv=wl.Hkv, w=wl.w, c=wl.c, L_max=wl.L_max,
+                        n_reuse=wl.n_reuse)
+    torch.cuda.synchronize()
+    n0 = ckv.chunkkv_launch_count()
+    out = ckv.compress_layers(qs, ks, vs, wl.cu_seqlens, Hq=wl.Hq, Hkv=wl.Hkv, w=wl.w, c=wl.c, L_max=wl.L_max,
+                              n_reuse=wl.n_reuse)
+    assert ckv.chunkkv_launch_count() - n0 == 6
+    assert ckv.chunkkv_status_check(out.workspace) == 0
 
 
 def test_select_is_bit_exact_on_given_scores(ckv):

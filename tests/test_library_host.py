@@ -25,13 +25,22 @@ def ckv():
 
 def test_exports_every_declared_function(ckv):
     text = open(HEADER).read()
-    names = set(re.findall(r"^\s*(?:const\s+char\*|chunkkv_status|int32_t)\s+(chunkkv_\w+)\s*\(", text,
+    names = set(re.findall(r"^\s*(?:const\s+char\*|chunkkv_status|int32_t|uint64_t)\s+(chunkkv_\w+)\s*\(", text,
                            flags=re.M))
     assert {"chunkkv_score", "chunkkv_select", "chunkkv_gather", "chunkkv_compress_layers",
             "chunkkv_workspace_size", "chunkkv_out_capacity", "chunkkv_status_check"} <= names
     lib = ctypes.CDLL(LIBPATH)
     for n in sorted(names):
         assert hasattr(lib, n), n
+
+
+def test_launch_counter_only_counts_launches(ckv):
+    n0 = ckv.chunkkv_launch_count()
+    assert isinstance(n0, int) and n0 >= 0
+    p, keep = _p(ckv)
+    ckv.chunkkv_workspace_size(p, 4, 2)            # host-side sizing launches nothing
+    ckv.chunkkv_out_capacity(p)
+    assert ckv.chunkkv_launch_count() == n0
 
 
 def test_status_strings(ckv):
