@@ -13,6 +13,7 @@ the same metric.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -108,6 +109,63 @@ def algorithmic_bytes(wl, counts) -> int:
     return k_read + q_read + 4 * kept * wl.d * elt
 
 
+def traffic_record(kernel: str):
+    """DRAM bytes per full launch of `kernel` from the committed ncu summary, if its source is unchanged."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f).get(kernel)
+        with open(os.path.join(ROOT, rec["source"]), "rb") as f:
+            digest = hashlib.sha256(f.read()).hexdigest()
+        return rec["bytes_per_launch"] if digest == rec["source_sha256"] else None
+    except Exception:
+        return None
+
+
+def phase_rooflines(wl, counts, phase_ms, peaks, peak_src, path):
+    """Roofline of the scoring, finalisation and gather launches of one compress step.
+
+    Algorithmic amounts per launch (all layers / reuse groups of the step):
+      score:    K of every scoring layer read once (T_total*Hkv*d*elt per group) and
+                2*w*G*T_total*Hkv*d flops; the roof is whichever takes longer at peak
+                (HBM copy bandwidth, or the sustained bf16 tensor rate);
+      finalize: one fp32 bin per (chunk, window row, KV head) per group read once;
+      gather:   kept K and V rows read and written (4*kept*d*elt per layer).
+    """
+    elt = 2 if wl.dtype == "bf16" else 4
+    groups = -(-wl.n_layers // wl.n_reuse)
+    cnt = counts.to("cpu").numpy().astype(np.int64)
+    kept_all = sum(int(cnt[layer // wl.n_reuse].sum()) for layer in range(wl.n_layers))
+    chunks = sum(-(-(wl.cu_seqlens[b + 1] - wl.cu_seqlens[b]) // wl.c) for b in range(wl.B))
+    hbm = peaks["hbm_gbs"]
+    tensor = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    out = []
+
+    def hbm_roof(phase, kernel, nbytes):
+        ms = phase_ms[phase]
+        ach = nbytes / (ms * 1e-3) / 1e9
+        return {"phase": phase, "kernel": kernel, "bound": "hbm", "achieved": round(ach, 2), "peak": hbm,
+                "unit": "GB/s", "frac": round(ach / hbm, 4), "traffic": traffic_record(kernel),
+                "algorithmic_bytes": int(nbytes), "avg_launch_ms": round(ms, 5),
+                "peak_source": f"{peak_src} hbm_gbs"}
+
+    score_bytes = groups * wl.T_total * wl.Hkv * wl.d * elt
+    score_flops = 2.0 * groups * wl.w * wl.G * wl.T_total * wl.Hkv * wl.d
+    kernel = "score_tc_kernel" if path == 1 else "score_simt_kernel"
+    if path == 1 and score_flops / (tensor * 1e12) > score_bytes / (hbm * 1e9):
+        ms = phase_ms["score"]
+        ach = score_flops / (ms * 1e-3) / 1e12
+        out.append({"phase": "score", "kernel": kernel, "bound": "tensor", "achieved": round(ach, 2),
+                    "peak": tensor, "unit": "TFLOP/s", "frac": round(ach / tensor, 4),
+                    "traffic": traffic_record(kernel), "algorithmic_flops": score_flops,
+                    "algorithmic_bytes": int(score_bytes), "avg_launch_ms": round(ms, 5),
+                    "peak_source": f"{peak_src} bf16_tflops_sustained"})
+    else:
+        out.append(hbm_roof("score", kernel, score_bytes))
+    out.append(hbm_roof("finalize", "finalize_kernel", groups * chunks * wl.Hkv * wl.w * wl.G * 4))
+    out.append(hbm_roof("gather", "gather_kernel", 4 * kept_all * wl.d * elt))
+    return out
+
+
 def run_gpu(args):
     import chunk_level_kv_gb300 as ckv
     ws_n, rank, local = dist_env()
@@ -172,24 +230,24 @@ def run_gpu(args):
     value = nbytes * ws_n / (step_ms * 1e-3) / 1e9
     tokens_s = wl.T_total * ws_n / (step_ms * 1e-3)
 
-    # ---- per-stage device time of the dominant kernel (window scoring), same stream, same data
-    score_ms = []
-    sc = torch.empty(wl.B, wl.Hkv, max(C_max, 1), device=dev)
-    ckv.chunkkv_score(p, qs[0], ks[0], sc, ws)
-    for layer in range(0, wl.n_layers, wl.n_reuse):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        ckv.chunkkv_score(p, qs[layer], ks[layer], sc, ws)
-        e1.record(stream)
-        score_ms.append((e0, e1))
-    torch.cuda.synchronize()
-    score_avg = sum(a.elapsed_time(b) for a, b in score_ms) / len(score_ms)
+    # ---- device time of each phase inside the same compress call: K more steps with the library's
+    # phase events recorded on its stream (a record between two launches ends their overlap, so these
+    # steps are not the headline ones)
     peaks, peak_src = measured_peaks()
-    elt = 2 if wl.dtype == "bf16" else 4
-    score_bytes = wl.T_total * wl.Hkv * wl.d * elt + wl.B * wl.w * wl.Hq * wl.d * elt
     path = ckv.chunkkv_score_path(p)
-    roof_peak = peaks["hbm_gbs"]
-    achieved = score_bytes / (score_avg * 1e-3) / 1e9
+    n_ev = len(ckv.PHASES) + 1
+    phase_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
+    for evs in phase_evs:
+        if flush is not None:
+            flush.fill_(1.0)
+        ckv.chunkkv_set_phase_events(evs)
+        step()
+    ckv.chunkkv_set_phase_events(None)
+    torch.cuda.synchronize()
+    phase_ms = {name: sum(evs[i].elapsed_time(evs[i + 1]) for evs in phase_evs) / len(phase_evs)
+                for i, name in enumerate(ckv.PHASES)}
+    roofs = phase_rooflines(wl, cnt, phase_ms, peaks, peak_src, path)
+    dominant = max(roofs, key=lambda r: phase_ms[r["phase"]])
 
     # ---- end to end through the C-ABI with host buffers (pinned), copies inside the timed region
     e2e = None
@@ -253,10 +311,9 @@ def run_gpu(args):
         "tokens_per_s": round(tokens_s, 1),
         "algorithmic_bytes_per_step": nbytes,
         "hbm_roof_frac": round(value / ws_n / peaks["hbm_gbs"], 4),
-        "roofline": {"kernel": "window scoring (chunkkv_score: " + ("tcgen05" if path == 1 else "SIMT") +
-                     " + finalize)", "bound": "hbm", "achieved": round(achieved, 2), "peak": roof_peak,
-                     "unit": "GB/s", "frac": round(achieved / roof_peak, 4), "traffic": None,
-                     "peak_source": f"{peak_src} hbm_gbs", "avg_launch_ms": round(score_avg, 5)},
+        "roofline": dominant,
+        "roofline_score": next(r for r in roofs if r["phase"] == "score"),
+        "phases_ms": {k: round(v, 5) for k, v in phase_ms.items()},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": int(launches),

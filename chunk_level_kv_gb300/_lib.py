@@ -49,6 +49,7 @@ def _load():
         "chunkkv_status_check": [vp, vp, ctypes.POINTER(i32)],
         "chunkkv_score_path": [P],
         "chunkkv_score_noalloc": [P, vp, vp, vp, vp],
+        "chunkkv_set_phase_events": [pp, i32],
     }
     for name, args in sigs.items():
         fn = getattr(lib, name)

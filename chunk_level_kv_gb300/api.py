@@ -93,6 +93,23 @@ def chunkkv_launch_count() -> int:
     return int(LIB.chunkkv_launch_count())
 
 
+PHASE_EVENTS = 7          # CHUNKKV_PHASE_EVENTS
+PHASES = ("pack", "score", "lse", "finalize", "select", "gather")
+
+
+def chunkkv_set_phase_events(events) -> None:
+    """None (off) or PHASE_EVENTS torch.cuda.Event objects that later compress calls of this
+    thread record at their phase boundaries (each event is recorded once here so that it exists)."""
+    if events is None:
+        _check("chunkkv_set_phase_events", LIB.chunkkv_set_phase_events(None, 0))
+        return
+    for e in events:
+        if not e.cuda_event:
+            e.record()
+    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    _check("chunkkv_set_phase_events", LIB.chunkkv_set_phase_events(arr, len(events)))
+
+
 def chunkkv_score(p: Params, q_win, k, chunk_scores, ws) -> None:
     _check("chunkkv_score", LIB.chunkkv_score(ctypes.byref(p), _ptr(q_win), _ptr(k), _ptr(chunk_scores),
                                               _ptr(ws), ws.numel() * ws.element_size(), _stream(k.device)))

@@ -188,11 +188,23 @@ cudaError_t run_score_groups(const Plan& pl, const ScoreGeom& g, const SeqTable&
 }
 
 // Log-sum-exp and finalisation of n_groups consecutive slots into their chunk scores.
+// Phase events of chunkkv_set_phase_events (this host thread), recorded only
+// inside chunkkv_compress_layers.
+thread_local void* t_phase_ev[CHUNKKV_PHASE_EVENTS];
+thread_local int t_phase_n = 0;
+thread_local bool t_in_compress = false;
+
+cudaError_t phase_mark(int i, cudaStream_t s) {
+  if (!t_in_compress || t_phase_n == 0) return cudaSuccess;
+  return cudaEventRecord((cudaEvent_t)t_phase_ev[i], s);
+}
+
 cudaError_t run_post_score(const Plan& pl, const ScoreGeom& g, const SeqTable& st, char* slots, float* scores,
                            int n_groups, cudaStream_t s) {
   float* rl = (float*)(slots + pl.off_rl);
   float* lse = (float*)(slots + pl.off_lse);
   cudaError_t e = launch_lse(g, st, rl, lse, n_groups, s);
+  if (e == cudaSuccess) e = phase_mark(3, s);
   if (e != cudaSuccess) return e;
   return launch_finalize(pl, g, st, rl, (const float*)(slots + pl.off_bins), lse, scores, n_groups, s);
 }
@@ -389,6 +401,10 @@ chunkkv_status chunkkv_compress_layers(const chunkkv_params* p, int32_t n_layers
   //  4. top-k selection and index build of every (group, sequence, head) in one launch;
   //  5. the gather of every layer (layer l with index group l / n_reuse).
   cudaError_t e = cudaSuccess;
+  struct InCompress {                   // phase events are recorded only inside this call
+    InCompress() { t_in_compress = true; }
+    ~InCompress() { t_in_compress = false; }
+  } in_compress;
   static thread_local std::vector<const void*> qsel, ksel;
   qsel.resize(n_groups);
   ksel.resize(n_groups);
@@ -396,17 +412,36 @@ chunkkv_status chunkkv_compress_layers(const chunkkv_params* p, int32_t n_layers
     qsel[i] = q_win[i * n_reuse];
     ksel[i] = k[i * n_reuse];
   }
-  if (pl.use_tc && pl.wG > 0) e = launch_pack_q(pl, g, qsel.data(), n_groups, base + pl.off_qpack, cs);
+  e = phase_mark(0, cs);
+  if (e == cudaSuccess && pl.use_tc && pl.wG > 0) e = launch_pack_q(pl, g, qsel.data(), n_groups, base + pl.off_qpack, cs);
+  if (e == cudaSuccess) e = phase_mark(1, cs);
   if (e == cudaSuccess)
     e = run_score_groups(pl, g, st, qsel.data(), ksel.data(), n_groups, base + pl.off_slots, base + pl.off_qpack, (int32_t*)w, cs);
+  if (e == cudaSuccess) e = phase_mark(2, cs);
   if (e == cudaSuccess) e = run_post_score(pl, g, st, base + pl.off_slots, scores, n_groups, cs);
+  if (e == cudaSuccess) e = phase_mark(4, cs);
   if (e == cudaSuccess) {
     SelectGeom sg = select_geom(p, pl);
     sg.scores_gs = g.scores_gs;
     e = launch_select(pl, sg, st, scores, indices, counts, n_groups, cs);
   }
+  if (e == cudaSuccess) e = phase_mark(5, cs);
   if (e == cudaSuccess) e = run_gather(p, pl, st, n_layers, n_reuse, k, v, k_out, v_out, indices, counts, cs);
+  if (e == cudaSuccess) e = phase_mark(6, cs);
   return cuda_status(e);
+}
+
+chunkkv_status chunkkv_set_phase_events(void* const* events, int32_t n_events) {
+  if (n_events == 0) {
+    t_phase_n = 0;
+    return CHUNKKV_OK;
+  }
+  if (n_events != CHUNKKV_PHASE_EVENTS || events == nullptr) return CHUNKKV_ERR_INVALID_ARG;
+  for (int i = 0; i < CHUNKKV_PHASE_EVENTS; ++i)
+    if (events[i] == nullptr) return CHUNKKV_ERR_INVALID_ARG;
+  for (int i = 0; i < CHUNKKV_PHASE_EVENTS; ++i) t_phase_ev[i] = events[i];
+  t_phase_n = CHUNKKV_PHASE_EVENTS;
+  return CHUNKKV_OK;
 }
 
 uint64_t chunkkv_launch_count(void) { return chunkkv::g_launch_count.load(std::memory_order_relaxed); }

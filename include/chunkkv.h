@@ -200,6 +200,23 @@ int32_t chunkkv_score_path(const chunkkv_params* p);
  */
 uint64_t chunkkv_launch_count(void);
 
+/*
+ * Phase timing of chunkkv_compress_layers (a measurement aid).
+ *   events: HOST array of CHUNKKV_PHASE_EVENTS cudaEvent_t handles (as void*)
+ *           that the caller created and keeps alive; NULL with n_events = 0
+ *           switches recording off.
+ * While set, each chunkkv_compress_layers call made by the same host thread
+ * records events[i] on its stream at phase boundary i: 0 before the window-row
+ * packing, 1 before scoring, 2 before the log-sum-exp, 3 before the
+ * finalisation, 4 before the top-k selection, 5 before the gather, 6 after the
+ * gather.  A record between two launches ends the programmatic-dependent-launch
+ * overlap there, so recorded calls run a little slower than unrecorded ones.
+ * Returns CHUNKKV_ERR_INVALID_ARG if n_events is neither 0 nor
+ * CHUNKKV_PHASE_EVENTS or a handle is NULL (the previous setting then stays).
+ */
+#define CHUNKKV_PHASE_EVENTS 7
+chunkkv_status chunkkv_set_phase_events(void* const* events, int32_t n_events);
+
 #ifdef __cplusplus
 }
 #endif

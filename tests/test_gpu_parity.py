@@ -129,6 +129,24 @@ def test_one_launch_per_phase(ckv):
     assert ckv.chunkkv_status_check(out.workspace) == 0
 
 
+def test_phase_events_mark_every_phase(ckv):
+    wl = configs.llama_model().with_params(seqlens=(3000,), n_layers=4, n_reuse=2, L_max=600, name="phase_events")
+    qs, ks, vs, _ = gen.make_all_layers(wl, DEV)
+    kw = dict(Hq=wl.Hq, Hkv=wl.Hkv, w=wl.w, c=wl.c, L_max=wl.L_max, n_reuse=wl.n_reuse)
+    ref = ckv.compress_layers(qs, ks, vs, wl.cu_seqlens, **kw)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(ckv.PHASES) + 1)]
+    ckv.chunkkv_set_phase_events(evs)
+    try:
+        out = ckv.compress_layers(qs, ks, vs, wl.cu_seqlens, **kw)
+    finally:
+        ckv.chunkkv_set_phase_events(None)
+    torch.cuda.synchronize()
+    times = [evs[i].elapsed_time(evs[i + 1]) for i in range(len(ckv.PHASES))]
+    assert all(t >= 0 for t in times) and times[1] > 0 and times[-1] > 0
+    assert torch.equal(out.indices, ref.indices) and torch.equal(out.counts, ref.counts)
+    assert all(torch.equal(a, b) for a, b in zip(out.k_out, ref.k_out))
+
+
 def test_select_is_bit_exact_on_given_scores(ckv):
     # both sides decide on the same fp32 scores: the selection must match exactly (ties included)
     rng = np.random.default_rng(0)

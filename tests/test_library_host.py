@@ -43,6 +43,14 @@ def test_launch_counter_only_counts_launches(ckv):
     assert ckv.chunkkv_launch_count() == n0
 
 
+def test_phase_events_argument_checks(ckv):
+    from chunk_level_kv_gb300._lib import LIB
+    arr = (ctypes.c_void_p * 7)()                      # NULL handles
+    assert LIB.chunkkv_set_phase_events(arr, 7) == 1
+    assert LIB.chunkkv_set_phase_events(arr, 3) == 1
+    assert LIB.chunkkv_set_phase_events(None, 0) == 0
+
+
 def test_status_strings(ckv):
     from chunk_level_kv_gb300._lib import LIB
     for code in range(6):
