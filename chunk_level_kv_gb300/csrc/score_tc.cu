@@ -147,9 +147,9 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap
       "[%0], [%1, {%3, %4, %5}], [%2], %6;"
       ::"r"(dst), "l"((uint64_t)map), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "l"(policy) : "memory");
 }
-__device__ __forceinline__ uint64_t policy_evict_first() {
+__device__ __forceinline__ uint64_t policy_evict_normal() {
   uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
 __device__ __forceinline__ uint64_t policy_evict_last() {
@@ -386,7 +386,9 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
     if (lane == 0) {
       uint32_t kc = 0, qc = 0;
       int qkey = -1;                                   // (group, sequence, head, M tile) of the loaded Q
-      const uint64_t kpol = policy_evict_first();      // keys are streamed once per M tile
+      // keys: normal priority, since the CTAs of the other M tiles of the same
+      // (unit, head) read each key tile too (evict-first cost re-reads from HBM)
+      const uint64_t kpol = policy_evict_normal();
       bool ok = true;
       for (int item = blockIdx.x; item < g.n_items && ok && !*abort_flag; item += gridDim.x) {
         const Item it = decode_item(g, st, item);
