@@ -109,14 +109,23 @@ def algorithmic_bytes(wl, counts) -> int:
     return k_read + q_read + 4 * kept * wl.d * elt
 
 
-def traffic_record(kernel: str):
-    """DRAM bytes per full launch of `kernel` from the committed ncu summary, if its source is unchanged."""
+def sources_digest(paths) -> str:
+    h = hashlib.sha256()
+    for rel in paths:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def traffic_record(workload: str, kernel: str):
+    """DRAM read + write bytes per full launch of `kernel` on `workload`, from the committed one-pass
+    ncu capture (profiles/traffic.json), or None if the kernel's sources changed since."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-            rec = json.load(f).get(kernel)
-        with open(os.path.join(ROOT, rec["source"]), "rb") as f:
-            digest = hashlib.sha256(f.read()).hexdigest()
-        return rec["bytes_per_launch"] if digest == rec["source_sha256"] else None
+            rec = json.load(f)["workloads"][workload][kernel]
+        if sources_digest(rec["sources"]) != rec["sources_sha256"]:
+            return None
+        return int(rec["dram_read_bytes"]) + int(rec["dram_write_bytes"])
     except Exception:
         return None
 
@@ -144,7 +153,7 @@ def phase_rooflines(wl, counts, phase_ms, peaks, peak_src, path):
         ms = phase_ms[phase]
         ach = nbytes / (ms * 1e-3) / 1e9
         return {"phase": phase, "kernel": kernel, "bound": "hbm", "achieved": round(ach, 2), "peak": hbm,
-                "unit": "GB/s", "frac": round(ach / hbm, 4), "traffic": traffic_record(kernel),
+                "unit": "GB/s", "frac": round(ach / hbm, 4), "traffic": traffic_record(wl.name, kernel),
                 "algorithmic_bytes": int(nbytes), "avg_launch_ms": round(ms, 5),
                 "peak_source": f"{peak_src} hbm_gbs"}
 
@@ -156,7 +165,7 @@ def phase_rooflines(wl, counts, phase_ms, peaks, peak_src, path):
         ach = score_flops / (ms * 1e-3) / 1e12
         out.append({"phase": "score", "kernel": kernel, "bound": "tensor", "achieved": round(ach, 2),
                     "peak": tensor, "unit": "TFLOP/s", "frac": round(ach / tensor, 4),
-                    "traffic": traffic_record(kernel), "algorithmic_flops": score_flops,
+                    "traffic": traffic_record(wl.name, kernel), "algorithmic_flops": score_flops,
                     "algorithmic_bytes": int(score_bytes), "avg_launch_ms": round(ms, 5),
                     "peak_source": f"{peak_src} bf16_tflops_sustained"})
     else:
