@@ -16,7 +16,7 @@ void tc_plan(Plan& pl);                                             // score_tc.
 cudaError_t launch_pack_q(const Plan& pl, const ScoreGeom& g, const void* const* q_layers, int n_layers,
                           void* qpack, cudaStream_t s);
 cudaError_t launch_score_tc(const Plan& pl, const ScoreGeom& g, const SeqTable& st, const void* const* k_groups,
-                            int n_groups, int64_t slot_gs, float* rl, float* bins, const void* qpack, int32_t* err,
+                            int n_groups, int64_t slot_bytes, float* rl, bin_t* bins, const void* qpack, int32_t* err,
                             cudaStream_t s);
 
 namespace {
@@ -123,7 +123,7 @@ chunkkv_status make_plan(const chunkkv_params* p, int n_layers, int n_reuse, Pla
   if (units * p->Hkv > INT32_MAX / 2) return CHUNKKV_ERR_UNSUPPORTED;
   pl.n_units = (int32_t)(units * p->Hkv);
   const size_t rl = align_up((size_t)pl.n_units * 2 * pl.wG * sizeof(float));
-  const size_t bins = align_up((size_t)pl.n_units * pl.cpu * pl.wG * sizeof(float));
+  const size_t bins = align_up((size_t)pl.n_units * pl.cpu * pl.wG * sizeof(bin_t));
   const size_t lse = align_up((size_t)p->B * p->Hkv * pl.wG * sizeof(float));
   pl.n_groups = n_layers > 0 ? (n_layers + n_reuse - 1) / n_reuse : 1;
   // Workspace: [header | one scratch slot per reuse group | packed window rows
@@ -163,7 +163,8 @@ ScoreGeom score_geom(const chunkkv_params* p, const Plan& pl) {
   g.q_stride_h = p->q_stride_h;
   g.kv_stride_t = p->kv_stride_t;
   g.kv_stride_h = p->kv_stride_h;
-  g.rl_gs = g.bins_gs = g.lse_gs = (int64_t)(pl.slot_bytes / sizeof(float));
+  g.rl_gs = g.lse_gs = (int64_t)(pl.slot_bytes / sizeof(float));
+  g.bins_gs = (int64_t)(pl.slot_bytes / sizeof(bin_t));
   g.scores_gs = (int64_t)(pl.scores_group_bytes / sizeof(float));
   return g;
 }
@@ -177,11 +178,12 @@ cudaError_t run_score_groups(const Plan& pl, const ScoreGeom& g, const SeqTable&
                              const void* const* k, int n_groups, char* slots, const void* qpack, int32_t* err,
                              cudaStream_t s) {
   float* rl = (float*)(slots + pl.off_rl);
-  float* bins = (float*)(slots + pl.off_bins);
+  bin_t* bins = (bin_t*)(slots + pl.off_bins);
   const int64_t slot_gs = (int64_t)(pl.slot_bytes / sizeof(float));
-  if (pl.use_tc) return launch_score_tc(pl, g, st, k, n_groups, slot_gs, rl, bins, qpack, err, s);
+  if (pl.use_tc) return launch_score_tc(pl, g, st, k, n_groups, (int64_t)pl.slot_bytes, rl, bins, qpack, err, s);
   for (int i = 0; i < n_groups; ++i) {
-    cudaError_t e = launch_score_simt(pl, g, st, q[i], k[i], rl + i * slot_gs, bins + i * slot_gs, s);
+    cudaError_t e = launch_score_simt(pl, g, st, q[i], k[i], rl + i * slot_gs,
+                                      (bin_t*)((char*)bins + i * pl.slot_bytes), s);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -206,7 +208,7 @@ cudaError_t run_post_score(const Plan& pl, const ScoreGeom& g, const SeqTable& s
   cudaError_t e = launch_lse(g, st, rl, lse, n_groups, s);
   if (e == cudaSuccess) e = phase_mark(3, s);
   if (e != cudaSuccess) return e;
-  return launch_finalize(pl, g, st, rl, (const float*)(slots + pl.off_bins), lse, scores, n_groups, s);
+  return launch_finalize(pl, g, st, rl, (const bin_t*)(slots + pl.off_bins), lse, scores, n_groups, s);
 }
 
 SelectGeom select_geom(const chunkkv_params* p, const Plan& pl) {

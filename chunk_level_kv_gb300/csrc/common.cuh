@@ -16,6 +16,22 @@ namespace chunkkv {
 constexpr int kMaxWG = 4096;          // window rows per KV head, w * G
 constexpr int kMaxD = 256;            // head dimension
 
+// Chunk bins are stored as 16-bit unsigned floats: 6 exponent bits and 10
+// mantissa bits, covering [2^-40, 2^24) of the row reference (code 0 is zero).
+// A bin is a sum of 2^(t - R) >= 0 over one chunk, at most the row sum l, which
+// the scoring kernels keep below 2^24; the encoding rounds half up at the 11th
+// significant bit, a relative error of at most 2^-11, and flushes bins below
+// 2^-40 of the reference to zero.
+using bin_t = uint16_t;
+constexpr uint32_t kBinExpBias = 87;                  // fp32 exponent field of 2^-40
+__device__ __forceinline__ bin_t bin_encode(float b) {
+  const int code = (int)((__float_as_uint(b) + 0x1000u) >> 13) - (int)(kBinExpBias << 10);
+  return (bin_t)min(max(code, 0), 0xFFFF);
+}
+__device__ __forceinline__ float bin_decode(uint32_t code) {
+  return code == 0 ? 0.f : __uint_as_float((code + (kBinExpBias << 10)) << 13);
+}
+
 // Per-sequence table passed by value: token offsets and scoring-unit offsets.
 // A scoring unit is one (sequence b, KV head h, run of `cpu` chunks); units of
 // one sequence are numbered u = 0 .. U_b-1 and all heads of a unit are
@@ -38,7 +54,7 @@ struct ScoreGeom {
   int64_t kv_stride_t, kv_stride_h;
   // Distance (in floats) between the buffers of consecutive reuse groups, for the
   // kernels that handle every group of a call in one launch (blockIdx.z = group).
-  int64_t rl_gs, bins_gs, lse_gs, scores_gs;
+  int64_t rl_gs, bins_gs, lse_gs, scores_gs;     // group strides: floats, bin_t, floats, floats
 };
 
 // Selection / index-build geometry (blockIdx.y = reuse group).
@@ -142,9 +158,9 @@ struct Plan {
 
 // Launchers (defined in the kernel translation units).
 cudaError_t launch_score_simt(const Plan& pl, const ScoreGeom& g, const SeqTable& st, const void* q,
-                              const void* k, float* rl, float* bins, cudaStream_t s);
+                              const void* k, float* rl, bin_t* bins, cudaStream_t s);
 cudaError_t launch_finalize(const Plan& pl, const ScoreGeom& g, const SeqTable& st, float* rl,
-                            const float* bins, const float* lse, float* scores, int n_groups, cudaStream_t s);
+                            const bin_t* bins, const float* lse, float* scores, int n_groups, cudaStream_t s);
 cudaError_t launch_lse(const ScoreGeom& g, const SeqTable& st, const float* rl, float* lse, int n_groups,
                        cudaStream_t s);
 cudaError_t launch_select(const Plan& pl, const SelectGeom& sg, const SeqTable& st, const float* scores,

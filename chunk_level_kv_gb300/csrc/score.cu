@@ -29,7 +29,7 @@ template <typename E>
 __global__ void __launch_bounds__(kSimtRows)
 score_simt_kernel(const E* __restrict__ q, const E* __restrict__ k, ScoreGeom g,
                   const __grid_constant__ SeqTable st, float* __restrict__ rl,
-                  float* __restrict__ bins) {
+                  bin_t* __restrict__ bins) {
   extern __shared__ float smem[];
   const int ld = g.d + 1;                       // padded rows: conflict-free per-thread rows
   float* qs = smem;                             // [kSimtRows][ld]
@@ -83,7 +83,7 @@ score_simt_kernel(const E* __restrict__ q, const E* __restrict__ k, ScoreGeom g,
     // sweep 2: exponentials relative to the unit maximum, summed per chunk
     float acc = 0.f, l = 0.f;
     int cur = 0;
-    float* brow = bins + (int64_t)gu * g.cpu * g.wG + r;
+    bin_t* brow = bins + (int64_t)gu * g.cpu * g.wG + r;
     for (int kt = 0; kt < nk; kt += kSimtKeys) {
       const int nt = min(kSimtKeys, nk - kt);
       __syncthreads();
@@ -99,7 +99,7 @@ score_simt_kernel(const E* __restrict__ q, const E* __restrict__ k, ScoreGeom g,
           for (int e = 0; e < g.d; ++e) dot = fmaf(qrow[e], kr[e], dot);
           const int ch = (kt + j) / g.c;
           if (ch != cur) {
-            brow[(int64_t)cur * g.wG] = acc;
+            brow[(int64_t)cur * g.wG] = bin_encode(acc);
             acc = 0.f;
             cur = ch;
           }
@@ -110,7 +110,7 @@ score_simt_kernel(const E* __restrict__ q, const E* __restrict__ k, ScoreGeom g,
       }
     }
     if (active) {
-      brow[(int64_t)cur * g.wG] = acc;
+      brow[(int64_t)cur * g.wG] = bin_encode(acc);
       rl[((int64_t)gu * 2 + 0) * g.wG + r] = m;
       rl[((int64_t)gu * 2 + 1) * g.wG + r] = l;
     }
@@ -119,7 +119,7 @@ score_simt_kernel(const E* __restrict__ q, const E* __restrict__ k, ScoreGeom g,
 }
 
 cudaError_t launch_score_simt(const Plan& pl, const ScoreGeom& g, const SeqTable& st, const void* q,
-                              const void* k, float* rl, float* bins, cudaStream_t s) {
+                              const void* k, float* rl, bin_t* bins, cudaStream_t s) {
   if (g.n_units == 0 || g.wG == 0) return cudaSuccess;
   const size_t smem = (size_t)(kSimtRows + kSimtKeys) * (g.d + 1) * sizeof(float);
   cudaError_t e;
@@ -150,7 +150,7 @@ constexpr int kFinChunks = 128;                 // chunks per CTA: blockIdx.y ti
 
 __global__ void __launch_bounds__(kFinThreads)
 finalize_kernel(ScoreGeom g, const __grid_constant__ SeqTable st, const float* __restrict__ rl,
-                const float* __restrict__ bins, const float* __restrict__ lse_rows, int lse_stride,
+                const bin_t* __restrict__ bins, const float* __restrict__ lse_rows, int lse_stride,
                 float* __restrict__ scores) {
   extern __shared__ float wts[];                // [wG]
   int b, h, u;
@@ -186,7 +186,7 @@ finalize_kernel(ScoreGeom g, const __grid_constant__ SeqTable st, const float* _
 
   const int nc = min(min(g.cpu, C - u * g.cpu) - cb, kFinChunks);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const float* ub = bins + ((int64_t)gu * g.cpu + cb) * g.wG;
+  const bin_t* ub = bins + ((int64_t)gu * g.cpu + cb) * g.wG;
   float* out = scores + ((int64_t)b * g.Hkv + h) * g.C_max + (int64_t)u * g.cpu + cb;
   // each warp sums eight chunks at a time: eight independent load streams per lane
   constexpr int kW = kFinThreads / 32;
@@ -196,26 +196,27 @@ finalize_kernel(ScoreGeom g, const __grid_constant__ SeqTable st, const float* _
 #pragma unroll
     for (int i = 0; i < kG; ++i) acc[i] = 0.f;
     const int m = min(kG, nc - ch0);
-    const float* cbase = ub + (int64_t)ch0 * g.wG;
+    const bin_t* cbase = ub + (int64_t)ch0 * g.wG;
     if ((g.wG & 3) == 0) {
-      // four consecutive rows per lane: 16-byte loads, kG of them in flight
+      // four consecutive rows per lane: 8-byte loads of four bins, kG of them in flight
       for (int r = 4 * lane; r < g.wG; r += 128) {
         const float4 w4 = *reinterpret_cast<const float4*>(wts + r);
-        float4 v[kG];
+        uint2 v[kG];
 #pragma unroll
         for (int i = 0; i < kG; ++i)
-          v[i] = i < m ? __ldcs(reinterpret_cast<const float4*>(cbase + (int64_t)i * g.wG + r))
-                       : make_float4(0.f, 0.f, 0.f, 0.f);
+          v[i] = i < m ? __ldcs(reinterpret_cast<const uint2*>(cbase + (int64_t)i * g.wG + r)) : make_uint2(0u, 0u);
 #pragma unroll
         for (int i = 0; i < kG; ++i)
-          acc[i] = fmaf(v[i].x, w4.x, fmaf(v[i].y, w4.y, fmaf(v[i].z, w4.z, fmaf(v[i].w, w4.w, acc[i]))));
+          acc[i] = fmaf(bin_decode(v[i].x & 0xFFFFu), w4.x,
+                        fmaf(bin_decode(v[i].x >> 16), w4.y,
+                             fmaf(bin_decode(v[i].y & 0xFFFFu), w4.z, fmaf(bin_decode(v[i].y >> 16), w4.w, acc[i]))));
       }
     } else {
       for (int r = lane; r < g.wG; r += 32) {
         const float wr = wts[r];
         float v[kG];
 #pragma unroll
-        for (int i = 0; i < kG; ++i) v[i] = i < m ? __ldcs(cbase + (int64_t)i * g.wG + r) : 0.f;
+        for (int i = 0; i < kG; ++i) v[i] = i < m ? bin_decode(__ldcs(cbase + (int64_t)i * g.wG + r)) : 0.f;
 #pragma unroll
         for (int i = 0; i < kG; ++i) acc[i] = fmaf(v[i], wr, acc[i]);
       }
@@ -308,7 +309,7 @@ __global__ void zero_scores_kernel(ScoreGeom g, const __grid_constant__ SeqTable
 }
 
 cudaError_t launch_finalize(const Plan& pl, const ScoreGeom& g, const SeqTable& st, float* rl,
-                            const float* bins, const float* lse, float* scores, int n_groups, cudaStream_t s) {
+                            const bin_t* bins, const float* lse, float* scores, int n_groups, cudaStream_t s) {
   (void)pl;
   if (g.n_units == 0 || n_groups == 0) return cudaSuccess;
   if (g.wG == 0)

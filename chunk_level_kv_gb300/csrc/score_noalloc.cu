@@ -85,7 +85,7 @@ extern "C" chunkkv_status chunkkv_score_noalloc(const chunkkv_params* p, const v
   const int64_t n_units = units * p->Hkv;
   if (n_units == 0) return CHUNKKV_OK;
   const size_t rl_bytes = align256((size_t)n_units * 2 * wG * sizeof(float));
-  const size_t bin_bytes = align256((size_t)n_units * cpu * wG * sizeof(float));
+  const size_t bin_bytes = align256((size_t)n_units * cpu * wG * sizeof(bin_t));
   if (rl_bytes + bin_bytes > kNoAllocScratchBytes) return CHUNKKV_ERR_WORKSPACE_TOO_SMALL;
   if ((wG > 0 && (!q_win || ((uintptr_t)q_win & 15u))) || !k || ((uintptr_t)k & 15u) || !chunk_scores)
     return CHUNKKV_ERR_INVALID_ARG;
@@ -117,7 +117,7 @@ extern "C" chunkkv_status chunkkv_score_noalloc(const chunkkv_params* p, const v
   g.kv_stride_h = p->kv_stride_h;
   g.rl_gs = g.bins_gs = g.lse_gs = g.scores_gs = 0;      // a single group
   float* rl = (float*)base;
-  float* bins = (float*)((char*)base + rl_bytes);
+  bin_t* bins = (bin_t*)((char*)base + rl_bytes);
   cudaStream_t cs = (cudaStream_t)stream;
   cudaError_t e = launch_score_simt(pl, g, st, q_win, k, rl, bins, cs);
   if (e == cudaSuccess) e = launch_finalize(pl, g, st, rl, bins, nullptr, chunk_scores, 1, cs);

@@ -59,7 +59,7 @@ constexpr uint32_t kIdesc = (1u << 4)                         // D = fp32
                           | (1u << 7) | (1u << 10)           // A = B = bf16
                           | ((uint32_t)(kN >> 3) << 17)      // N
                           | ((uint32_t)(128 >> 4) << 24);    // M
-constexpr float kBig = 18446744073709551616.0f;              // 2^64: rescale threshold
+constexpr float kBig = 16777216.0f;                          // 2^24: rescale threshold (bin range)
 
 // One launch scores up to kMaxGroups reuse groups (one layer each): items are
 // enumerated group by group, each group with its own key tensor map and its own
@@ -70,7 +70,7 @@ struct TcGeom {
   int32_t B, Hkv, wG, MT, cpu, ku;
   int32_t items_pg;                  // work items per group: units x M tiles
   int32_t n_items;                   // items_pg x groups of this launch
-  int64_t slot_gs;                   // floats between the scratch slots of consecutive groups
+  int64_t slot_bytes;                // bytes between the scratch slots of consecutive groups
   float alpha;                       // log2(e) / sqrt(d)
   long long timeout;                 // clock64 cycles per wait
 };
@@ -158,8 +158,9 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   return p;
 }
 // A bin store that asks L2 to keep the line: the finalisation reads it back soon.
-__device__ __forceinline__ void st_keep(float* ptr, float v, uint64_t policy) {
-  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(ptr), "f"(v), "l"(policy) : "memory");
+__device__ __forceinline__ void st_keep(bin_t* ptr, float v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.b16 [%0], %1, %2;" ::"l"(ptr), "h"((unsigned short)bin_encode(v)), "l"(policy)
+               : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -251,7 +252,7 @@ struct RowState {
 // points at bins[(gu*cpu + q)*wG + row], q being the unit-local chunk that holds
 // the tile's column 0.
 template <int C, int PH, int SEG, bool MASK>
-__device__ __forceinline__ void tile_seg(const uint32_t (&r)[16], float2 alpha2, RowState& s, float* bin, int wG,
+__device__ __forceinline__ void tile_seg(const uint32_t (&r)[16], float2 alpha2, RowState& s, bin_t* bin, int wG,
                                          int valid, bool write, uint64_t pol) {
   static_assert(C >= 2, "pairs hold at most one chunk end");
   float2 acc = s.carry;
@@ -284,7 +285,7 @@ __device__ __forceinline__ void tile_seg(const uint32_t (&r)[16], float2 alpha2,
 }
 
 template <int C, int PH, int SEG, bool MASK>
-__device__ __forceinline__ void tile_segs(const uint32_t (&r)[kN / 16][16], float2 alpha, RowState& s, float* bin,
+__device__ __forceinline__ void tile_segs(const uint32_t (&r)[kN / 16][16], float2 alpha, RowState& s, bin_t* bin,
                                           int wG, int valid, bool write, uint64_t pol) {
   if constexpr (SEG < kN / 16) {
     tile_seg<C, PH, SEG, MASK>(r[SEG], alpha, s, bin, wG, valid, write, pol);
@@ -296,7 +297,7 @@ __device__ __forceinline__ void tile_segs(const uint32_t (&r)[kN / 16][16], floa
 // (kN/16 x16 loads, one wait), so the column pairs are independent work that
 // the scheduler can interleave freely.
 template <int C, int PH, bool MASK>
-__device__ __forceinline__ void tile_phase(uint32_t taddr, float2 alpha, RowState& s, float* bin, int wG, int valid,
+__device__ __forceinline__ void tile_phase(uint32_t taddr, float2 alpha, RowState& s, bin_t* bin, int wG, int valid,
                                            bool write, uint64_t pol) {
   uint32_t r[kN / 16][16];
 #pragma unroll
@@ -307,7 +308,7 @@ __device__ __forceinline__ void tile_phase(uint32_t taddr, float2 alpha, RowStat
 }
 
 template <int C, int PH = 0>
-__device__ __forceinline__ void tile_dispatch(int ph, bool mask, uint32_t taddr, float2 alpha, RowState& s, float* bin,
+__device__ __forceinline__ void tile_dispatch(int ph, bool mask, uint32_t taddr, float2 alpha, RowState& s, bin_t* bin,
                                               int wG, int valid, bool write, uint64_t pol) {
   if constexpr (PH < C) {
     if (ph == PH) {
@@ -339,7 +340,7 @@ __device__ __forceinline__ float tile_max(uint32_t taddr, int valid) {
 template <int C>
 __global__ void __launch_bounds__(kThreads, 2)
 score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_constant__ SeqTable st,
-                float* __restrict__ rl, float* __restrict__ bins, int32_t* __restrict__ err) {
+                float* __restrict__ rl, bin_t* __restrict__ bins, int32_t* __restrict__ err) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw;
   if (smem_u32(smem_raw) & 1023u) {                         // swizzled tiles need 1024-byte alignment
@@ -500,8 +501,8 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
       const int row = it.mt * 128 + rloc;
       const bool write = row < g.wG;
       const bool warp_live = it.mt * 128 + lg * 32 < g.wG;         // whole warp of padding rows: no work
-      float* ubins = bins + it.grp * g.slot_gs + (size_t)it.unit * g.cpu * g.wG + row;
-      float* url = rl + it.grp * g.slot_gs + (size_t)it.unit * 2 * g.wG + row;
+      bin_t* ubins = (bin_t*)((char*)bins + it.grp * g.slot_bytes) + (size_t)it.unit * g.cpu * g.wG + row;
+      float* url = (float*)((char*)rl + it.grp * g.slot_bytes) + (size_t)it.unit * 2 * g.wG + row;
       RowState s{make_float2(0.f, 0.f), make_float2(0.f, 0.f), 0.f};
       const float2 alpha2 = make_float2(g.alpha, g.alpha);
       float R = 0.f;
@@ -535,7 +536,8 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
             const float R2 = over ? fmaxf(R, tm) : R;
             const float f = ex2(R - R2);
             if (over && write)
-              for (int ch = 0; ch < q; ++ch) ubins[(size_t)ch * g.wG] *= f;
+              for (int ch = 0; ch < q; ++ch)
+                ubins[(size_t)ch * g.wG] = bin_encode(bin_decode(ubins[(size_t)ch * g.wG]) * f);
             s = before;
             s.l *= f;
             s.carry = make_float2(s.carry.x * f, s.carry.y * f);
@@ -554,7 +556,7 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
         if ((ntile * kN) % C != 0) {
           const float cs = s.carry.x + s.carry.y;
           const int ch = (ntile * kN) / C;
-          if (ch < g.cpu) ubins[(size_t)ch * g.wG] = cs;
+          if (ch < g.cpu) ubins[(size_t)ch * g.wG] = bin_encode(cs);
           s.l += cs;
         }
         url[0] = R;
@@ -643,7 +645,7 @@ DeviceInfo& device_info(int dev) {
 }
 
 template <int C>
-cudaError_t launch_c(const TcGeom& tg, const TcMaps& maps, const SeqTable& st, float* rl, float* bins, int32_t* err,
+cudaError_t launch_c(const TcGeom& tg, const TcMaps& maps, const SeqTable& st, float* rl, bin_t* bins, int32_t* err,
                      int slot, cudaStream_t s) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -717,7 +719,7 @@ cudaError_t launch_pack_q(const Plan& pl, const ScoreGeom& g, const void* const*
 // keys k_groups[i] and writes the scratch slot at rl + i * slot_gs and
 // bins + i * slot_gs (slot_gs in floats).
 cudaError_t launch_score_tc(const Plan& pl, const ScoreGeom& g, const SeqTable& st, const void* const* k_groups,
-                            int n_groups, int64_t slot_gs, float* rl, float* bins, const void* qpack, int32_t* err,
+                            int n_groups, int64_t slot_bytes, float* rl, bin_t* bins, const void* qpack, int32_t* err,
                             cudaStream_t s) {
   tc::EncodeFn enc = tc::encode_fn();
   if (enc == nullptr) return cudaErrorNotSupported;
@@ -758,11 +760,11 @@ cudaError_t launch_score_tc(const Plan& pl, const ScoreGeom& g, const SeqTable& 
     tg.ku = pl.ku;
     tg.items_pg = g.n_units * MT;
     tg.n_items = tg.items_pg * n;
-    tg.slot_gs = slot_gs;
+    tg.slot_bytes = slot_bytes;
     tg.alpha = g.alpha;
     tg.timeout = 4000000000LL;     // about two seconds of clock64 cycles per wait
-    float* rlg = rl + g0 * slot_gs;
-    float* bg = bins + g0 * slot_gs;
+    float* rlg = (float*)((char*)rl + g0 * slot_bytes);
+    bin_t* bg = (bin_t*)((char*)bins + g0 * slot_bytes);
     cudaError_t e = cudaErrorNotSupported;
     switch (pl.c) {
       case 3: e = tc::launch_c<3>(tg, maps, st, rlg, bg, err, 0, s); break;
