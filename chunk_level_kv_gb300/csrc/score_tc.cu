@@ -385,6 +385,7 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
   if (warp == 0) {
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
+      pdl_wait();                                      // the packed window rows come from the previous launch
       uint32_t kc = 0, qc = 0;
       int qkey = -1;                                   // (group, sequence, head, M tile) of the loaded Q
       // keys: normal priority, since the CTAs of the other M tiles of the same
