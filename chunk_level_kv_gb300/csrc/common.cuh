@@ -28,6 +28,13 @@ __device__ __forceinline__ bin_t bin_encode(float b) {
   const int code = (int)((__float_as_uint(b) + 0x1000u) >> 13) - (int)(kBinExpBias << 10);
   return (bin_t)min(max(code, 0), 0xFFFF);
 }
+// Encoding for bins known to be at most 2^23 (the tensor-core kernel rescales a
+// row before its sum passes that): the exponent bias folds into the rounding add
+// and the arithmetic shift leaves bins below 2^-40 negative, so one clamp suffices.
+__device__ __forceinline__ bin_t bin_encode_bounded(float b) {
+  const int code = ((int)__float_as_uint(b) + (0x1000 - (int)(kBinExpBias << 23))) >> 13;
+  return (bin_t)max(code, 0);
+}
 __device__ __forceinline__ float bin_decode(uint32_t code) {
   return code == 0 ? 0.f : __uint_as_float((code + (kBinExpBias << 10)) << 13);
 }

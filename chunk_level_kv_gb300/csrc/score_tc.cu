@@ -59,7 +59,7 @@ constexpr uint32_t kIdesc = (1u << 4)                         // D = fp32
                           | (1u << 7) | (1u << 10)           // A = B = bf16
                           | ((uint32_t)(kN >> 3) << 17)      // N
                           | ((uint32_t)(128 >> 4) << 24);    // M
-constexpr float kBig = 16777216.0f;                          // 2^24: rescale threshold (bin range)
+constexpr float kBig = 8388608.0f;                           // 2^23: rescale threshold (within the bin range)
 
 // One launch scores up to kMaxGroups reuse groups (one layer each): items are
 // enumerated group by group, each group with its own key tensor map and its own
@@ -159,7 +159,7 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
 }
 // A bin store that asks L2 to keep the line: the finalisation reads it back soon.
 __device__ __forceinline__ void st_keep(bin_t* ptr, float v, uint64_t policy) {
-  asm volatile("st.global.L2::cache_hint.b16 [%0], %1, %2;" ::"l"(ptr), "h"((unsigned short)bin_encode(v)), "l"(policy)
+  asm volatile("st.global.L2::cache_hint.b16 [%0], %1, %2;" ::"l"(ptr), "h"((unsigned short)bin_encode_bounded(v)), "l"(policy)
                : "memory");
 }
 

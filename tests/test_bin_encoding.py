@@ -46,3 +46,18 @@ def test_monotone_and_exact_on_short_mantissas():
     assert np.all(np.diff(y) >= 0)
     z = (np.arange(1, 1024, dtype=np.float32) / 1024 + 1) * np.float32(2.0 ** -7)     # 10-bit mantissas
     assert np.array_equal(decode(encode(z)), z)
+
+
+def encode_bounded(b):
+    """The tensor-core kernel's encoder for bins at most 2^23: bias folded into the rounding add,
+    arithmetic shift, one clamp at zero."""
+    u = np.asarray(b, np.float32).view(np.uint32).astype(np.int64)
+    return np.maximum((u + (0x1000 - (BIAS << 23))) >> 13, 0).astype(np.uint32)     # numpy >> floors
+
+
+def test_bounded_encoder_matches_up_to_2_23():
+    rng = np.random.default_rng(11)
+    x = np.concatenate([(2.0 ** rng.uniform(-45, 23, 1_000_000)).astype(np.float32),
+                        np.float32([0.0, 2.0 ** -40, 2.0 ** -41, 2.0 ** 23, 2.0 ** 23 * 0.9999])])
+    assert np.array_equal(encode_bounded(x), encode(x))
+    assert encode_bounded(np.float32(2.0 ** 23)).item() < 0xFFFF
