@@ -137,7 +137,7 @@ def phase_rooflines(wl, counts, phase_ms, peaks, peak_src, path):
       score:    K of every scoring layer read once (T_total*Hkv*d*elt per group) and
                 2*w*G*T_total*Hkv*d flops; the roof is whichever takes longer at peak
                 (HBM copy bandwidth, or the sustained bf16 tensor rate);
-      finalize: one fp32 bin per (chunk, window row, KV head) per group read once;
+      finalize: one 16-bit bin per (chunk, window row, KV head) per group read once;
       gather:   kept K and V rows read and written (4*kept*d*elt per layer).
     """
     elt = 2 if wl.dtype == "bf16" else 4
@@ -170,7 +170,7 @@ def phase_rooflines(wl, counts, phase_ms, peaks, peak_src, path):
                     "peak_source": f"{peak_src} bf16_tflops_sustained"})
     else:
         out.append(hbm_roof("score", kernel, score_bytes))
-    out.append(hbm_roof("finalize", "finalize_kernel", groups * chunks * wl.Hkv * wl.w * wl.G * 4))
+    out.append(hbm_roof("finalize", "finalize_kernel", groups * chunks * wl.Hkv * wl.w * wl.G * 2))
     out.append(hbm_roof("gather", "gather_kernel", 4 * kept_all * wl.d * elt))
     return out
 

@@ -10,7 +10,8 @@
 //   R_r   a reference exponent (base 2: logits times log2(e)/sqrt(d)),
 //   l_r   = sum_{j in unit} 2^(t_rj - R_r),
 //   bin[i][r] = sum_{j in chunk i} 2^(t_rj - R_r)   for the unit's chunks,
-// all in fp32.  finalize_kernel then forms lse_r over every unit of the head,
+// R and l in fp32, the bins as 16-bit unsigned floats (bin_encode).  lse_kernel
+// then forms lse_r over every unit of the head, and finalize_kernel
 // the weights 2^(R_r - lse_r) and A_i = sum_r bin[i][r] * weight_r.  This
 // single pass over K needs no second read of the keys and no grid barrier.
 #include "common.cuh"

@@ -13,8 +13,8 @@
 //     S from TMEM, forms 2^(s*log2(e)/sqrt(d) - R) with R the row maximum of the
 //     item's first tile, and sums those per chunk (chunk boundaries are compile
 //     time constants for each of the C / gcd(80, C) tile phases), writing one
-//     fp32 bin per (chunk, row) and the row's (R, sum) at the end of the item.
-// A row whose values would outgrow the first-tile reference by more than 2^64
+//     16-bit bin per (chunk, row) and the row's (R, sum) at the end of the item.
+// A row whose values would outgrow the first-tile reference by more than 2^23
 // switches to the new maximum and rescales what it already wrote.
 //
 // Warp roles (192 threads): warp 0 = TMA producer, warp 1 = TMEM owner and MMA
