@@ -50,6 +50,7 @@ def _load():
         "chunkkv_score_path": [P],
         "chunkkv_score_noalloc": [P, vp, vp, vp, vp],
         "chunkkv_set_phase_events": [pp, i32],
+        "chunkkv_selftest_wait_timeout": [vp, sz, vp],
     }
     for name, args in sigs.items():
         fn = getattr(lib, name)

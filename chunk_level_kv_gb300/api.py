@@ -150,6 +150,13 @@ def chunkkv_compress_layers(p: Params, n_reuse: int, q_win, k, v, k_out, v_out, 
                                        ws.numel() * ws.element_size(), _stream(counts.device)))
 
 
+def chunkkv_selftest_wait_timeout(ws) -> None:
+    """Failure-path self test: a bounded device wait that nothing completes gives up after about a
+    millisecond and records code 0x1FF in ws's error word (read it with chunkkv_status_check)."""
+    _check("chunkkv_selftest_wait_timeout",
+           LIB.chunkkv_selftest_wait_timeout(_ptr(ws), ws.numel() * ws.element_size(), _stream(ws.device)))
+
+
 def chunkkv_status_check(ws) -> int:
     """Synchronises the current stream and reports a device-side wait that gave up (raises)."""
     code = ctypes.c_int32()

@@ -13,6 +13,7 @@ std::atomic<unsigned long long> g_launch_count{0};
 
 bool tc_supported(const Plan& pl);                                  // score_tc.cu
 void tc_plan(Plan& pl);                                             // score_tc.cu
+cudaError_t launch_wait_selftest(int32_t* err, long long timeout, cudaStream_t s);   // score_tc.cu
 cudaError_t launch_pack_q(const Plan& pl, const ScoreGeom& g, const void* const* q_layers, int n_layers,
                           void* qpack, cudaStream_t s);
 cudaError_t launch_score_tc(const Plan& pl, const ScoreGeom& g, const SeqTable& st, const void* const* k_groups,
@@ -444,6 +445,12 @@ chunkkv_status chunkkv_set_phase_events(void* const* events, int32_t n_events) {
   for (int i = 0; i < CHUNKKV_PHASE_EVENTS; ++i) t_phase_ev[i] = events[i];
   t_phase_n = CHUNKKV_PHASE_EVENTS;
   return CHUNKKV_OK;
+}
+
+chunkkv_status chunkkv_selftest_wait_timeout(void* ws, size_t ws_bytes, chunkkv_stream_t stream) {
+  if (ws == nullptr || !aligned16(ws) || ws_bytes < kHeaderBytes) return CHUNKKV_ERR_INVALID_ARG;
+  // about a millisecond of clock64 cycles, instead of the scoring kernel's two seconds
+  return cuda_status(launch_wait_selftest((int32_t*)ws, 2000000LL, (cudaStream_t)stream));
 }
 
 uint64_t chunkkv_launch_count(void) { return chunkkv::g_launch_count.load(std::memory_order_relaxed); }

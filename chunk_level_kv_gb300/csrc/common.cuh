@@ -38,6 +38,14 @@ __device__ __forceinline__ bin_t bin_encode_bounded(float b) {
 __device__ __forceinline__ float bin_decode(uint32_t code) {
   return code == 0 ? 0.f : __uint_as_float((code + (kBinExpBias << 10)) << 13);
 }
+// The two bins packed in a 32-bit word (low half first) for the finalisation's
+// weighted sums: three integer ops a bin, reading code 0 as 2^-40 of the row
+// reference instead of 0 (below the encoding's own flush error).
+__device__ __forceinline__ float2 bin_decode2(uint32_t v) {
+  const uint32_t lo = ((v << 13) & 0x1FFFE000u) + (kBinExpBias << 23);
+  const uint32_t hi = ((v >> 3) & 0x1FFFE000u) + (kBinExpBias << 23);
+  return make_float2(__uint_as_float(lo), __uint_as_float(hi));
+}
 
 // Per-sequence table passed by value: token offsets and scoring-unit offsets.
 // A scoring unit is one (sequence b, KV head h, run of `cpu` chunks); units of
@@ -92,6 +100,7 @@ enum DeviceError : int32_t {
   kDevTimeoutTmaProducer = 0x101,
   kDevTimeoutMma = 0x102,
   kDevTimeoutEpilogue = 0x103,
+  kDevTimeoutSelftest = 0x1FF,      // chunkkv_selftest_wait_timeout
   kDevMisalignedSmem = 0x201,
 };
 

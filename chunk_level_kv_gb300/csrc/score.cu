@@ -207,10 +207,10 @@ finalize_kernel(ScoreGeom g, const __grid_constant__ SeqTable st, const float* _
         for (int i = 0; i < kG; ++i)
           v[i] = i < m ? __ldcs(reinterpret_cast<const uint2*>(cbase + (int64_t)i * g.wG + r)) : make_uint2(0u, 0u);
 #pragma unroll
-        for (int i = 0; i < kG; ++i)
-          acc[i] = fmaf(bin_decode(v[i].x & 0xFFFFu), w4.x,
-                        fmaf(bin_decode(v[i].x >> 16), w4.y,
-                             fmaf(bin_decode(v[i].y & 0xFFFFu), w4.z, fmaf(bin_decode(v[i].y >> 16), w4.w, acc[i]))));
+        for (int i = 0; i < kG; ++i) {
+          const float2 b01 = bin_decode2(v[i].x), b23 = bin_decode2(v[i].y);
+          acc[i] = fmaf(b01.x, w4.x, fmaf(b01.y, w4.y, fmaf(b23.x, w4.z, fmaf(b23.y, w4.w, acc[i]))));
+        }
       }
     } else {
       for (int r = lane; r < g.wG; r += 32) {

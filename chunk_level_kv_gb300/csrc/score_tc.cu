@@ -614,6 +614,25 @@ __global__ void pack_q_kernel(const __grid_constant__ PackArgs pa, ScoreGeom g, 
   pdl_trigger();
 }
 
+// Failure-path self test: one thread waits, through the same bounded wait as the
+// scoring kernel's roles, on an mbarrier phase that nothing completes.  The wait
+// runs out after `timeout` clock64 cycles, records kDevTimeoutSelftest in the
+// workspace error word and raises the CTA abort flag; the kernel then returns.
+__global__ void wait_selftest_kernel(int32_t* err, long long timeout) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);                 // one arrival expected, none made
+    abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const Ctl ctl{err, (volatile int*)&abort_flag, timeout};
+    if (wait_bar(ctl, smem_u32(&bar), 0, kDevTimeoutSelftest)) atomicExch(err, 0x7FFFFFFF);   // must not happen
+  }
+}
+
 // ---------------------------------------------------------------- host side
 using EncodeFn = PFN_cuTensorMapEncodeTiled_v12000;
 
@@ -780,6 +799,13 @@ cudaError_t launch_score_tc(const Plan& pl, const ScoreGeom& g, const SeqTable& 
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+cudaError_t launch_wait_selftest(int32_t* err, long long timeout, cudaStream_t s) {
+  tc::wait_selftest_kernel<<<1, 32, 0, s>>>(err, timeout);
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) g_launch_count.fetch_add(1, std::memory_order_relaxed);
+  return e;
 }
 
 }  // namespace chunkkv

@@ -186,6 +186,18 @@ chunkkv_status chunkkv_score_noalloc(const chunkkv_params* p, const void* q_win,
  */
 chunkkv_status chunkkv_status_check(void* ws, chunkkv_stream_t stream, int32_t* device_code);
 
+/*
+ * Self test of the failure path (a test aid; no counterpart in the pages).
+ * Launches one thread that waits, through the same bounded wait as the
+ * tensor-core scoring kernel, on a barrier that nothing completes.  The wait
+ * gives up after about a millisecond, records device code 0x1FF in the error
+ * word of ws and the kernel returns, leaving the context usable; a following
+ * chunkkv_status_check(ws, ...) then returns CHUNKKV_ERR_TIMEOUT with that code.
+ *   ws: device workspace of at least 256 bytes (its error word is written).
+ * Returns CHUNKKV_ERR_INVALID_ARG for a NULL, misaligned or too small ws.
+ */
+chunkkv_status chunkkv_selftest_wait_timeout(void* ws, size_t ws_bytes, chunkkv_stream_t stream);
+
 /* Static description of a status code. */
 const char* chunkkv_status_string(chunkkv_status s);
 

@@ -61,3 +61,19 @@ def test_bounded_encoder_matches_up_to_2_23():
                         np.float32([0.0, 2.0 ** -40, 2.0 ** -41, 2.0 ** 23, 2.0 ** 23 * 0.9999])])
     assert np.array_equal(encode_bounded(x), encode(x))
     assert encode_bounded(np.float32(2.0 ** 23)).item() < 0xFFFF
+
+
+def decode2(v):
+    """The finalisation's decode of two bins packed in a 32-bit word (code 0 reads as 2^-40)."""
+    v = np.asarray(v, np.uint32).astype(np.uint64)
+    lo = (((v << 13) & 0x1FFFE000) + (BIAS << 23)).astype(np.uint32).view(np.float32)
+    hi = (((v >> 3) & 0x1FFFE000) + (BIAS << 23)).astype(np.uint32).view(np.float32)
+    return lo, hi
+
+
+def test_pair_decode_matches_single_decode():
+    v = np.random.default_rng(13).integers(0, 2 ** 32, 500_000, dtype=np.uint64).astype(np.uint32)
+    lo, hi = decode2(v)
+    for half, got in ((v & 0xFFFF, lo), (v >> 16, hi)):
+        want = decode(half)
+        assert np.array_equal(np.where(half == 0, np.float32(2.0 ** -40), want), got)

@@ -147,6 +147,21 @@ def test_phase_events_mark_every_phase(ckv):
     assert all(torch.equal(a, b) for a, b in zip(out.k_out, ref.k_out))
 
 
+def test_bounded_wait_gives_up_and_reports(ckv):
+    import ctypes
+    from chunk_level_kv_gb300._lib import LIB
+    from chunk_level_kv_gb300.api import _stream
+    ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
+    ckv.chunkkv_selftest_wait_timeout(ws)
+    code = ctypes.c_int32()
+    st = LIB.chunkkv_status_check(ctypes.c_void_p(ws.data_ptr()), _stream(ws.device), ctypes.byref(code))
+    assert st == 5 and code.value == 0x1FF                 # CHUNKKV_ERR_TIMEOUT, the self-test site
+    assert ckv.chunkkv_status_check(ws) == 0              # the word was cleared ...
+    wl = configs.tiny()                                   # ... and the context still computes
+    out, verdicts = run_and_check(ckv, wl)
+    assert verdicts == ["exact", "exact"]
+
+
 def test_select_is_bit_exact_on_given_scores(ckv):
     # both sides decide on the same fp32 scores: the selection must match exactly (ties included)
     rng = np.random.default_rng(0)

@@ -51,6 +51,12 @@ def test_phase_events_argument_checks(ckv):
     assert LIB.chunkkv_set_phase_events(None, 0) == 0
 
 
+def test_selftest_argument_checks(ckv):
+    from chunk_level_kv_gb300._lib import LIB
+    assert LIB.chunkkv_selftest_wait_timeout(None, 256, None) == 1
+    assert LIB.chunkkv_selftest_wait_timeout(ctypes.c_void_p(16), 128, None) == 1     # too small: no launch
+
+
 def test_status_strings(ckv):
     from chunk_level_kv_gb300._lib import LIB
     for code in range(6):
