@@ -198,7 +198,24 @@ finalize_kernel(ScoreGeom g, const __grid_constant__ SeqTable st, const float* _
     for (int i = 0; i < kG; ++i) acc[i] = 0.f;
     const int m = min(kG, nc - ch0);
     const bin_t* cbase = ub + (int64_t)ch0 * g.wG;
-    if ((g.wG & 3) == 0) {
+    if ((g.wG & 7) == 0 && g.wG >= 256) {
+      // eight consecutive rows per lane: 16-byte loads of eight bins, kG of them in flight
+      for (int r = 8 * lane; r < g.wG; r += 256) {
+        const float4 wa = *reinterpret_cast<const float4*>(wts + r);
+        const float4 wb = *reinterpret_cast<const float4*>(wts + r + 4);
+        uint4 v[kG];
+#pragma unroll
+        for (int i = 0; i < kG; ++i)
+          v[i] = i < m ? __ldcs(reinterpret_cast<const uint4*>(cbase + (int64_t)i * g.wG + r)) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int i = 0; i < kG; ++i) {
+          const float2 b01 = bin_decode2(v[i].x), b23 = bin_decode2(v[i].y);
+          const float2 b45 = bin_decode2(v[i].z), b67 = bin_decode2(v[i].w);
+          acc[i] = fmaf(b01.x, wa.x, fmaf(b01.y, wa.y, fmaf(b23.x, wa.z, fmaf(b23.y, wa.w, acc[i]))));
+          acc[i] = fmaf(b45.x, wb.x, fmaf(b45.y, wb.y, fmaf(b67.x, wb.z, fmaf(b67.y, wb.w, acc[i]))));
+        }
+      }
+    } else if ((g.wG & 3) == 0) {
       // four consecutive rows per lane: 8-byte loads of four bins, kG of them in flight
       for (int r = 4 * lane; r < g.wG; r += 128) {
         const float4 w4 = *reinterpret_cast<const float4*>(wts + r);
