@@ -96,6 +96,24 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(self.rows)}
 
 
+def slowest_rank(step_ms: float, ws_n: int) -> float:
+    """The job's step time: the maximum over the ranks of the default process group (all_reduce MAX;
+    on the GPU for NCCL, on the host for gloo)."""
+    if ws_n <= 1:
+        return step_ms
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([step_ms], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t)
+
+
+def job_rate(units_per_rank: float, ws_n: int, step_ms: float) -> float:
+    """Whole-job throughput: the units every rank processed (replicas: the same per rank) per second
+    of the slowest rank's step."""
+    return units_per_rank * ws_n / (step_ms * 1e-3)
+
+
 def algorithmic_bytes(wl, counts) -> int:
     """K read by the scoring layers + kept K, V rows read and written on every layer + Q_w."""
     elt = 2 if wl.dtype == "bf16" else 4
@@ -230,14 +248,10 @@ def run_gpu(args):
     clocks = sampler.stop()
     ms = [a.elapsed_time(b) for a, b in times]
     ckv.chunkkv_status_check(ws)
-    step_ms = sum(ms) / len(ms)
-    if ws_n > 1:
-        t = torch.tensor([step_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        step_ms = float(t)
+    step_ms = slowest_rank(sum(ms) / len(ms), ws_n)
     nbytes = algorithmic_bytes(wl, cnt)
-    value = nbytes * ws_n / (step_ms * 1e-3) / 1e9
-    tokens_s = wl.T_total * ws_n / (step_ms * 1e-3)
+    value = job_rate(nbytes, ws_n, step_ms) / 1e9
+    tokens_s = job_rate(wl.T_total, ws_n, step_ms)
 
     # ---- device time of each phase inside the same compress call: K more steps with the library's
     # phase events recorded on its stream (a record between two launches ends their overlap, so these
