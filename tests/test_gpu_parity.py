@@ -8,6 +8,7 @@ import torch
 import oracle
 from parity import check_gather, check_indices, check_scores, f64
 from synthetic import configs, generator as gen
+from synthetic.generator import NeedleSpec
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0") if torch.cuda.is_available() else None
@@ -104,6 +105,33 @@ def test_degenerate_parameters(ckv, kw):
     if kw.get("L_max") == 100000:
         n = int(out.counts[0, 0, 0])
         assert n == 1234 and torch.equal(out.indices[0, 0, 0, :n].cpu(), torch.arange(1234, dtype=torch.int32))
+
+
+def test_maximum_batch_ragged(ckv):
+    # CHUNKKV_MAX_BATCH sequences of 0..400 tokens (empty, shorter than the window, several units)
+    rng = np.random.default_rng(2024)
+    seqlens = tuple(int(x) for x in rng.integers(0, 401, size=1024))
+    seqlens = (0,) + seqlens[1:511] + (7,) + seqlens[512:]
+    wl = configs.mistral_ragged().with_params(seqlens=seqlens, B=1024, Hq=8, Hkv=2, w=16, L_max=64,
+                                              n_layers=2, n_reuse=2, needles=NeedleSpec(kind="none"),
+                                              name="max_batch_1024")
+    run_and_check(ckv, wl, seqs=[0, 1, 2, 511, 700, 1023])
+
+
+def test_maximum_window_rows(ckv):
+    # w*G = 4096 window rows per KV head (the library's limit): 32 M tiles on the tensor-core path
+    wl = configs.llama_layer().with_params(seqlens=(1500,), Hq=32, Hkv=1, w=128, L_max=300, name="wG4096")
+    p, keep = ckv.make_params(cu_seqlens=wl.cu_seqlens, Hq=wl.Hq, Hkv=wl.Hkv, d=wl.d, w=wl.w, c=wl.c,
+                              L_max=wl.L_max, dtype=torch.bfloat16)
+    assert ckv.chunkkv_score_path(p) == 1
+    run_and_check(ckv, wl)
+
+
+@pytest.mark.parametrize("d,dtype", [(64, "bf16"), (256, "bf16"), (256, "f32")])
+def test_other_head_dims_portable_path(ckv, d, dtype):
+    wl = configs.llama_layer().with_params(seqlens=(900,), d=d, dtype=dtype, Hq=8, Hkv=2, w=8, L_max=100,
+                                           name=f"d{d}_{dtype}")
+    run_and_check(ckv, wl)
 
 
 @pytest.mark.parametrize("Hq,Hkv,w", [(32, 8, 32), (28, 4, 64)])
