@@ -11,7 +11,6 @@ namespace chunkkv {
 
 std::atomic<unsigned long long> g_launch_count{0};
 
-bool tc_supported(const Plan& pl);                                  // score_tc.cu
 void tc_plan(Plan& pl);                                             // score_tc.cu
 cudaError_t launch_wait_selftest(int32_t* err, long long timeout, cudaStream_t s);   // score_tc.cu
 cudaError_t launch_pack_q(const Plan& pl, const ScoreGeom& g, const void* const* q_layers, int n_layers,

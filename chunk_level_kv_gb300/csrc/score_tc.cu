@@ -132,14 +132,7 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
       ::"r"(dst), "l"((uint64_t)map), "r"(bar), "r"(c0), "r"(c1) : "memory");
 }
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
-                                            int c2) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
-      "[%2];" ::"r"(dst), "l"((uint64_t)map), "r"(bar), "r"(c0), "r"(c1), "r"(c2) : "memory");
-}
-
-// Same as tma_load_3d with an L2 eviction-priority policy (createpolicy) attached.
+// A 3-D tile load with an L2 eviction-priority policy (createpolicy) attached.
 __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
                                                  int c2, uint64_t policy) {
   asm volatile(
@@ -698,10 +691,6 @@ int c_slot(int c) {
 int lcm_i(int a, int b) { return a / gcd_c(a, b) * b; }
 
 }  // namespace tc
-
-bool tc_supported(const Plan& pl) {
-  return pl.elt == 2 && pl.d == tc::kD && pl.wG > 0 && tc::c_slot(pl.c) >= 0 && tc::encode_fn() != nullptr;
-}
 
 void tc_plan(Plan& pl) {
   pl.use_tc = 0;
