@@ -31,6 +31,11 @@ form the rest supports):
       chunks' tokens and the last w tokens (no duplicates).
   R6  Selection is independent per (sequence, layer, KV head); a reuse layer
       reuses the index list of the same (sequence, KV head).
+  R9  The adjacent-layer similarity behind Algorithm 2 (§4.2, "observation":
+      the indices ChunkKV selects are highly similar from one layer to the next,
+      by Jaccard similarity) is taken over the kept index sets I_l of layers
+      scored independently (N_reuse = 1), per (sequence, KV head):
+      J = |I_l ∩ I_{l+1}| / |I_l ∪ I_{l+1}|.
 """
 from __future__ import annotations
 
@@ -178,3 +183,20 @@ def compress_layers(q_win, k, v, cu_seqlens, Hq: int, Hkv: int, w: int, c: int, 
                 vo.append([gather(np.asarray(v[layer][t0:t1, h, :]), idx[b][h]) for h in range(Hkv)])
             res["k_out"][layer], res["v_out"][layer] = ko, vo
     return res
+
+
+# ---------------------------------------------------------------- §4.2 observation (reading R9)
+
+def layer_overlap(idx_a: np.ndarray, idx_b: np.ndarray) -> tuple:
+    """(|A ∩ B|, |A ∪ B|) of two kept index sets: the counts behind the adjacent-layer Jaccard
+    similarity that motivates Algorithm 2 (ChunkKV §4.2, observation; reading R9)."""
+    a = set(int(x) for x in np.asarray(idx_a).ravel())
+    b = set(int(x) for x in np.asarray(idx_b).ravel())
+    return len(a & b), len(a | b)
+
+
+def layer_jaccard(idx_a: np.ndarray, idx_b: np.ndarray) -> float:
+    """|A ∩ B| / |A ∪ B| (1.0 for two empty sets)."""
+    inter, union = layer_overlap(idx_a, idx_b)
+    return 1.0 if union == 0 else inter / union
+

@@ -253,3 +253,51 @@ def test_ragged_batch_is_per_sequence():
                                               k[cu[b]:cu[b + 1], h], 5, 4, 10)
             assert np.array_equal(r["indices"][0][b][h], idx)
     assert r["indices"][0][1][0].size == 0
+
+
+# ---------------------------------------------------------------- adjacent-layer overlap (reading R9)
+
+def _merge_counts(a, b):
+    """Two-pointer merge over sorted, duplicate-free arrays: (|A ∩ B|, |A ∪ B|), a formulation
+    independent of the oracle's set arithmetic."""
+    i = j = inter = union = 0
+    while i < len(a) or j < len(b):
+        if j == len(b) or (i < len(a) and a[i] < b[j]):
+            i += 1
+        elif i == len(a) or b[j] < a[i]:
+            j += 1
+        else:
+            inter += 1
+            i += 1
+            j += 1
+        union += 1
+    return inter, union
+
+
+def test_layer_overlap_closed_forms():
+    a = np.arange(100, 200)
+    assert oracle.layer_overlap(a, a) == (100, 100) and oracle.layer_jaccard(a, a) == 1.0
+    assert oracle.layer_overlap(a, a + 100) == (0, 200) and oracle.layer_jaccard(a, a + 100) == 0.0
+    assert oracle.layer_overlap(a, a[10:30]) == (20, 100)                       # nested
+    assert oracle.layer_overlap(np.arange(0, 10), np.arange(5, 15)) == (5, 15)
+    assert oracle.layer_jaccard([], []) == 1.0 and oracle.layer_overlap([], [3]) == (0, 1)
+
+
+def test_layer_overlap_against_merge_counts():
+    rng = np.random.default_rng(17)
+    for _ in range(200):
+        T = int(rng.integers(1, 400))
+        a = np.sort(rng.choice(T, size=int(rng.integers(0, T + 1)), replace=False))
+        b = np.sort(rng.choice(T, size=int(rng.integers(0, T + 1)), replace=False))
+        assert oracle.layer_overlap(a, b) == _merge_counts(a, b)
+        assert oracle.layer_overlap(a, b) == oracle.layer_overlap(b, a)
+
+
+def test_window_only_budget_gives_identical_lists():
+    # L_max < c keeps only the recent window in every layer, so adjacent layers overlap fully
+    rng = np.random.default_rng(3)
+    T, w, c, d = 300, 16, 10, 8
+    rows = rng.standard_normal((w, d))
+    i1 = oracle.chunkkv_head(rows, rng.standard_normal((T, d)), c, w, 5)[2]
+    i2 = oracle.chunkkv_head(rows, rng.standard_normal((T, d)), c, w, 5)[2]
+    assert oracle.layer_jaccard(i1, i2) == 1.0 and len(i1) == w
