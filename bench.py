@@ -272,6 +272,34 @@ def run_gpu(args):
     roofs = phase_rooflines(wl, cnt, phase_ms, peaks, peak_src, path)
     dominant = max(roofs, key=lambda r: phase_ms[r["phase"]])
 
+    # ---- §4.2 observation behind Algorithm 2: adjacent-layer overlap of the kept lists with every layer
+    # scored (n_reuse = 1), and the device time of the overlap kernel
+    overlap = None
+    if wl.n_layers > 1 and not args.no_diagnostics:
+        idx1 = torch.empty(wl.n_layers, wl.B, wl.Hkv, n_cap, dtype=torch.int32, device=dev)
+        cnt1 = torch.empty(wl.n_layers, wl.B, wl.Hkv, dtype=torch.int32, device=dev)
+        ws1 = torch.zeros(ckv.chunkkv_workspace_size(p, wl.n_layers, 1), dtype=torch.uint8, device=dev)
+        q_all = [x if x is not None else gen.gen_q_window(wl, i, dev) for i, x in enumerate(qs)]   # every layer's own
+        ckv.chunkkv_compress_layers(p, 1, q_all, ks, vs, ko, vo, idx1, cnt1, None, ws1)
+        del ws1
+        inter, uni = ckv.chunkkv_layer_overlap(p, idx1, cnt1)
+        torch.cuda.synchronize()
+        reps = []
+        for _ in range(5):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            ckv.chunkkv_layer_overlap(p, idx1, cnt1)
+            e1.record(stream)
+            reps.append((e0, e1))
+        torch.cuda.synchronize()
+        ov_ms = statistics.median(a.elapsed_time(b) for a, b in reps)
+        read = int(cnt1.sum()) * 4 + cnt1.numel() * 4
+        u = uni.double()
+        jac = torch.where(u > 0, inter.double() / u.clamp(min=1), torch.ones_like(u))
+        overlap = {"lists": wl.n_layers, "mean_adjacent_jaccard": round(float(jac.mean()), 4),
+                   "min_adjacent_jaccard": round(float(jac.min()), 4), "kernel_ms": round(ov_ms, 5),
+                   "index_bytes_read": read, "achieved_GBps": round(read / (ov_ms * 1e-3) / 1e9, 2)}
+
     # ---- end to end through the C-ABI with host buffers (pinned), copies inside the timed region
     e2e = None
     if not args.no_e2e:
@@ -360,6 +388,7 @@ def run_gpu(args):
         "roofline": dominant,
         "roofline_score": next(r for r in roofs if r["phase"] == "score"),
         "phases_ms": {k: round(v, 5) for k, v in phase_ms.items()},
+        "layer_overlap": overlap,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": int(launches),
@@ -439,6 +468,7 @@ def main():
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--workload", choices=sorted(configs.ALL), default="llama_model")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-diagnostics", action="store_true", help="skip the adjacent-layer overlap measurement")
     ap.add_argument("--layers", type=int, default=0, help="keep only the first N layers (profiling)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -51,6 +51,7 @@ def _load():
         "chunkkv_score_noalloc": [P, vp, vp, vp, vp],
         "chunkkv_set_phase_events": [pp, i32],
         "chunkkv_selftest_wait_timeout": [vp, sz, vp],
+        "chunkkv_layer_overlap": [P, i32, vp, vp, vp, vp, vp],
     }
     for name, args in sigs.items():
         fn = getattr(lib, name)

@@ -150,6 +150,17 @@ def chunkkv_compress_layers(p: Params, n_reuse: int, q_win, k, v, k_out, v_out, 
                                        ws.numel() * ws.element_size(), _stream(counts.device)))
 
 
+def chunkkv_layer_overlap(p: Params, indices, counts):
+    """(inter, union) int32 [n_lists - 1, B, Hkv]: overlap counts of adjacent kept index lists
+    (indices [n_lists, B, Hkv, n_cap], counts [n_lists, B, Hkv] as chunkkv_compress_layers writes)."""
+    n = indices.shape[0]
+    inter = torch.empty((max(n - 1, 0),) + tuple(counts.shape[1:]), dtype=torch.int32, device=counts.device)
+    uni = torch.empty_like(inter)
+    _check("chunkkv_layer_overlap", LIB.chunkkv_layer_overlap(ctypes.byref(p), n, _ptr(indices), _ptr(counts),
+                                                              _ptr(inter), _ptr(uni), _stream(counts.device)))
+    return inter, uni
+
+
 def chunkkv_selftest_wait_timeout(ws) -> None:
     """Failure-path self test: a bounded device wait that nothing completes gives up after about a
     millisecond and records code 0x1FF in ws's error word (read it with chunkkv_status_check)."""

@@ -13,6 +13,8 @@ std::atomic<unsigned long long> g_launch_count{0};
 
 void tc_plan(Plan& pl);                                             // score_tc.cu
 cudaError_t launch_wait_selftest(int32_t* err, long long timeout, cudaStream_t s);   // score_tc.cu
+cudaError_t launch_overlap(const SeqTable& st, int Hkv, int n_cap, int n_lists, int max_T, const int32_t* indices,
+                           const int32_t* counts, int32_t* inter, int32_t* uni, cudaStream_t s);   // overlap.cu
 cudaError_t launch_pack_q(const Plan& pl, const ScoreGeom& g, const void* const* q_layers, int n_layers,
                           void* qpack, cudaStream_t s);
 cudaError_t launch_score_tc(const Plan& pl, const ScoreGeom& g, const SeqTable& st, const void* const* k_groups,
@@ -75,6 +77,7 @@ chunkkv_status make_plan(const chunkkv_params* p, int n_layers, int n_reuse, Pla
     n_cap = std::max<int>(n_cap, (int)cap);
   }
   pl.C_max = C_max;
+  pl.max_T = max_T;
   pl.n_cap = n_cap;
   // scoring units: the tensor-core path sizes them for its tiles, the SIMT path
   // uses about 512 keys
@@ -444,6 +447,21 @@ chunkkv_status chunkkv_set_phase_events(void* const* events, int32_t n_events) {
   for (int i = 0; i < CHUNKKV_PHASE_EVENTS; ++i) t_phase_ev[i] = events[i];
   t_phase_n = CHUNKKV_PHASE_EVENTS;
   return CHUNKKV_OK;
+}
+
+chunkkv_status chunkkv_layer_overlap(const chunkkv_params* p, int32_t n_lists, const int32_t* indices,
+                                     const int32_t* counts, int32_t* inter, int32_t* uni, chunkkv_stream_t stream) {
+  Plan pl;
+  static thread_local SeqTable st;
+  chunkkv_status s = make_plan(p, 1, 1, pl, &st);
+  if (s != CHUNKKV_OK) return s;
+  if (n_lists < 1) return CHUNKKV_ERR_INVALID_ARG;
+  if (n_lists == 1 || pl.B * pl.Hkv == 0) return CHUNKKV_OK;
+  if (!counts || !inter || !uni || (pl.n_cap > 0 && !indices)) return CHUNKKV_ERR_INVALID_ARG;
+  if ((size_t)(pl.max_T + 31) / 32 * sizeof(uint32_t) > 227 * 1024) return CHUNKKV_ERR_UNSUPPORTED;
+  if ((int64_t)n_lists - 1 > 65535) return CHUNKKV_ERR_UNSUPPORTED;
+  return cuda_status(launch_overlap(st, pl.Hkv, pl.n_cap, n_lists, pl.max_T, indices, counts, inter, uni,
+                                    (cudaStream_t)stream));
 }
 
 chunkkv_status chunkkv_selftest_wait_timeout(void* ws, size_t ws_bytes, chunkkv_stream_t stream) {

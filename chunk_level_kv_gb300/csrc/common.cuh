@@ -156,7 +156,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // Workspace plan shared by the C-ABI entry points and the launchers.
 struct Plan {
   int32_t B, Hkv, G, d, w, wG, c, L_max, elt;
-  int32_t C_max, n_cap;
+  int32_t C_max, n_cap, max_T;
   int32_t cpu, ku, n_units;
   int32_t use_tc;                 // tensor-core scoring kernel
   int32_t tc_mt;                  // 128-row M tiles of the window rows (tensor-core path)

@@ -34,8 +34,7 @@ namespace tc {
 
 constexpr int kN = 80;                         // keys per tile (MMA N)
 constexpr int kD = 128;                        // head dimension
-constexpr int kStagesK = (115712 - 2 * 128 * 128 - 256) / (2 * kN * 128) < 6
-                             ? (115712 - 2 * 128 * 128 - 256) / (2 * kN * 128) : 6;   // K tiles in shared memory (two CTAs per SM)
+constexpr int kStagesK = 4;                    // key tiles in shared memory (two CTAs of 112 KB per SM)
 constexpr int kStagesQ = 1;                    // Q tile in shared memory (reused across items)
 // The window-row tile lives in TMEM (columns 0..63, copied from shared memory
 // once per tile change) and feeds the MMAs as operand A, so that the tensor
@@ -43,7 +42,7 @@ constexpr int kStagesQ = 1;                    // Q tile in shared memory (reuse
 // M=128, N=80 MMA asks for more shared-memory bandwidth than an SM has).  The
 // accumulators take the columns after it.
 constexpr int kQCols = 64;                     // 128 rows x 128 bf16 = 64 32-bit columns
-constexpr int kStagesT = (256 - kQCols) / kN < 3 ? (256 - kQCols) / kN : 3;   // accumulator stages in TMEM
+constexpr int kStagesT = 2;                    // accumulator stages in TMEM (80 columns each)
 constexpr int kTmemCols = 256;
 static_assert(kStagesT >= 2 && kQCols + kStagesT * kN <= kTmemCols, "TMEM budget");
 constexpr int kThreads = 192;                  // warp 0 TMA, warp 1 MMA, warps 2-5 softmax

@@ -187,6 +187,26 @@ chunkkv_status chunkkv_score_noalloc(const chunkkv_params* p, const void* q_win,
 chunkkv_status chunkkv_status_check(void* ws, chunkkv_stream_t stream, int32_t* device_code);
 
 /*
+ * Adjacent-layer overlap of kept index lists: the Jaccard similarity of
+ * consecutive layers' selections that ChunkKV §4.2 reports as the observation
+ * behind Algorithm 2 (layer-wise index reuse), as exact counts.  Run on lists
+ * scored independently per layer (chunkkv_compress_layers with n_reuse = 1) it
+ * measures how much a reuse depth N_reuse would change the kept tokens.
+ *   indices: device [n_lists, B, Hkv, n_cap_max] int32, each list ascending and
+ *            duplicate-free in [0, T_b) for its first counts[...] entries
+ *            (the layout chunkkv_compress_layers writes);
+ *   counts:  device [n_lists, B, Hkv] int32;
+ *   inter, uni: device [n_lists - 1, B, Hkv] int32, written with
+ *            |I_l ∩ I_{l+1}| and |I_l ∪ I_{l+1}| for l = 0 .. n_lists - 2
+ *            (Jaccard = inter / uni; two empty lists give 0 / 0).
+ * Positions outside [0, T_b) are ignored.  n_lists == 1 or an empty batch
+ * writes nothing.  Returns CHUNKKV_ERR_UNSUPPORTED when a sequence is longer
+ * than the kernel's shared-memory bitmap holds (about 1.86 M tokens).
+ */
+chunkkv_status chunkkv_layer_overlap(const chunkkv_params* p, int32_t n_lists, const int32_t* indices,
+                                     const int32_t* counts, int32_t* inter, int32_t* uni, chunkkv_stream_t stream);
+
+/*
  * Self test of the failure path (a test aid; no counterpart in the pages).
  * Launches one thread that waits, through the same bounded wait as the
  * tensor-core scoring kernel, on a barrier that nothing completes.  The wait

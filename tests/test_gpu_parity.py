@@ -190,6 +190,56 @@ def test_bounded_wait_gives_up_and_reports(ckv):
     assert verdicts == ["exact", "exact"]
 
 
+@pytest.mark.parametrize("case", ["llama6", "ragged3"])
+def test_layer_overlap_counts(ckv, case):
+    # adjacent-layer overlap of the kept lists of independently scored layers (n_reuse = 1),
+    # bit-exact against the oracle's set counts on the GPU's own lists
+    if case == "llama6":
+        wl = configs.llama_model().with_params(seqlens=(3000,), n_layers=6, n_reuse=1, L_max=600, name="overlap6")
+    else:
+        wl = configs.mistral_ragged().with_params(seqlens=(1000, 0, 20, 2500, 7, 333), B=6, n_layers=3,
+                                                  n_reuse=1, L_max=256, name="overlap_ragged")
+    qs, ks, vs, _ = gen.make_all_layers(wl, DEV)
+    out = ckv.compress_layers(qs, ks, vs, wl.cu_seqlens, Hq=wl.Hq, Hkv=wl.Hkv, w=wl.w, c=wl.c, L_max=wl.L_max,
+                              n_reuse=1)
+    p, keep = ckv.make_params(cu_seqlens=wl.cu_seqlens, Hq=wl.Hq, Hkv=wl.Hkv, d=wl.d, w=wl.w, c=wl.c,
+                              L_max=wl.L_max, dtype=ks[0].dtype)
+    inter, uni = ckv.chunkkv_layer_overlap(p, out.indices, out.counts)
+    idx, cnt = out.indices.cpu().numpy(), out.counts.cpu().numpy()
+    inter, uni = inter.cpu().numpy(), uni.cpu().numpy()
+    jac = []
+    for l in range(wl.n_layers - 1):
+        for b in range(wl.B):
+            for h in range(wl.Hkv):
+                want = oracle.layer_overlap(idx[l, b, h, :cnt[l, b, h]], idx[l + 1, b, h, :cnt[l + 1, b, h]])
+                assert (int(inter[l, b, h]), int(uni[l, b, h])) == want, (l, b, h)
+                if want[1]:
+                    jac.append(want[0] / want[1])
+    if case == "llama6":
+        # 16 of 20 needle spans survive from layer to layer: selections overlap well above chance
+        assert np.mean(jac) > 0.2
+
+
+def test_layer_overlap_on_given_lists(ckv):
+    # identical, disjoint and partly overlapping lists, and positions outside [0, T) ignored
+    T, n_cap = 100, 8
+    p, keep = ckv.make_params(cu_seqlens=[0, T], Hq=2, Hkv=2, d=64, w=4, c=2, L_max=4, dtype=torch.float32)
+    lists = np.full((3, 1, 2, n_cap), -1, dtype=np.int32)
+    cnt = np.zeros((3, 1, 2), dtype=np.int32)
+    lists[0, 0, 0, :4], cnt[0, 0, 0] = [1, 5, 9, 97], 4
+    lists[1, 0, 0, :4], cnt[1, 0, 0] = [1, 5, 9, 97], 4
+    lists[2, 0, 0, :3], cnt[2, 0, 0] = [2, 5, 98], 3
+    lists[0, 0, 1, :2], cnt[0, 0, 1] = [0, 1], 2
+    lists[1, 0, 1, :3], cnt[1, 0, 1] = [2, 3, 150], 3          # 150 >= T: ignored by the probe
+    lists[2, 0, 1, :0], cnt[2, 0, 1] = [], 0
+    n_cap_lib, _ = ckv.chunkkv_out_capacity(p)
+    buf = np.full((3, 1, 2, n_cap_lib), -1, dtype=np.int32)
+    buf[..., :n_cap] = lists
+    inter, uni = ckv.chunkkv_layer_overlap(p, torch.from_numpy(buf).to(DEV), torch.from_numpy(cnt).to(DEV))
+    assert inter.cpu().tolist() == [[[4, 0]], [[1, 0]]]
+    assert uni.cpu().tolist() == [[[4, 5]], [[6, 3]]]
+
+
 def test_select_is_bit_exact_on_given_scores(ckv):
     # both sides decide on the same fp32 scores: the selection must match exactly (ties included)
     rng = np.random.default_rng(0)
