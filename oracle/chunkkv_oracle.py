@@ -36,6 +36,10 @@ form the rest supports):
       by Jaccard similarity) is taken over the kept index sets I_l of layers
       scored independently (N_reuse = 1), per (sequence, KV head):
       J = |I_l ∩ I_{l+1}| / |I_l ∪ I_{l+1}|.
+  R10 Optional causal window (an option beside reading R1's unmasked window):
+      window query q (0 <= q < w) sits at sequence position T - w + q and sees
+      only keys j <= T - w + q; a query whose position is negative (T < w) sees
+      no key and adds nothing.
 """
 from __future__ import annotations
 
@@ -57,11 +61,14 @@ def group_window_rows(q_win_seq: np.ndarray, h: int, G: int) -> np.ndarray:
     return np.concatenate(rows, axis=0).astype(np.float64)
 
 
-def key_scores(rows: np.ndarray, keys: np.ndarray) -> np.ndarray:
+def key_scores(rows: np.ndarray, keys: np.ndarray, limits=None) -> np.ndarray:
     """Per-key attention mass a_j = sum over window rows of softmax_j(rows . keys^T / sqrt(d)).
 
     ChunkKV §4.1 Algorithm 1 step 1 (window attention A, w x T_k) with the
     probabilities of Kara §2 Eq. (1) (reading R1).  rows [R, d], keys [T, d].
+    limits: None, or per row the last key index the row may see (reading R10):
+    the softmax of row r runs over keys 0..limits[r] only, and a row with a
+    negative limit adds nothing.
     """
     T, d = keys.shape
     if T == 0:
@@ -69,10 +76,20 @@ def key_scores(rows: np.ndarray, keys: np.ndarray) -> np.ndarray:
     if rows.shape[0] == 0:
         return np.zeros(T)
     logits = (rows.astype(np.float64) @ keys.astype(np.float64).T) / math.sqrt(d)   # [R, T]
-    logits -= logits.max(axis=1, keepdims=True)
-    p = np.exp(logits)
-    p /= p.sum(axis=1, keepdims=True)                                                # each row sums to 1
-    return p.sum(axis=0)
+    if limits is None:
+        logits -= logits.max(axis=1, keepdims=True)
+        p = np.exp(logits)
+        p /= p.sum(axis=1, keepdims=True)                                            # each row sums to 1
+        return p.sum(axis=0)
+    a = np.zeros(T)
+    for r, lim in enumerate(limits):
+        n = min(int(lim), T - 1) + 1                                                 # keys 0 .. lim
+        if n <= 0:
+            continue
+        x = logits[r, :n] - logits[r, :n].max()
+        p = np.exp(x)
+        a[:n] += p / p.sum()
+    return a
 
 
 def chunk_scores(a: np.ndarray, c: int) -> np.ndarray:
@@ -117,10 +134,18 @@ def kept_indices(chunks: list, T: int, c: int, w: int) -> np.ndarray:
     return np.array(sorted(keep), dtype=np.int64)
 
 
-def chunkkv_head(rows: np.ndarray, keys: np.ndarray, c: int, w: int, L_max: int):
+def window_limits(n_rows: int, T: int, w: int) -> np.ndarray:
+    """Last visible key of each window row under the causal window (reading R10): rows are ordered
+    (group member g, window row q) as group_window_rows returns them; row q sits at T - w + q."""
+    q = np.arange(n_rows) % max(w, 1)
+    return T - w + q
+
+
+def chunkkv_head(rows: np.ndarray, keys: np.ndarray, c: int, w: int, L_max: int, causal: bool = False):
     """Algorithm 1 for one (sequence, KV head): returns (A, selected chunks, kept indices)."""
     T = keys.shape[0]
-    A = chunk_scores(key_scores(rows, keys), c)
+    limits = window_limits(rows.shape[0], T, w) if causal else None
+    A = chunk_scores(key_scores(rows, keys, limits), c)
     sel = top_chunks(A, n_select(T, c, L_max))
     return A, sel, kept_indices(sel, T, c, w)
 
@@ -138,7 +163,7 @@ def scoring_layer(layer: int, n_reuse: int) -> int:
 
 
 def compress_layers(q_win, k, v, cu_seqlens, Hq: int, Hkv: int, w: int, c: int, L_max: int,
-                    n_reuse: int, want_kv: bool = True):
+                    n_reuse: int, want_kv: bool = True, causal: bool = False):
     """ChunkKV with layer-wise index reuse over all layers of a batch of sequences.
 
     q_win[l]: [B, w, Hq, d] (read for layers with l mod N_reuse == 0 only);
@@ -165,7 +190,7 @@ def compress_layers(q_win, k, v, cu_seqlens, Hq: int, Hkv: int, w: int, c: int, 
                 row_s, row_c, row_i = [], [], []
                 for h in range(Hkv):
                     A, sel, idx = chunkkv_head(group_window_rows(qb, h, G),
-                                               np.asarray(k[layer][t0:t1, h, :]), c, w, L_max)
+                                               np.asarray(k[layer][t0:t1, h, :]), c, w, L_max, causal)
                     row_s.append(A)
                     row_c.append(sel)
                     row_i.append(idx)

@@ -301,3 +301,54 @@ def test_window_only_budget_gives_identical_lists():
     i1 = oracle.chunkkv_head(rows, rng.standard_normal((T, d)), c, w, 5)[2]
     i2 = oracle.chunkkv_head(rows, rng.standard_normal((T, d)), c, w, 5)[2]
     assert oracle.layer_jaccard(i1, i2) == 1.0 and len(i1) == w
+
+
+# ---------------------------------------------------------------- causal window option (reading R10)
+
+def test_causal_window_of_one_row_is_unmasked():
+    # the single window query sits at T - 1 and sees every key
+    rng = np.random.default_rng(21)
+    rows, keys = rng.standard_normal((3, 8)), rng.standard_normal((57, 8))      # G = 3 rows of one window position
+    lim = oracle.window_limits(3, 57, 1)
+    assert np.array_equal(lim, [56, 56, 56])
+    assert np.allclose(oracle.key_scores(rows, keys, lim), oracle.key_scores(rows, keys), rtol=0, atol=1e-15)
+
+
+def test_causal_window_zero_keys_closed_form():
+    # K = 0: window query q sees T - w + q + 1 keys with equal probability
+    T, w, G, d = 23, 5, 2, 4
+    rows = np.random.default_rng(1).standard_normal((G * w, d))
+    a = oracle.key_scores(rows, np.zeros((T, d)), oracle.window_limits(G * w, T, w))
+    want = np.zeros(T)
+    for q in range(w):
+        n = T - w + q + 1
+        want[:n] += G / n
+    assert np.allclose(a, want, rtol=0, atol=1e-14)
+    assert math.isclose(a.sum(), G * w, rel_tol=1e-14)
+
+
+def test_causal_window_brute_force_50_digits():
+    rng = np.random.default_rng(8)
+    T, w, d = 9, 4, 3
+    rows, keys = rng.standard_normal((w, d)), rng.standard_normal((T, d))
+    lim = oracle.window_limits(w, T, w)
+    got = oracle.key_scores(rows, keys, lim)
+    mpmath.mp.dps = 50
+    want = [mpmath.mpf(0)] * T
+    for r in range(w):
+        s = [sum(mpmath.mpf(float(rows[r, e])) * mpmath.mpf(float(keys[j, e])) for e in range(d)) / mpmath.sqrt(d)
+             for j in range(T)]
+        for j in range(int(lim[r]) + 1):
+            want[j] += 1 / sum(mpmath.e ** (s[i] - s[j]) for i in range(int(lim[r]) + 1))
+    assert np.allclose(got, [float(x) for x in want], rtol=1e-13, atol=1e-15)
+
+
+def test_causal_window_rows_before_the_sequence_add_nothing():
+    # T < w: window queries at negative positions see no key
+    rng = np.random.default_rng(4)
+    T, w, d = 3, 5, 4
+    rows, keys = rng.standard_normal((w, d)), rng.standard_normal((T, d))
+    lim = oracle.window_limits(w, T, w)                       # -2, -1, 0, 1, 2
+    a = oracle.key_scores(rows, keys, lim)
+    assert math.isclose(a.sum(), 3.0, rel_tol=1e-14)          # only the three rows at 0, 1, 2 count
+    assert np.allclose(a, oracle.key_scores(rows[2:], keys, lim[2:]), rtol=0, atol=1e-15)
