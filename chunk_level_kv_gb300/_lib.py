@@ -28,6 +28,7 @@ class Params(ctypes.Structure):
         ("cu_seqlens", ctypes.POINTER(ctypes.c_int32)),
         ("q_stride_b", ctypes.c_int64), ("q_stride_w", ctypes.c_int64), ("q_stride_h", ctypes.c_int64),
         ("kv_stride_t", ctypes.c_int64), ("kv_stride_h", ctypes.c_int64),
+        ("causal_window", ctypes.c_int32),
     ]
 
 

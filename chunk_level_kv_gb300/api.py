@@ -44,7 +44,7 @@ def _stream(device) -> ctypes.c_void_p:
 
 
 def make_params(*, cu_seqlens, Hq: int, Hkv: int, d: int, w: int, c: int, L_max: int,
-                dtype: torch.dtype, q_strides=None, kv_strides=None):
+                dtype: torch.dtype, q_strides=None, kv_strides=None, causal_window: bool = False):
     """chunkkv_params from sizes; q_strides = (b, w, head), kv_strides = (token, head) in elements.
 
     Returns (params, keepalive): keepalive owns the host cu_seqlens array.
@@ -58,17 +58,17 @@ def make_params(*, cu_seqlens, Hq: int, Hkv: int, d: int, w: int, c: int, L_max:
     p = Params(B=B, Hq=Hq, Hkv=Hkv, d=d, w=w, c=c, L_max=L_max, dtype=_DT[dtype],
                cu_seqlens=ctypes.cast(cu, ctypes.POINTER(ctypes.c_int32)),
                q_stride_b=q_strides[0], q_stride_w=q_strides[1], q_stride_h=q_strides[2],
-               kv_stride_t=kv_strides[0], kv_stride_h=kv_strides[1])
+               kv_stride_t=kv_strides[0], kv_stride_h=kv_strides[1], causal_window=int(bool(causal_window)))
     return p, cu
 
 
-def params_for(q_win, k, cu_seqlens, *, Hkv: int, w: int, c: int, L_max: int):
+def params_for(q_win, k, cu_seqlens, *, Hkv: int, w: int, c: int, L_max: int, causal_window: bool = False):
     """chunkkv_params describing q_win [B, w, Hq, d] and k [T_total, Hkv, d] as laid out in memory."""
     Hq, d = q_win.shape[2], q_win.shape[3]
     assert q_win.stride(3) == 1 and k.stride(2) == 1, "the head dimension must be contiguous"
     return make_params(cu_seqlens=cu_seqlens, Hq=Hq, Hkv=Hkv, d=d, w=w, c=c, L_max=L_max,
                        dtype=k.dtype, q_strides=(q_win.stride(0), q_win.stride(1), q_win.stride(2)),
-                       kv_strides=(k.stride(0), k.stride(1)))
+                       kv_strides=(k.stride(0), k.stride(1)), causal_window=causal_window)
 
 
 def chunkkv_out_capacity(p: Params):
@@ -187,11 +187,12 @@ class CompressResult:
 
 
 def compress_layers(q_win, k, v, cu_seqlens, *, Hq: int, Hkv: int, w: int, c: int, L_max: int,
-                    n_reuse: int = 1, return_scores: bool = False, workspace=None) -> CompressResult:
+                    n_reuse: int = 1, return_scores: bool = False, workspace=None,
+                    causal_window: bool = False) -> CompressResult:
     """Allocate outputs with torch and run chunkkv_compress_layers on the current stream."""
     k0 = k[0]
     q0 = next(x for x in q_win if x is not None)
-    p, keep = params_for(q0, k0, cu_seqlens, Hkv=Hkv, w=w, c=c, L_max=L_max)
+    p, keep = params_for(q0, k0, cu_seqlens, Hkv=Hkv, w=w, c=c, L_max=L_max, causal_window=causal_window)
     assert p.Hq == Hq
     n_cap, c_max = chunkkv_out_capacity(p)
     n_layers = len(k)

@@ -36,6 +36,7 @@ chunkkv_status check_params(const chunkkv_params* p) {
     return CHUNKKV_ERR_INVALID_ARG;
   if (p->Hq % p->Hkv != 0) return CHUNKKV_ERR_INVALID_ARG;
   if (p->dtype != CHUNKKV_F32 && p->dtype != CHUNKKV_BF16) return CHUNKKV_ERR_INVALID_ARG;
+  if (p->causal_window != 0 && p->causal_window != 1) return CHUNKKV_ERR_INVALID_ARG;
   if (p->B > CHUNKKV_MAX_BATCH || p->d > kMaxD) return CHUNKKV_ERR_UNSUPPORTED;
   if ((int64_t)p->w * (p->Hq / p->Hkv) > kMaxWG) return CHUNKKV_ERR_UNSUPPORTED;
   if ((int64_t)p->B * p->Hkv > 65535) return CHUNKKV_ERR_UNSUPPORTED;
@@ -148,7 +149,7 @@ chunkkv_status make_plan(const chunkkv_params* p, int n_layers, int n_reuse, Pla
 }
 
 ScoreGeom score_geom(const chunkkv_params* p, const Plan& pl) {
-  ScoreGeom g;
+  ScoreGeom g = {};
   g.Hq = p->Hq;
   g.Hkv = p->Hkv;
   g.G = pl.G;
@@ -161,6 +162,7 @@ ScoreGeom score_geom(const chunkkv_params* p, const Plan& pl) {
   g.n_units = pl.n_units;
   g.C_max = pl.C_max;
   g.alpha = (float)(1.4426950408889634 / sqrt((double)p->d));
+  g.causal = p->causal_window;
   g.q_stride_b = p->q_stride_b;
   g.q_stride_w = p->q_stride_w;
   g.q_stride_h = p->q_stride_h;
@@ -215,7 +217,7 @@ cudaError_t run_post_score(const Plan& pl, const ScoreGeom& g, const SeqTable& s
 }
 
 SelectGeom select_geom(const chunkkv_params* p, const Plan& pl) {
-  SelectGeom sg;
+  SelectGeom sg = {};
   sg.Hkv = p->Hkv;
   sg.c = p->c;
   sg.w = p->w;
@@ -229,7 +231,7 @@ SelectGeom select_geom(const chunkkv_params* p, const Plan& pl) {
 }
 
 GatherGeom gather_geom(const chunkkv_params* p, const Plan& pl) {
-  GatherGeom gg;
+  GatherGeom gg = {};
   gg.Hkv = p->Hkv;
   gg.d = p->d;
   gg.elt = pl.elt;

@@ -7,6 +7,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <climits>
 
 #include "chunkkv.h"
 
@@ -65,6 +66,7 @@ struct ScoreGeom {
   int32_t n_units;    // Hkv * uoff[B]
   int32_t C_max;      // chunk capacity of the score array
   float alpha;        // log2(e) / sqrt(d): logits are handled as base-2 exponents
+  int32_t causal;     // window query q sees keys 0 .. T - w + q only (chunkkv_params.causal_window)
   int64_t q_stride_b, q_stride_w, q_stride_h;
   int64_t kv_stride_t, kv_stride_h;
   // Distance (in floats) between the buffers of consecutive reuse groups, for the

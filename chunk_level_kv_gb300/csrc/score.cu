@@ -61,6 +61,9 @@ score_simt_kernel(const E* __restrict__ q, const E* __restrict__ k, ScoreGeom g,
     const int r = rb + tid;
     const bool active = r < g.wG;
     const float* qrow = qs + tid * ld;
+    // causal window: the row's window query (r mod w) sees keys up to T - w + (r mod w);
+    // in unit-local key numbers that is `last` (may be negative: nothing visible)
+    const int last = g.causal ? T - g.w + (g.w > 0 ? r % g.w : 0) - k0 : INT_MAX;
 
     // sweep 1: row maximum of the base-2 exponents over the unit
     float m = -INFINITY;
@@ -73,7 +76,7 @@ score_simt_kernel(const E* __restrict__ q, const E* __restrict__ k, ScoreGeom g,
       }
       __syncthreads();
       if (active) {
-        for (int j = 0; j < nt; ++j) {
+        for (int j = 0; j < nt && kt + j <= last; ++j) {
           float dot = 0.f;
           const float* kr = ks + j * ld;
           for (int e = 0; e < g.d; ++e) dot = fmaf(qrow[e], kr[e], dot);
@@ -104,7 +107,7 @@ score_simt_kernel(const E* __restrict__ q, const E* __restrict__ k, ScoreGeom g,
             acc = 0.f;
             cur = ch;
           }
-          const float p = exp2f(dot * g.alpha - m);
+          const float p = kt + j <= last ? exp2f(dot * g.alpha - m) : 0.f;
           acc += p;
           l += p;
         }
@@ -178,10 +181,14 @@ finalize_kernel(ScoreGeom g, const __grid_constant__ SeqTable st, const float* _
       float M = -INFINITY;
       for (int v = 0; v < U; ++v) M = fmaxf(M, rl_head[v * stride_u + r]);
       float S = 0.f;
-      for (int v = 0; v < U; ++v) S += rl_head[v * stride_u + g.wG + r] * exp2f(rl_head[v * stride_u + r] - M);
+      for (int v = 0; v < U; ++v) {
+        const float l = rl_head[v * stride_u + g.wG + r];
+        if (l > 0.f) S += l * exp2f(rl_head[v * stride_u + r] - M);   // units the row saw no key of add nothing
+      }
       lse = M + log2f(S);
     }
-    wts[r] = exp2f(rl[(int64_t)gu * 2 * g.wG + r] - lse);
+    const float R = rl[(int64_t)gu * 2 * g.wG + r];
+    wts[r] = R == -INFINITY ? 0.f : exp2f(R - lse);        // a row that saw no key in this unit
   }
   __syncthreads();
 

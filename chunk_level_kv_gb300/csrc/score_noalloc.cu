@@ -97,7 +97,7 @@ extern "C" chunkkv_status chunkkv_score_noalloc(const chunkkv_params* p, const v
   pl.B = p->B;
   pl.Hkv = p->Hkv;
   pl.elt = p->dtype == CHUNKKV_BF16 ? 2 : 4;
-  ScoreGeom g;
+  ScoreGeom g = {};
   g.Hq = p->Hq;
   g.Hkv = p->Hkv;
   g.G = G;
@@ -110,6 +110,7 @@ extern "C" chunkkv_status chunkkv_score_noalloc(const chunkkv_params* p, const v
   g.n_units = (int32_t)n_units;
   g.C_max = C_max;
   g.alpha = (float)(1.4426950408889634 / sqrt((double)p->d));
+  g.causal = p->causal_window;
   g.q_stride_b = p->q_stride_b;
   g.q_stride_w = p->q_stride_w;
   g.q_stride_h = p->q_stride_h;

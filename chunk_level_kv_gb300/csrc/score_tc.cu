@@ -67,6 +67,7 @@ constexpr int kMaxGroups = 32;
 
 struct TcGeom {
   int32_t B, Hkv, wG, MT, cpu, ku;
+  int32_t w;                         // window length (for the causal-window limit)
   int32_t items_pg;                  // work items per group: units x M tiles
   int32_t n_items;                   // items_pg x groups of this launch
   int64_t slot_bytes;                // bytes between the scratch slots of consecutive groups
@@ -329,7 +330,7 @@ __device__ __forceinline__ float tile_max(uint32_t taddr, int valid) {
 }
 
 // ---------------------------------------------------------------- the kernel
-template <int C>
+template <int C, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 2)
 score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_constant__ SeqTable st,
                 float* __restrict__ rl, bin_t* __restrict__ bins, int32_t* __restrict__ err) {
@@ -498,6 +499,8 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
       float* url = (float*)((char*)rl + it.grp * g.slot_bytes) + (size_t)it.unit * 2 * g.wG + row;
       RowState s{make_float2(0.f, 0.f), make_float2(0.f, 0.f), 0.f};
       const float2 alpha2 = make_float2(g.alpha, g.alpha);
+      // causal window: packed position of the window's first query (T - w in the sequence)
+      const int64_t causal_from = CAUSAL ? (int64_t)st.cu[it.b + 1] - g.w : 0;
       float R = 0.f;
       bool ok = true;
       for (int t = 0; t < ntile; ++t) {
@@ -509,7 +512,15 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
         tc_fence_after();
         if (warp_live) {
           const uint32_t taddr = lane_base + kQCols + ts * kN;
-          const int valid = min(kN, nk - t * kN);
+          int valid = min(kN, nk - t * kN);
+          bool mask = valid < kN;
+          if (CAUSAL && it.tok0 + t * kN + kN > causal_from) {
+            // a tile reaching the window: the row's window query sees keys up to
+            // T - w + (row mod w), a per-thread limit (the TMEM loads stay warp-wide)
+            const int last = causal_from + row % g.w - (int)(it.tok0 + t * kN);
+            valid = max(min(valid, last + 1), 0);
+            mask = __any_sync(0xffffffffu, valid < kN);
+          }
           if (t == 0) {
             R = tile_max(taddr, valid) * g.alpha;
             s.negR = make_float2(-R, -R);
@@ -517,7 +528,7 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
           const int ph = (t * kN) % C;
           const int q = (t * kN) / C;
           const RowState before = s;
-          tile_dispatch<C>(ph, valid < kN, taddr, alpha2, s, ubins + (size_t)q * g.wG, g.wG, valid, write, bpol);
+          tile_dispatch<C>(ph, mask, taddr, alpha2, s, ubins + (size_t)q * g.wG, g.wG, valid, write, bpol);
           // every bin is at most the row sum: one test per tile catches any value
           // that outgrew the reference (and inf / NaN)
           const bool over = !(s.l <= kBig);
@@ -536,7 +547,7 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
             s.carry = make_float2(s.carry.x * f, s.carry.y * f);
             R = R2;
             s.negR = make_float2(-R2, -R2);
-            tile_dispatch<C>(ph, valid < kN, taddr, alpha2, s, ubins + (size_t)q * g.wG, g.wG, valid, write, bpol);
+            tile_dispatch<C>(ph, mask, taddr, alpha2, s, ubins + (size_t)q * g.wG, g.wG, valid, write, bpol);
           }
         }
         tc_fence_before();
@@ -656,7 +667,7 @@ DeviceInfo& device_info(int dev) {
   return d;
 }
 
-template <int C>
+template <int C, bool CAUSAL>
 cudaError_t launch_c(const TcGeom& tg, const TcMaps& maps, const SeqTable& st, float* rl, bin_t* bins, int32_t* err,
                      int slot, cudaStream_t s) {
   int dev = 0;
@@ -664,7 +675,7 @@ cudaError_t launch_c(const TcGeom& tg, const TcMaps& maps, const SeqTable& st, f
   if (e != cudaSuccess) return e;
   DeviceInfo& di = device_info(dev);
   if (!di.attr_set[slot]) {
-    e = cudaFuncSetAttribute(score_tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    e = cudaFuncSetAttribute(score_tc_kernel<C, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     di.attr_set[slot] = true;
   }
@@ -675,8 +686,15 @@ cudaError_t launch_c(const TcGeom& tg, const TcMaps& maps, const SeqTable& st, f
   const int period = tg.Hkv * tg.MT;
   if (grid >= period) grid -= grid % period;
   grid = std::min(tg.n_items, grid);
-  return launch_pdl(score_tc_kernel<C>, dim3(grid), dim3(kThreads), (size_t)kSmemBytes, s, maps, tg, st, rl, bins,
+  return launch_pdl(score_tc_kernel<C, CAUSAL>, dim3(grid), dim3(kThreads), (size_t)kSmemBytes, s, maps, tg, st, rl, bins,
                     err);
+}
+
+template <int C>
+cudaError_t launch_causal(bool causal, const TcGeom& tg, const TcMaps& maps, const SeqTable& st, float* rl,
+                          bin_t* bins, int32_t* err, int slot, cudaStream_t s) {
+  return causal ? launch_c<C, true>(tg, maps, st, rl, bins, err, slot + 8, s)
+                : launch_c<C, false>(tg, maps, st, rl, bins, err, slot, s);
 }
 
 constexpr int kSupportedC[] = {3, 4, 5, 8, 10, 16, 20, 30};
@@ -759,13 +777,14 @@ cudaError_t launch_score_tc(const Plan& pl, const ScoreGeom& g, const SeqTable& 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     }
-    tc::TcGeom tg;
+    tc::TcGeom tg = {};
     tg.B = pl.B;
     tg.Hkv = pl.Hkv;
     tg.wG = pl.wG;
     tg.MT = MT;
     tg.cpu = pl.cpu;
     tg.ku = pl.ku;
+    tg.w = g.w;
     tg.items_pg = g.n_units * MT;
     tg.n_items = tg.items_pg * n;
     tg.slot_bytes = slot_bytes;
@@ -775,14 +794,14 @@ cudaError_t launch_score_tc(const Plan& pl, const ScoreGeom& g, const SeqTable& 
     bin_t* bg = (bin_t*)((char*)bins + g0 * slot_bytes);
     cudaError_t e = cudaErrorNotSupported;
     switch (pl.c) {
-      case 3: e = tc::launch_c<3>(tg, maps, st, rlg, bg, err, 0, s); break;
-      case 4: e = tc::launch_c<4>(tg, maps, st, rlg, bg, err, 1, s); break;
-      case 5: e = tc::launch_c<5>(tg, maps, st, rlg, bg, err, 2, s); break;
-      case 8: e = tc::launch_c<8>(tg, maps, st, rlg, bg, err, 3, s); break;
-      case 10: e = tc::launch_c<10>(tg, maps, st, rlg, bg, err, 4, s); break;
-      case 16: e = tc::launch_c<16>(tg, maps, st, rlg, bg, err, 5, s); break;
-      case 20: e = tc::launch_c<20>(tg, maps, st, rlg, bg, err, 6, s); break;
-      case 30: e = tc::launch_c<30>(tg, maps, st, rlg, bg, err, 7, s); break;
+      case 3: e = tc::launch_causal<3>(g.causal != 0, tg, maps, st, rlg, bg, err, 0, s); break;
+      case 4: e = tc::launch_causal<4>(g.causal != 0, tg, maps, st, rlg, bg, err, 1, s); break;
+      case 5: e = tc::launch_causal<5>(g.causal != 0, tg, maps, st, rlg, bg, err, 2, s); break;
+      case 8: e = tc::launch_causal<8>(g.causal != 0, tg, maps, st, rlg, bg, err, 3, s); break;
+      case 10: e = tc::launch_causal<10>(g.causal != 0, tg, maps, st, rlg, bg, err, 4, s); break;
+      case 16: e = tc::launch_causal<16>(g.causal != 0, tg, maps, st, rlg, bg, err, 5, s); break;
+      case 20: e = tc::launch_causal<20>(g.causal != 0, tg, maps, st, rlg, bg, err, 6, s); break;
+      case 30: e = tc::launch_causal<30>(g.causal != 0, tg, maps, st, rlg, bg, err, 7, s); break;
     }
     if (e != cudaSuccess) return e;
   }

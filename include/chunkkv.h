@@ -83,6 +83,9 @@ typedef struct chunkkv_params {
   const int32_t* cu_seqlens;  /* HOST array [B+1]: cu[0] = 0, non-decreasing; T_b = cu[b+1]-cu[b] */
   int64_t q_stride_b, q_stride_w, q_stride_h;   /* element strides of q_win                     */
   int64_t kv_stride_t, kv_stride_h;             /* element strides of k and v (and their layers) */
+  int32_t causal_window;  /* 0: every window query sees all T_b keys (the algorithm as printed);
+                             1: window query q (0 <= q < w) sits at position T_b - w + q and sees
+                             keys 0 .. T_b - w + q only (a query at a negative position adds nothing) */
 } chunkkv_params;
 
 /*

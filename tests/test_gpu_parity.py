@@ -21,12 +21,12 @@ def ckv():
 
 
 def run_and_check(ckv, wl, layers_to_check=None, heads=None, seqs=None, qs=None, ks=None, vs=None,
-                  spans=None):
+                  spans=None, causal=False):
     """Compress all layers on the GPU; compare scoring groups / heads / sequences with the oracle."""
     if ks is None:
         qs, ks, vs, spans = gen.make_all_layers(wl, DEV)
     out = ckv.compress_layers(qs, ks, vs, wl.cu_seqlens, Hq=wl.Hq, Hkv=wl.Hkv, w=wl.w, c=wl.c,
-                              L_max=wl.L_max, n_reuse=wl.n_reuse, return_scores=True)
+                              L_max=wl.L_max, n_reuse=wl.n_reuse, return_scores=True, causal_window=causal)
     assert ckv.chunkkv_status_check(out.workspace) == 0
     cu = wl.cu_seqlens
     G = wl.G
@@ -45,8 +45,9 @@ def run_and_check(ckv, wl, layers_to_check=None, heads=None, seqs=None, qs=None,
             T = cu[b + 1] - cu[b]
             kb = f64(kf[cu[b]:cu[b + 1]])
             for h in heads:
-                A = oracle.chunk_scores(oracle.key_scores(oracle.group_window_rows(qf[b], h, G), kb[:, h]),
-                                        wl.c)
+                rows = oracle.group_window_rows(qf[b], h, G)
+                lim = oracle.window_limits(rows.shape[0], T, wl.w) if causal else None
+                A = oracle.chunk_scores(oracle.key_scores(rows, kb[:, h], lim), wl.c)
                 what = f"{wl.name} group {g} seq {b} head {h}"
                 check_scores(scores[g, b, h], A, what)
                 n = int(cnt[g, b, h])
@@ -238,6 +239,25 @@ def test_layer_overlap_on_given_lists(ckv):
     inter, uni = ckv.chunkkv_layer_overlap(p, torch.from_numpy(buf).to(DEV), torch.from_numpy(cnt).to(DEV))
     assert inter.cpu().tolist() == [[[4, 0]], [[1, 0]]]
     assert uni.cpu().tolist() == [[[4, 5]], [[6, 3]]]
+
+
+@pytest.mark.parametrize("case", ["tiny_f32", "bf16_G4", "bf16_G7_c30", "ragged_short"])
+def test_causal_window(ckv, case):
+    # chunkkv_params.causal_window = 1: window query q sees keys up to T - w + q (reading R10)
+    if case == "tiny_f32":
+        wl = configs.tiny()
+    elif case == "bf16_G4":
+        wl = configs.llama_layer().with_params(seqlens=(3001,), L_max=300, name="causal_G4")
+    elif case == "bf16_G7_c30":
+        wl = configs.llama_layer().with_params(seqlens=(4500,), c=30, w=64, Hq=28, Hkv=4, L_max=900,
+                                               name="causal_G7")
+    else:
+        wl = configs.mistral_ragged().with_params(seqlens=(1000, 0, 20, 2500, 7, 333), B=6, n_layers=3,
+                                                  L_max=256, name="causal_ragged")
+    out, _ = run_and_check(ckv, wl, causal=True)
+    # the option changes the scores of the chunks inside the window
+    plain, _ = run_and_check(ckv, wl, causal=False)
+    assert not torch.equal(out.chunk_scores, plain.chunk_scores)
 
 
 def test_select_is_bit_exact_on_given_scores(ckv):
