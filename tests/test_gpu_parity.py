@@ -260,6 +260,18 @@ def test_causal_window(ckv, case):
     assert not torch.equal(out.chunk_scores, plain.chunk_scores)
 
 
+def test_hybrid_chunk_then_token_level(ckv):
+    # §5.7 hybrid policy: chunk-level selection (c = 10) in the lower half of the layers and
+    # token-level selection (c = 1) in the upper half, as two calls over the two halves
+    wl = configs.llama_model().with_params(seqlens=(2500,), n_layers=4, n_reuse=1, L_max=500, name="hybrid")
+    qs, ks, vs, spans = gen.make_all_layers(wl, DEV)
+    lower = wl.with_params(n_layers=2, name="hybrid_lower_c10")
+    upper = wl.with_params(n_layers=2, c=1, name="hybrid_upper_c1")
+    out_lo, _ = run_and_check(ckv, lower, qs=qs[:2], ks=ks[:2], vs=vs[:2], spans=spans[:2])
+    out_hi, _ = run_and_check(ckv, upper, qs=qs[2:], ks=ks[2:], vs=vs[2:], spans=spans[2:])
+    assert out_lo.indices.shape[-1] >= 500 and out_hi.indices.shape[-1] >= 500
+
+
 def test_select_is_bit_exact_on_given_scores(ckv):
     # both sides decide on the same fp32 scores: the selection must match exactly (ties included)
     rng = np.random.default_rng(0)
