@@ -215,7 +215,9 @@ def compress_layers(q_win, k, v, cu_seqlens, *, Hq: int, Hkv: int, w: int, c: in
 
 
 __all__ = [
-    "ChunkKVError", "CompressResult", "Params", "chunkkv_compress_layers", "chunkkv_gather",
-    "chunkkv_out_capacity", "chunkkv_score", "chunkkv_score_noalloc", "chunkkv_score_path", "chunkkv_select", "chunkkv_status_check",
-    "chunkkv_workspace_size", "compress_layers", "make_params", "params_for", "MAX_GATHER_LAYERS",
+    "ChunkKVError", "CompressResult", "Params", "MAX_GATHER_LAYERS", "PHASES", "PHASE_EVENTS",
+    "chunkkv_compress_layers", "chunkkv_gather", "chunkkv_launch_count", "chunkkv_layer_overlap",
+    "chunkkv_out_capacity", "chunkkv_score", "chunkkv_score_noalloc", "chunkkv_score_path", "chunkkv_select",
+    "chunkkv_selftest_wait_timeout", "chunkkv_set_phase_events", "chunkkv_status_check",
+    "chunkkv_workspace_size", "compress_layers", "make_params", "params_for",
 ]

@@ -30,6 +30,19 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 bool aligned16(const void* ptr) { return ((uintptr_t)ptr & 15u) == 0; }
 
+// SMs of the current device.  Without a visible device (sizes computed on a
+// host that has no GPU) a GB300's 152 is assumed; a plan made for another SM
+// count then asks for a different workspace size, which the size check catches.
+int current_sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
+    cudaGetLastError();
+    return 152;
+  }
+  return sms;
+}
+
 chunkkv_status check_params(const chunkkv_params* p) {
   if (p == nullptr) return CHUNKKV_ERR_INVALID_ARG;
   if (p->B < 0 || p->Hq < 1 || p->Hkv < 1 || p->d < 1 || p->w < 0 || p->c < 1 || p->L_max < 0)
@@ -87,9 +100,9 @@ chunkkv_status make_plan(const chunkkv_params* p, int n_layers, int n_reuse, Pla
   tc_plan(pl);                                    // may switch to the tensor-core geometry
   if (pl.use_tc) {
     // Unit length for the persistent tensor-core grid: the multiple m of the
-    // base unit that minimises (waves of work items) x (tiles per item) on a
-    // two-CTA-per-SM GB300 (304 slots); ties go to longer units.
-    const int slots = 2 * 152;
+    // base unit that minimises (waves of work items) x (tiles per item) with
+    // two CTAs per SM (304 slots on a GB300); ties go to longer units.
+    const int slots = 2 * current_sm_count();
     const int64_t per_unit_items = (int64_t)p->Hkv * pl.tc_mt;
     const int base_tiles = pl.tc_base_chunks * p->c / pl.tc_tile_n;
     int64_t best_cost = INT64_MAX;
@@ -194,7 +207,6 @@ cudaError_t run_score_groups(const Plan& pl, const ScoreGeom& g, const SeqTable&
   return cudaSuccess;
 }
 
-// Log-sum-exp and finalisation of n_groups consecutive slots into their chunk scores.
 // Phase events of chunkkv_set_phase_events (this host thread), recorded only
 // inside chunkkv_compress_layers.
 thread_local void* t_phase_ev[CHUNKKV_PHASE_EVENTS];
@@ -206,6 +218,7 @@ cudaError_t phase_mark(int i, cudaStream_t s) {
   return cudaEventRecord((cudaEvent_t)t_phase_ev[i], s);
 }
 
+// Log-sum-exp and finalisation of n_groups consecutive slots into their chunk scores.
 cudaError_t run_post_score(const Plan& pl, const ScoreGeom& g, const SeqTable& st, char* slots, float* scores,
                            int n_groups, cudaStream_t s) {
   float* rl = (float*)(slots + pl.off_rl);
@@ -477,12 +490,15 @@ uint64_t chunkkv_launch_count(void) { return chunkkv::g_launch_count.load(std::m
 chunkkv_status chunkkv_status_check(void* ws, chunkkv_stream_t stream, int32_t* device_code) {
   if (ws == nullptr) return CHUNKKV_ERR_INVALID_ARG;
   cudaStream_t cs = (cudaStream_t)stream;
-  if (cudaStreamSynchronize(cs) != cudaSuccess) return CHUNKKV_ERR_CUDA;
+  // everything on the caller's stream, so that no other stream is waited for
   int32_t code = 0;
-  if (cudaMemcpy(&code, ws, sizeof(code), cudaMemcpyDeviceToHost) != cudaSuccess) return CHUNKKV_ERR_CUDA;
+  if (cudaMemcpyAsync(&code, ws, sizeof(code), cudaMemcpyDeviceToHost, cs) != cudaSuccess ||
+      cudaStreamSynchronize(cs) != cudaSuccess)
+    return CHUNKKV_ERR_CUDA;
   if (device_code) *device_code = code;
   if (code != 0) {
-    if (cudaMemset(ws, 0, sizeof(int32_t)) != cudaSuccess) return CHUNKKV_ERR_CUDA;
+    if (cudaMemsetAsync(ws, 0, sizeof(int32_t), cs) != cudaSuccess || cudaStreamSynchronize(cs) != cudaSuccess)
+      return CHUNKKV_ERR_CUDA;
     return CHUNKKV_ERR_TIMEOUT;
   }
   return CHUNKKV_OK;

@@ -146,9 +146,11 @@ cudaError_t launch_score_simt(const Plan& pl, const ScoreGeom& g, const SeqTable
 }
 
 // ------------------------------------------------------------------ finalisation
-// One CTA per unit.  lse_r is formed from the (R, l) pairs of every unit of the
-// same (sequence, head); the unit's bins are then weighted by 2^(R_r - lse_r)
-// and summed over rows, one warp per chunk (coalesced over rows).
+// One CTA per (unit, block of up to 128 chunks, reuse group).  The weights
+// 2^(R_r - lse_r) go to shared memory (lse_r from lse_kernel, or formed here
+// from the (R, l) pairs of every unit of the head when no lse array is given);
+// the bins are then weighted and summed over rows, each warp taking eight
+// chunks at a time with its lanes on consecutive rows (coalesced loads).
 constexpr int kFinThreads = 256;
 constexpr int kFinChunks = 128;                 // chunks per CTA: blockIdx.y tiles a unit
 
@@ -175,7 +177,7 @@ finalize_kernel(ScoreGeom g, const __grid_constant__ SeqTable st, const float* _
 
   for (int r = threadIdx.x; r < g.wG; r += blockDim.x) {
     float lse;
-    if (lse_rows != nullptr) {                      // formed by the scoring kernel
+    if (lse_rows != nullptr) {                      // formed by lse_kernel
       lse = lse_rows[((int64_t)b * g.Hkv + h) * lse_stride + r];
     } else {
       float M = -INFINITY;

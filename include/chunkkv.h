@@ -13,8 +13,10 @@
  * The window scores are attention probabilities as in "Kara" §2 Eq. (1):
  * softmax over all T keys of (Q_w K^T / sqrt(d)) for each window-query row,
  * summed over the w window rows and over the G = Hq / Hkv query heads that
- * share a KV head (query head hq belongs to KV head hq / G).  There is no
- * causal mask inside the window.  Top-k ties go to the lower chunk index.
+ * share a KV head (query head hq belongs to KV head hq / G).  By default no
+ * causal mask applies inside the window (the algorithm as printed);
+ * chunkkv_params.causal_window = 1 masks each window query to the keys at or
+ * before its own position.  Top-k ties go to the lower chunk index.
  * The kept list is the ascending, duplicate-free union of the selected
  * chunks' tokens and the last w tokens.
  *
@@ -22,8 +24,8 @@
  *  - Device pointers point to GPU global memory owned by the caller; the
  *    library never allocates or frees device memory while it runs and keeps
  *    no per-call state between calls (its one fixed device array is the
- *    scratch of chunkkv_score_noalloc, described there).  Host arrays (cu_seqlens, pointer tables) are read
- *    during the call only.
+ *    scratch of chunkkv_score_noalloc, described there).  Host arrays
+ *    (cu_seqlens, pointer tables) are read during the call only.
  *  - Every call is asynchronous on the given stream (0 = legacy default).
  *  - Arguments are checked on the host before anything is launched; a bad
  *    argument returns an error code and launches nothing.  A failed launch
