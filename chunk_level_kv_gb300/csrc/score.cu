@@ -146,40 +146,75 @@ cudaError_t launch_score_simt(const Plan& pl, const ScoreGeom& g, const SeqTable
 }
 
 // ------------------------------------------------------------------ finalisation
-// One CTA per (unit, block of up to 128 chunks, reuse group).  The weights
-// 2^(R_r - lse_r) go to shared memory (lse_r from lse_kernel, or formed here
-// from the (R, l) pairs of every unit of the head when no lse array is given);
-// the bins are then weighted and summed over rows, each warp taking eight
-// chunks at a time with its lanes on consecutive rows (coalesced loads).
+// One CTA per (unit, block of up to 128 chunks, reuse group).  Chunk i of the
+// unit scores A_i = sum_r bin[i][r] * 2^(R_r - lse_r); each warp takes eight
+// chunks at a time with its lanes on consecutive rows (coalesced bin loads).
+//  - With an lse array (lse_kernel ran before), every lane forms the weights
+//    of its own rows from R and lse as it loads its bins: all loads of a step
+//    are issued together and the CTA needs no shared memory or barrier.
+//  - Without one (the no-allocation scoring call), the weights go to shared
+//    memory first, lse_r being formed from the (R, l) pairs of every unit of
+//    the head.
 constexpr int kFinThreads = 256;
 constexpr int kFinChunks = 128;                 // chunks per CTA: blockIdx.y tiles a unit
 
-__global__ void __launch_bounds__(kFinThreads)
+// weight of one row: 2^(R - lse), zero for a row that saw no key in this unit
+__device__ __forceinline__ float fin_weight(float R, float lse) { return R == -INFINITY ? 0.f : exp2f(R - lse); }
+
+// Weights of rows r .. r+NV-1 (r a multiple of NV, NV in {1, 4, 8}).
+template <bool LSE, int NV>
+__device__ __forceinline__ void fin_weights(float (&wv)[NV], const float* wts, const float* Rrow, const float* Lrow,
+                                            int r) {
+  if constexpr (!LSE) {
+#pragma unroll
+    for (int j = 0; j < NV; j += (NV >= 4 ? 4 : 1)) {
+      if constexpr (NV >= 4) {
+        const float4 x = *reinterpret_cast<const float4*>(wts + r + j);
+        wv[j] = x.x, wv[j + 1] = x.y, wv[j + 2] = x.z, wv[j + 3] = x.w;
+      } else {
+        wv[j] = wts[r + j];
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < NV; j += (NV >= 4 ? 4 : 1)) {
+      if constexpr (NV >= 4) {
+        const float4 R = *reinterpret_cast<const float4*>(Rrow + r + j);
+        const float4 L = *reinterpret_cast<const float4*>(Lrow + r + j);
+        wv[j] = fin_weight(R.x, L.x), wv[j + 1] = fin_weight(R.y, L.y);
+        wv[j + 2] = fin_weight(R.z, L.z), wv[j + 3] = fin_weight(R.w, L.w);
+      } else {
+        wv[j] = fin_weight(Rrow[r + j], Lrow[r + j]);
+      }
+    }
+  }
+}
+
+template <bool LSE>
+__global__ void __launch_bounds__(kFinThreads, 4)
 finalize_kernel(ScoreGeom g, const __grid_constant__ SeqTable st, const float* __restrict__ rl,
-                const bin_t* __restrict__ bins, const float* __restrict__ lse_rows, int lse_stride,
-                float* __restrict__ scores) {
-  extern __shared__ float wts[];                // [wG]
+                const bin_t* __restrict__ bins, const float* __restrict__ lse_rows, float* __restrict__ scores) {
+  extern __shared__ float wts[];                // [wG], only without an lse array
   int b, h, u;
   const int gu = blockIdx.x;
   const int cb = blockIdx.y * kFinChunks;       // this CTA's block of the unit's chunks
   rl += blockIdx.z * g.rl_gs;                   // this CTA's reuse group
   bins += blockIdx.z * g.bins_gs;
-  if (lse_rows != nullptr) lse_rows += blockIdx.z * g.lse_gs;
   scores += blockIdx.z * g.scores_gs;
   pdl_wait();
   decode_unit(st, g.Hkv, gu, b, h, u);
   const int T = st.cu[b + 1] - st.cu[b];
   const int C = (T + g.c - 1) / g.c;
   if (min(g.cpu, C - u * g.cpu) <= cb) return;  // no chunk of this unit in this block
-  const int U = st.uoff[b + 1] - st.uoff[b];
-  const int64_t stride_u = (int64_t)g.Hkv * 2 * g.wG;          // between units of one head
-  const float* rl_head = rl + ((int64_t)st.uoff[b] * g.Hkv + h) * 2 * g.wG;
-
-  for (int r = threadIdx.x; r < g.wG; r += blockDim.x) {
-    float lse;
-    if (lse_rows != nullptr) {                      // formed by lse_kernel
-      lse = lse_rows[((int64_t)b * g.Hkv + h) * lse_stride + r];
-    } else {
+  const float* Rrow = rl + (int64_t)gu * 2 * g.wG;                 // R of this unit's rows
+  const float* Lrow = nullptr;
+  if constexpr (LSE) {
+    Lrow = lse_rows + blockIdx.z * g.lse_gs + ((int64_t)b * g.Hkv + h) * g.wG;
+  } else {
+    const int U = st.uoff[b + 1] - st.uoff[b];
+    const int64_t stride_u = (int64_t)g.Hkv * 2 * g.wG;          // between units of one head
+    const float* rl_head = rl + ((int64_t)st.uoff[b] * g.Hkv + h) * 2 * g.wG;
+    for (int r = threadIdx.x; r < g.wG; r += blockDim.x) {
       float M = -INFINITY;
       for (int v = 0; v < U; ++v) M = fmaxf(M, rl_head[v * stride_u + r]);
       float S = 0.f;
@@ -187,18 +222,15 @@ finalize_kernel(ScoreGeom g, const __grid_constant__ SeqTable st, const float* _
         const float l = rl_head[v * stride_u + g.wG + r];
         if (l > 0.f) S += l * exp2f(rl_head[v * stride_u + r] - M);   // units the row saw no key of add nothing
       }
-      lse = M + log2f(S);
+      wts[r] = fin_weight(Rrow[r], M + log2f(S));
     }
-    const float R = rl[(int64_t)gu * 2 * g.wG + r];
-    wts[r] = R == -INFINITY ? 0.f : exp2f(R - lse);        // a row that saw no key in this unit
+    __syncthreads();
   }
-  __syncthreads();
 
   const int nc = min(min(g.cpu, C - u * g.cpu) - cb, kFinChunks);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const bin_t* ub = bins + ((int64_t)gu * g.cpu + cb) * g.wG;
   float* out = scores + ((int64_t)b * g.Hkv + h) * g.C_max + (int64_t)u * g.cpu + cb;
-  // each warp sums eight chunks at a time: eight independent load streams per lane
   constexpr int kW = kFinThreads / 32;
   constexpr int kG = 8;
   for (int ch0 = warp * kG; ch0 < nc; ch0 += kW * kG) {
@@ -210,42 +242,44 @@ finalize_kernel(ScoreGeom g, const __grid_constant__ SeqTable st, const float* _
     if ((g.wG & 7) == 0 && g.wG >= 256) {
       // eight consecutive rows per lane: 16-byte loads of eight bins, kG of them in flight
       for (int r = 8 * lane; r < g.wG; r += 256) {
-        const float4 wa = *reinterpret_cast<const float4*>(wts + r);
-        const float4 wb = *reinterpret_cast<const float4*>(wts + r + 4);
         uint4 v[kG];
 #pragma unroll
         for (int i = 0; i < kG; ++i)
           v[i] = i < m ? __ldcs(reinterpret_cast<const uint4*>(cbase + (int64_t)i * g.wG + r)) : make_uint4(0u, 0u, 0u, 0u);
+        float wv[8];
+        fin_weights<LSE, 8>(wv, wts, Rrow, Lrow, r);
 #pragma unroll
         for (int i = 0; i < kG; ++i) {
           const float2 b01 = bin_decode2(v[i].x), b23 = bin_decode2(v[i].y);
           const float2 b45 = bin_decode2(v[i].z), b67 = bin_decode2(v[i].w);
-          acc[i] = fmaf(b01.x, wa.x, fmaf(b01.y, wa.y, fmaf(b23.x, wa.z, fmaf(b23.y, wa.w, acc[i]))));
-          acc[i] = fmaf(b45.x, wb.x, fmaf(b45.y, wb.y, fmaf(b67.x, wb.z, fmaf(b67.y, wb.w, acc[i]))));
+          acc[i] = fmaf(b01.x, wv[0], fmaf(b01.y, wv[1], fmaf(b23.x, wv[2], fmaf(b23.y, wv[3], acc[i]))));
+          acc[i] = fmaf(b45.x, wv[4], fmaf(b45.y, wv[5], fmaf(b67.x, wv[6], fmaf(b67.y, wv[7], acc[i]))));
         }
       }
     } else if ((g.wG & 3) == 0) {
       // four consecutive rows per lane: 8-byte loads of four bins, kG of them in flight
       for (int r = 4 * lane; r < g.wG; r += 128) {
-        const float4 w4 = *reinterpret_cast<const float4*>(wts + r);
         uint2 v[kG];
 #pragma unroll
         for (int i = 0; i < kG; ++i)
           v[i] = i < m ? __ldcs(reinterpret_cast<const uint2*>(cbase + (int64_t)i * g.wG + r)) : make_uint2(0u, 0u);
+        float wv[4];
+        fin_weights<LSE, 4>(wv, wts, Rrow, Lrow, r);
 #pragma unroll
         for (int i = 0; i < kG; ++i) {
           const float2 b01 = bin_decode2(v[i].x), b23 = bin_decode2(v[i].y);
-          acc[i] = fmaf(b01.x, w4.x, fmaf(b01.y, w4.y, fmaf(b23.x, w4.z, fmaf(b23.y, w4.w, acc[i]))));
+          acc[i] = fmaf(b01.x, wv[0], fmaf(b01.y, wv[1], fmaf(b23.x, wv[2], fmaf(b23.y, wv[3], acc[i]))));
         }
       }
     } else {
       for (int r = lane; r < g.wG; r += 32) {
-        const float wr = wts[r];
         float v[kG];
 #pragma unroll
         for (int i = 0; i < kG; ++i) v[i] = i < m ? bin_decode(__ldcs(cbase + (int64_t)i * g.wG + r)) : 0.f;
+        float wv[1];
+        fin_weights<LSE, 1>(wv, wts, Rrow, Lrow, r);
 #pragma unroll
-        for (int i = 0; i < kG; ++i) acc[i] = fmaf(v[i], wr, acc[i]);
+        for (int i = 0; i < kG; ++i) acc[i] = fmaf(v[i], wv[0], acc[i]);
       }
     }
 #pragma unroll
@@ -341,15 +375,18 @@ cudaError_t launch_finalize(const Plan& pl, const ScoreGeom& g, const SeqTable& 
   if (g.n_units == 0 || n_groups == 0) return cudaSuccess;
   if (g.wG == 0)
     return launch_pdl(zero_scores_kernel, dim3(g.n_units, 1, n_groups), dim3(128), 0, s, g, st, scores);
+  dim3 grid(g.n_units, (g.cpu + kFinChunks - 1) / kFinChunks, n_groups);
+  if (lse != nullptr)
+    return launch_pdl(finalize_kernel<true>, grid, dim3(kFinThreads), 0, s, g, st, (const float*)rl, bins, lse,
+                      scores);
   const size_t smem = (size_t)g.wG * sizeof(float);
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(finalize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(finalize_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
   }
-  dim3 grid(g.n_units, (g.cpu + kFinChunks - 1) / kFinChunks, n_groups);
-  return launch_pdl(finalize_kernel, grid, dim3(kFinThreads), smem, s, g, st, (const float*)rl, bins, lse,
-                    (int)g.wG, scores);
+  return launch_pdl(finalize_kernel<false>, grid, dim3(kFinThreads), smem, s, g, st, (const float*)rl, bins, lse,
+                    scores);
 }
 
 }  // namespace chunkkv

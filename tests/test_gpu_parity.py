@@ -272,6 +272,36 @@ def test_hybrid_chunk_then_token_level(ckv):
     assert out_lo.indices.shape[-1] >= 500 and out_hi.indices.shape[-1] >= 500
 
 
+def test_decode_time_recompression(ckv):
+    # Decode-time compression (reading R11): the score-based paradigm of Kara §2 Eqs. (2)-(3)
+    # compresses again once the cache reaches its threshold.  Here the cache of each (sequence,
+    # KV head) is its compressed prompt followed by the tokens decoded since, and Algorithm 1 runs
+    # over it with the latest w queries as the window.  Heads keep different counts after the
+    # first pass, so the second pass treats every head's cache as a sequence of its own (one KV
+    # head, its G query heads).
+    wl = configs.llama_layer().with_params(seqlens=(3001,), L_max=600, name="decode_prefill")
+    out1, _ = run_and_check(ckv, wl)
+    n1 = [int(x) for x in out1.counts[0, 0].cpu()]
+    tail = 347                                   # tokens decoded since the first pass
+    assert all(n + tail > wl.L_max + wl.w for n in n1)
+    wl2 = wl.with_params(seqlens=tuple(n + tail for n in n1), B=wl.Hkv, Hq=wl.G, Hkv=1, seed=wl.seed + 500,
+                         needles=NeedleSpec(kind="none"), name="decode_recompress")
+    q2 = gen.gen_q_window(wl2, 0, DEV)
+    k2 = gen.gen_kv_raw(wl2, 0, gen.TENSOR_K, DEV)
+    v2 = gen.gen_kv_raw(wl2, 0, gen.TENSOR_V, DEV)
+    cu2 = wl2.cu_seqlens
+    for h, n in enumerate(n1):                   # the compressed prompt, then the decoded tokens
+        k2[cu2[h]:cu2[h] + n, 0] = out1.k_out[0][0, h, :n]
+        v2[cu2[h]:cu2[h] + n, 0] = out1.v_out[0][0, h, :n]
+    out2, _ = run_and_check(ckv, wl2, qs=[q2], ks=[k2], vs=[v2], spans=[None])
+    # the second pass keeps the newest w tokens of every cache
+    for h, n in enumerate(n1):
+        cnt = int(out2.counts[0, h, 0])
+        got = out2.indices[0, h, 0, :cnt].cpu().numpy()
+        T2 = n + tail
+        assert (got[-wl.w:] == np.arange(T2 - wl.w, T2)).all()
+
+
 def test_select_is_bit_exact_on_given_scores(ckv):
     # both sides decide on the same fp32 scores: the selection must match exactly (ties included)
     rng = np.random.default_rng(0)
