@@ -30,6 +30,19 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 bool aligned16(const void* ptr) { return ((uintptr_t)ptr & 15u) == 0; }
 
+// The tensor-core scoring kernel reads a scoring layer's keys through a TMA
+// tensor map, which needs device memory; everything else the kernels read or
+// write with plain loads and stores, which may also be host memory that the
+// GPU addresses directly (pinned or registered).
+bool device_memory(const void* ptr) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeDevice;
+}
+
 // SMs of the current device.  Without a visible device (sizes computed on a
 // host that has no GPU) a GB300's 152 is assumed; a plan made for another SM
 // count then asks for a different workspace size, which the size check catches.
@@ -337,6 +350,7 @@ chunkkv_status chunkkv_score(const chunkkv_params* p, const void* q_win, const v
       !aligned16(ws))
     return CHUNKKV_ERR_INVALID_ARG;
   if (ws_bytes < pl.total_bytes) return CHUNKKV_ERR_WORKSPACE_TOO_SMALL;
+  if (pl.use_tc && !device_memory(k)) return CHUNKKV_ERR_INVALID_ARG;
   cudaStream_t cs = (cudaStream_t)stream;
   char* w = (char*)ws;
   char* base = w + pl.header_bytes;
@@ -407,6 +421,9 @@ chunkkv_status chunkkv_compress_layers(const chunkkv_params* p, int32_t n_layers
       return CHUNKKV_ERR_INVALID_ARG;
   }
   if (ws_bytes < pl.total_bytes) return CHUNKKV_ERR_WORKSPACE_TOO_SMALL;
+  if (pl.use_tc)
+    for (int l = 0; l < n_layers; l += n_reuse)
+      if (!device_memory(k[l])) return CHUNKKV_ERR_INVALID_ARG;
   cudaStream_t cs = (cudaStream_t)stream;
   char* w = (char*)ws;
   char* base = w + pl.header_bytes;

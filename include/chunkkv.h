@@ -26,6 +26,15 @@
  *    no per-call state between calls (its one fixed device array is the
  *    scratch of chunkkv_score_noalloc, described there).  Host arrays
  *    (cu_seqlens, pointer tables) are read during the call only.
+ *  - "Addressable" pointers (the K/V data that only the gather and the
+ *    portable scoring kernel touch, marked below) may also point to host
+ *    memory that the GPU reads and writes directly: pinned (cudaHostAlloc,
+ *    cudaHostRegister) or, on systems with coherent host access, any host
+ *    memory.  The kernels then move only the kept rows across the host link
+ *    (NVLink-C2C on Grace systems) instead of a staging copy of whole
+ *    layers.  Keys read by the tensor-core scoring kernel go through a TMA
+ *    tensor map and must be device memory; a host pointer there is rejected
+ *    with CHUNKKV_ERR_INVALID_ARG before anything is launched.
  *  - Every call is asynchronous on the given stream (0 = legacy default).
  *  - Arguments are checked on the host before anything is launched; a bad
  *    argument returns an error code and launches nothing.  A failed launch
@@ -111,8 +120,9 @@ chunkkv_status chunkkv_workspace_size(const chunkkv_params* p, int32_t n_layers,
  * Window scores per chunk for one layer (ChunkKV §4.1 Algorithm 1 steps 1-3,
  * with the probabilities of Kara §2 Eq. (1)):
  *   A[b][h][i] = sum over g < G, q < w, j in chunk i of softmax_j(Q_w[b,q,h*G+g,:] . K[b,j,h,:] / sqrt(d))
- * q_win, k: device, layouts above.  chunk_scores: device, written for i < C_b.
- * ws: device workspace of ws_bytes >= chunkkv_workspace_size(p, 1, 1).
+ * q_win: addressable; k: device when chunkkv_score_path(p) is 1 (tensor
+ * cores), else addressable; layouts above.  chunk_scores: device, written for
+ * i < C_b.  ws: device workspace of ws_bytes >= chunkkv_workspace_size(p, 1, 1).
  */
 chunkkv_status chunkkv_score(const chunkkv_params* p, const void* q_win, const void* k,
                              float* chunk_scores, void* ws, size_t ws_bytes, chunkkv_stream_t stream);
@@ -132,8 +142,9 @@ chunkkv_status chunkkv_select(const chunkkv_params* p, const float* chunk_scores
  * index_select of K and V by a kept-index list (ChunkKV §4.1 Algorithm 1 step
  * 6), for n_layers layers that share one list (ChunkKV §4.2 Algorithm 2):
  *   k_out[l][b][h][r][:] = k[l][cu_seqlens[b] + indices[b][h][r]][h][:]  for r < counts[b][h]
- * and the same for v.  k, v, k_out, v_out: HOST arrays of n_layers device
- * pointers (1 <= n_layers <= CHUNKKV_MAX_GATHER_LAYERS); indices, counts: device.
+ * and the same for v.  k, v, k_out, v_out: HOST arrays of n_layers
+ * addressable pointers (1 <= n_layers <= CHUNKKV_MAX_GATHER_LAYERS); indices,
+ * counts: device.
  * Indices must lie in [0, T_b); the copy is bit-exact.
  */
 chunkkv_status chunkkv_gather(const chunkkv_params* p, int32_t n_layers, const int32_t* indices,
@@ -145,9 +156,11 @@ chunkkv_status chunkkv_gather(const chunkkv_params* p, int32_t n_layers, const i
  * Algorithm 1): layers with l % n_reuse == 0 run score + select into index
  * group g = l / n_reuse; every layer l gathers its own K, V with group
  * l / n_reuse.
- *   q_win: HOST array of n_layers device pointers (entries of layers with
- *          l % n_reuse != 0 are not read and may be NULL);
- *   k, v, k_out, v_out: HOST arrays of n_layers device pointers;
+ *   q_win: HOST array of n_layers addressable pointers (entries of layers
+ *          with l % n_reuse != 0 are not read and may be NULL);
+ *   k, v, k_out, v_out: HOST arrays of n_layers addressable pointers, except
+ *          that k[l] of a scoring layer (l % n_reuse == 0) is device memory
+ *          when chunkkv_score_path(p) is 1;
  *   indices: device [ceil(n_layers / n_reuse), B, Hkv, n_cap_max];
  *   counts:  device [ceil(n_layers / n_reuse), B, Hkv];
  *   chunk_scores: NULL, or device [ceil(n_layers / n_reuse), B, Hkv, C_max];

@@ -357,6 +357,79 @@ def test_gather_is_bit_exact(ckv):
                 assert not ko[layer][b, h, n:].any()          # rows beyond the count are untouched
 
 
+def test_gather_operands_in_pinned_host_memory(ckv):
+    # K, V read from and K', V' written to pinned host memory by the gather kernel itself (the GPU
+    # addresses it across the host link): bit-exact, rows beyond the count untouched
+    rng = np.random.default_rng(2)
+    seqlens = [500, 3, 129]
+    cu = [0] + list(itertools.accumulate(seqlens))
+    Hkv, d = 4, 128
+    p, keep = ckv.make_params(cu_seqlens=cu, Hq=Hkv, Hkv=Hkv, d=d, w=8, c=10, L_max=100,
+                              dtype=torch.bfloat16)
+    n_cap, _ = ckv.chunkkv_out_capacity(p)
+    k = [torch.randn(cu[-1], Hkv, d).to(torch.bfloat16).pin_memory() for _ in range(2)]
+    v = [torch.randn(cu[-1], Hkv, d).to(torch.bfloat16).pin_memory() for _ in range(2)]
+    counts = torch.tensor([[min(n_cap, T) - (h % 2) * min(n_cap, T) // 3 for h in range(Hkv)] for T in seqlens],
+                          dtype=torch.int32)
+    idx = torch.zeros(len(seqlens), Hkv, n_cap, dtype=torch.int32)
+    for b, T in enumerate(seqlens):
+        for h in range(Hkv):
+            n = int(counts[b, h])
+            idx[b, h, :n] = torch.from_numpy(np.sort(rng.choice(T, size=n, replace=False))).int()
+    ko = [torch.zeros(len(seqlens), Hkv, n_cap, d, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    vo = [torch.zeros_like(x).pin_memory() for x in ko]
+    ckv.chunkkv_gather(p, idx.to(DEV), counts.to(DEV), k, v, ko, vo)
+    torch.cuda.synchronize()
+    for layer in range(2):
+        for b in range(len(seqlens)):
+            for h in range(Hkv):
+                n = int(counts[b, h])
+                check_gather(ko[layer][b, h, :n], k[layer][cu[b]:cu[b + 1], h], idx[b, h, :n].numpy())
+                check_gather(vo[layer][b, h, :n], v[layer][cu[b]:cu[b + 1], h], idx[b, h, :n].numpy())
+                assert not ko[layer][b, h, n:].any() and not vo[layer][b, h, n:].any()
+
+
+def test_compress_with_host_resident_kv(ckv):
+    # the scoring layers' keys in device memory (the tensor-core kernel reads them through TMA), the
+    # other layers' K and every V in pinned host memory, K' and V' written to pinned host memory:
+    # identical to the all-device call.  A scoring layer's keys in host memory are rejected before
+    # anything is launched.
+    wl = configs.llama_model().with_params(seqlens=(3000, 1234), B=2, n_layers=4, n_reuse=2, L_max=600,
+                                           name="host_kv")
+    qs, ks, vs, _ = gen.make_all_layers(wl, DEV)
+    ref = ckv.compress_layers(qs, ks, vs, wl.cu_seqlens, Hq=wl.Hq, Hkv=wl.Hkv, w=wl.w, c=wl.c,
+                              L_max=wl.L_max, n_reuse=wl.n_reuse)
+    p, keep = ckv.params_for(next(q for q in qs if q is not None), ks[0], wl.cu_seqlens, Hkv=wl.Hkv, w=wl.w,
+                             c=wl.c, L_max=wl.L_max)
+    assert ckv.chunkkv_score_path(p) == 1
+    hk = [x.cpu().pin_memory() for x in ks]
+    hv = [x.cpu().pin_memory() for x in vs]
+    kmix = [ks[layer] if layer % wl.n_reuse == 0 else hk[layer] for layer in range(wl.n_layers)]
+    hko = [torch.zeros(x.shape, dtype=x.dtype).pin_memory() for x in ref.k_out]
+    hvo = [torch.zeros(x.shape, dtype=x.dtype).pin_memory() for x in ref.v_out]
+    idx, cnt = torch.empty_like(ref.indices), torch.empty_like(ref.counts)
+    ws = torch.zeros(ckv.chunkkv_workspace_size(p, wl.n_layers, wl.n_reuse), dtype=torch.uint8, device=DEV)
+    ckv.chunkkv_compress_layers(p, wl.n_reuse, qs, kmix, hv, hko, hvo, idx, cnt, None, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(cnt, ref.counts)
+    counts = cnt.cpu()
+    for layer in range(wl.n_layers):
+        grp = layer // wl.n_reuse
+        for b in range(wl.B):
+            for h in range(wl.Hkv):
+                n = int(counts[grp, b, h])
+                assert torch.equal(idx[grp, b, h, :n], ref.indices[grp, b, h, :n])
+                for got, want in ((hko, ref.k_out), (hvo, ref.v_out)):
+                    assert torch.equal(got[layer][b, h, :n].view(torch.int16),
+                                       want[layer][b, h, :n].cpu().view(torch.int16))
+                    assert not got[layer][b, h, n:].any()
+    assert ckv.chunkkv_status_check(ws) == 0
+    kbad = [hk[0]] + list(ks[1:])
+    with pytest.raises(ckv.ChunkKVError) as e:
+        ckv.chunkkv_compress_layers(p, wl.n_reuse, qs, kbad, hv, hko, hvo, idx, cnt, None, ws)
+    assert e.value.code == 1                  # CHUNKKV_ERR_INVALID_ARG, nothing launched
+
+
 def test_score_entry_point_alone(ckv):
     wl = configs.llama_layer().with_params(seqlens=(5000, 3000), B=2, name="score_only")
     q, k, v, _ = gen.make_all_layers(wl, DEV)
