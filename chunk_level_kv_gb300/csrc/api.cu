@@ -20,6 +20,10 @@ cudaError_t launch_pack_q(const Plan& pl, const ScoreGeom& g, const void* const*
 cudaError_t launch_score_tc(const Plan& pl, const ScoreGeom& g, const SeqTable& st, const void* const* k_groups,
                             int n_groups, int64_t slot_bytes, float* rl, bin_t* bins, const void* qpack, int32_t* err,
                             cudaStream_t s);
+bool head_path(const Plan& pl, int n_groups, int sms);                                 // select.cu
+cudaError_t launch_head(const Plan& pl, const ScoreGeom& g, const SelectGeom& sg, const SeqTable& st,
+                        const float* rl, const bin_t* bins, float* scores, int32_t* indices, int32_t* counts,
+                        int n_groups, cudaStream_t s);
 
 namespace {
 
@@ -436,6 +440,7 @@ chunkkv_status chunkkv_compress_layers(const chunkkv_params* p, int32_t n_layers
   //  2. the scoring kernel of each reuse group, back to back, each into its own slot;
   //  3. log-sum-exp and finalisation of all groups in one launch each;
   //  4. top-k selection and index build of every (group, sequence, head) in one launch;
+  //     (3 and 4 are one launch, head_kernel, when the call has enough heads to fill the GPU)
   //  5. the gather of every layer (layer l with index group l / n_reuse).
   cudaError_t e = cudaSuccess;
   struct InCompress {                   // phase events are recorded only inside this call
@@ -455,12 +460,22 @@ chunkkv_status chunkkv_compress_layers(const chunkkv_params* p, int32_t n_layers
   if (e == cudaSuccess)
     e = run_score_groups(pl, g, st, qsel.data(), ksel.data(), n_groups, base + pl.off_slots, base + pl.off_qpack, (int32_t*)w, cs);
   if (e == cudaSuccess) e = phase_mark(2, cs);
-  if (e == cudaSuccess) e = run_post_score(pl, g, st, base + pl.off_slots, scores, n_groups, cs);
-  if (e == cudaSuccess) e = phase_mark(4, cs);
-  if (e == cudaSuccess) {
-    SelectGeom sg = select_geom(p, pl);
-    sg.scores_gs = g.scores_gs;
-    e = launch_select(pl, sg, st, scores, indices, counts, n_groups, cs);
+  SelectGeom sg = select_geom(p, pl);
+  sg.scores_gs = g.scores_gs;
+  if (head_path(pl, n_groups, current_sm_count())) {
+    // enough (group, sequence, head) CTAs to fill the GPU: log-sum-exp, finalisation and selection
+    // of a head in one CTA (the lse and select phases are then empty)
+    if (e == cudaSuccess) e = phase_mark(3, cs);
+    if (e == cudaSuccess) {
+      char* slots = base + pl.off_slots;
+      e = launch_head(pl, g, sg, st, (const float*)(slots + pl.off_rl), (const bin_t*)(slots + pl.off_bins), scores,
+                      indices, counts, n_groups, cs);
+    }
+    if (e == cudaSuccess) e = phase_mark(4, cs);
+  } else {
+    if (e == cudaSuccess) e = run_post_score(pl, g, st, base + pl.off_slots, scores, n_groups, cs);
+    if (e == cudaSuccess) e = phase_mark(4, cs);
+    if (e == cudaSuccess) e = launch_select(pl, sg, st, scores, indices, counts, n_groups, cs);
   }
   if (e == cudaSuccess) e = phase_mark(5, cs);
   if (e == cudaSuccess) e = run_gather(p, pl, st, n_layers, n_reuse, k, v, k_out, v_out, indices, counts, cs);

@@ -14,7 +14,7 @@
 // then forms lse_r over every unit of the head, and finalize_kernel
 // the weights 2^(R_r - lse_r) and A_i = sum_r bin[i][r] * weight_r.  This
 // single pass over K needs no second read of the keys and no grid barrier.
-#include "common.cuh"
+#include "fin.cuh"
 
 namespace chunkkv {
 
@@ -158,38 +158,6 @@ cudaError_t launch_score_simt(const Plan& pl, const ScoreGeom& g, const SeqTable
 constexpr int kFinThreads = 256;
 constexpr int kFinChunks = 128;                 // chunks per CTA: blockIdx.y tiles a unit
 
-// weight of one row: 2^(R - lse), zero for a row that saw no key in this unit
-__device__ __forceinline__ float fin_weight(float R, float lse) { return R == -INFINITY ? 0.f : exp2f(R - lse); }
-
-// Weights of rows r .. r+NV-1 (r a multiple of NV, NV in {1, 4, 8}).
-template <bool LSE, int NV>
-__device__ __forceinline__ void fin_weights(float (&wv)[NV], const float* wts, const float* Rrow, const float* Lrow,
-                                            int r) {
-  if constexpr (!LSE) {
-#pragma unroll
-    for (int j = 0; j < NV; j += (NV >= 4 ? 4 : 1)) {
-      if constexpr (NV >= 4) {
-        const float4 x = *reinterpret_cast<const float4*>(wts + r + j);
-        wv[j] = x.x, wv[j + 1] = x.y, wv[j + 2] = x.z, wv[j + 3] = x.w;
-      } else {
-        wv[j] = wts[r + j];
-      }
-    }
-  } else {
-#pragma unroll
-    for (int j = 0; j < NV; j += (NV >= 4 ? 4 : 1)) {
-      if constexpr (NV >= 4) {
-        const float4 R = *reinterpret_cast<const float4*>(Rrow + r + j);
-        const float4 L = *reinterpret_cast<const float4*>(Lrow + r + j);
-        wv[j] = fin_weight(R.x, L.x), wv[j + 1] = fin_weight(R.y, L.y);
-        wv[j + 2] = fin_weight(R.z, L.z), wv[j + 3] = fin_weight(R.w, L.w);
-      } else {
-        wv[j] = fin_weight(Rrow[r + j], Lrow[r + j]);
-      }
-    }
-  }
-}
-
 template <bool LSE>
 __global__ void __launch_bounds__(kFinThreads, 4)
 finalize_kernel(ScoreGeom g, const __grid_constant__ SeqTable st, const float* __restrict__ rl,
@@ -232,64 +200,8 @@ finalize_kernel(ScoreGeom g, const __grid_constant__ SeqTable st, const float* _
   const bin_t* ub = bins + ((int64_t)gu * g.cpu + cb) * g.wG;
   float* out = scores + ((int64_t)b * g.Hkv + h) * g.C_max + (int64_t)u * g.cpu + cb;
   constexpr int kW = kFinThreads / 32;
-  constexpr int kG = 8;
-  for (int ch0 = warp * kG; ch0 < nc; ch0 += kW * kG) {
-    float acc[kG];
-#pragma unroll
-    for (int i = 0; i < kG; ++i) acc[i] = 0.f;
-    const int m = min(kG, nc - ch0);
-    const bin_t* cbase = ub + (int64_t)ch0 * g.wG;
-    if ((g.wG & 7) == 0 && g.wG >= 256) {
-      // eight consecutive rows per lane: 16-byte loads of eight bins, kG of them in flight
-      for (int r = 8 * lane; r < g.wG; r += 256) {
-        uint4 v[kG];
-#pragma unroll
-        for (int i = 0; i < kG; ++i)
-          v[i] = i < m ? __ldcs(reinterpret_cast<const uint4*>(cbase + (int64_t)i * g.wG + r)) : make_uint4(0u, 0u, 0u, 0u);
-        float wv[8];
-        fin_weights<LSE, 8>(wv, wts, Rrow, Lrow, r);
-#pragma unroll
-        for (int i = 0; i < kG; ++i) {
-          const float2 b01 = bin_decode2(v[i].x), b23 = bin_decode2(v[i].y);
-          const float2 b45 = bin_decode2(v[i].z), b67 = bin_decode2(v[i].w);
-          acc[i] = fmaf(b01.x, wv[0], fmaf(b01.y, wv[1], fmaf(b23.x, wv[2], fmaf(b23.y, wv[3], acc[i]))));
-          acc[i] = fmaf(b45.x, wv[4], fmaf(b45.y, wv[5], fmaf(b67.x, wv[6], fmaf(b67.y, wv[7], acc[i]))));
-        }
-      }
-    } else if ((g.wG & 3) == 0) {
-      // four consecutive rows per lane: 8-byte loads of four bins, kG of them in flight
-      for (int r = 4 * lane; r < g.wG; r += 128) {
-        uint2 v[kG];
-#pragma unroll
-        for (int i = 0; i < kG; ++i)
-          v[i] = i < m ? __ldcs(reinterpret_cast<const uint2*>(cbase + (int64_t)i * g.wG + r)) : make_uint2(0u, 0u);
-        float wv[4];
-        fin_weights<LSE, 4>(wv, wts, Rrow, Lrow, r);
-#pragma unroll
-        for (int i = 0; i < kG; ++i) {
-          const float2 b01 = bin_decode2(v[i].x), b23 = bin_decode2(v[i].y);
-          acc[i] = fmaf(b01.x, wv[0], fmaf(b01.y, wv[1], fmaf(b23.x, wv[2], fmaf(b23.y, wv[3], acc[i]))));
-        }
-      }
-    } else {
-      for (int r = lane; r < g.wG; r += 32) {
-        float v[kG];
-#pragma unroll
-        for (int i = 0; i < kG; ++i) v[i] = i < m ? bin_decode(__ldcs(cbase + (int64_t)i * g.wG + r)) : 0.f;
-        float wv[1];
-        fin_weights<LSE, 1>(wv, wts, Rrow, Lrow, r);
-#pragma unroll
-        for (int i = 0; i < kG; ++i) acc[i] = fmaf(v[i], wv[0], acc[i]);
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < kG; ++i) {
-      float a = acc[i];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-      if (lane == 0 && i < m) out[ch0 + i] = a;
-    }
-  }
+  for (int ch0 = warp * kFinGroup; ch0 < nc; ch0 += kW * kFinGroup)
+    fin_group<LSE>(ub + (int64_t)ch0 * g.wG, g.wG, min(kFinGroup, nc - ch0), wts, Rrow, Lrow, out + ch0, lane);
   pdl_trigger();
 }
 
@@ -299,13 +211,6 @@ finalize_kernel(ScoreGeom g, const __grid_constant__ SeqTable st, const float* _
 // 32nd unit, four units per step with their loads issued together, and the
 // partial (M, S) pairs are merged through shared memory.
 constexpr int kLseThreads = 256;
-
-__device__ __forceinline__ void lse_merge(float& M, float& S, float Mv, float Sv) {
-  if (Sv == 0.f) return;
-  const float Mn = fmaxf(M, Mv);
-  S = S * exp2f(M - Mn) + Sv * exp2f(Mv - Mn);
-  M = Mn;
-}
 
 __global__ void __launch_bounds__(kLseThreads)
 lse_kernel(ScoreGeom g, const __grid_constant__ SeqTable st, const float* __restrict__ rl,

@@ -18,7 +18,7 @@
 //     ascending by construction, so no sort is needed.
 #include <cub/block/block_scan.cuh>
 
-#include "common.cuh"
+#include "fin.cuh"
 
 namespace chunkkv {
 
@@ -141,29 +141,23 @@ select_kernel(SelectGeom sg, const __grid_constant__ SeqTable st, const float* _
 constexpr int kSelBins = 2048;
 constexpr int kSelRegThreads = 1024;
 
+// Selection and index build of one (sequence, head) by the whole CTA (kSelRegThreads
+// threads): thread t holds the order keys of chunks t*ITEMS .. t*ITEMS+ITEMS-1.
+// A: the head's C chunk scores; out: its kept indices; count: its kept count.
 template <int ITEMS>
-__global__ void __launch_bounds__(kSelRegThreads)
-select_reg_kernel(SelectGeom sg, const __grid_constant__ SeqTable st, const float* __restrict__ scores,
-                  int32_t* __restrict__ indices, int32_t* __restrict__ counts) {
+__device__ __forceinline__ void select_head(const SelectGeom& sg, int T, const float* A, int32_t* out,
+                                            int32_t* count) {
   using Scan = cub::BlockScan<int, kSelRegThreads>;
   constexpr int BPT = kSelBins / kSelRegThreads;           // histogram bins per thread in the scan
   __shared__ typename Scan::TempStorage scan_tmp;
   __shared__ int hist[kSelBins];
   __shared__ uint32_t sh_prefix;
   __shared__ int sh_remaining, sh_straddle;
-
-  const int bh = blockIdx.x;
-  const int b = bh / sg.Hkv;
   const int tid = threadIdx.x;
-  const int T = st.cu[b + 1] - st.cu[b];
   const int c = sg.c;
   const int C = (T + c - 1) / c;
   const int k = min(sg.L_max / c, C);
-  const float* A = scores + blockIdx.y * sg.scores_gs + (int64_t)bh * sg.C_max;
-  int32_t* out = indices + blockIdx.y * sg.idx_gs + (int64_t)bh * sg.n_cap;
-  counts += blockIdx.y * sg.cnt_gs;
   const int i0 = tid * ITEMS;
-  pdl_wait();
 
   uint32_t key[ITEMS];
 #pragma unroll
@@ -262,7 +256,104 @@ select_reg_kernel(SelectGeom sg, const __grid_constant__ SeqTable st, const floa
   for (int t = tid; t < strad; t += blockDim.x) out[tail0 + t] = sc * c + t;
   const int rec0 = tail0 + strad;
   for (int t = tid; t < T - Rs; t += blockDim.x) out[rec0 + t] = Rs + t;
-  if (tid == 0) counts[bh] = rec0 + (T - Rs);
+  if (tid == 0) *count = rec0 + (T - Rs);
+}
+
+template <int ITEMS>
+__global__ void __launch_bounds__(kSelRegThreads)
+select_reg_kernel(SelectGeom sg, const __grid_constant__ SeqTable st, const float* __restrict__ scores,
+                  int32_t* __restrict__ indices, int32_t* __restrict__ counts) {
+  const int bh = blockIdx.x;
+  const int b = bh / sg.Hkv;
+  const int T = st.cu[b + 1] - st.cu[b];
+  const float* A = scores + blockIdx.y * sg.scores_gs + (int64_t)bh * sg.C_max;
+  int32_t* out = indices + blockIdx.y * sg.idx_gs + (int64_t)bh * sg.n_cap;
+  counts += blockIdx.y * sg.cnt_gs;
+  pdl_wait();
+  select_head<ITEMS>(sg, T, A, out, counts + bh);
+  pdl_trigger();
+}
+
+// Log-sum-exp, finalisation and selection of one (sequence, head, reuse group)
+// in one CTA, for calls with enough heads to fill the GPU with such CTAs: the
+// row log-sum-exps go to shared memory, the chunk scores to the score array
+// (read back from L2 by the selection in the same CTA), and no other launch sits
+// between the scoring kernel and the gather.  Shared memory: lse[wG], then the
+// partial (M, S) pairs of the P = kSelRegThreads / wG thread groups that split
+// the units of every row when wG < kSelRegThreads.
+template <int ITEMS>
+__global__ void __launch_bounds__(kSelRegThreads)
+head_kernel(ScoreGeom g, SelectGeom sg, const __grid_constant__ SeqTable st, const float* __restrict__ rl,
+            const bin_t* __restrict__ bins, float* __restrict__ scores, int32_t* __restrict__ indices,
+            int32_t* __restrict__ counts) {
+  extern __shared__ float hsh[];
+  const int bh = blockIdx.x;
+  const int b = bh / g.Hkv, h = bh - b * g.Hkv;
+  rl += blockIdx.y * g.rl_gs;
+  bins += blockIdx.y * g.bins_gs;
+  float* A = scores + blockIdx.y * g.scores_gs + (int64_t)bh * g.C_max;
+  int32_t* out = indices + blockIdx.y * sg.idx_gs + (int64_t)bh * sg.n_cap;
+  counts += blockIdx.y * sg.cnt_gs;
+  const int T = st.cu[b + 1] - st.cu[b];
+  const int C = (T + g.c - 1) / g.c;
+  const int U = st.uoff[b + 1] - st.uoff[b];
+  pdl_wait();
+
+  // 1. base-2 log-sum-exp of every window row of the head over its U units
+  float* lse_s = hsh;
+  float* part = hsh + g.wG;
+  const int P = g.wG < kSelRegThreads ? kSelRegThreads / g.wG : 1;
+  const int64_t ustride = (int64_t)g.Hkv * 2 * g.wG;            // between units of one head
+  const float* rl_head = rl + ((int64_t)st.uoff[b] * g.Hkv + h) * 2 * g.wG;
+  for (int t = threadIdx.x; t < g.wG * P; t += kSelRegThreads) {
+    const int r = t % g.wG, p = t / g.wG;
+    const float* base = rl_head + r;
+    float M = -INFINITY, S = 0.f;
+    int v = p;
+    for (; v + 3 * P < U; v += 4 * P) {
+      float Rv[4], lv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        Rv[i] = base[(v + i * P) * ustride];
+        lv[i] = base[(v + i * P) * ustride + g.wG];
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) lse_merge(M, S, Rv[i], lv[i]);
+    }
+    for (; v < U; v += P) lse_merge(M, S, base[v * ustride], base[v * ustride + g.wG]);
+    if (P == 1) {
+      lse_s[r] = M + log2f(S);
+    } else {
+      part[2 * t] = M;
+      part[2 * t + 1] = S;
+    }
+  }
+  if (P > 1) {
+    __syncthreads();
+    for (int r = threadIdx.x; r < g.wG; r += kSelRegThreads) {
+      float M = -INFINITY, S = 0.f;
+      for (int p = 0; p < P; ++p) lse_merge(M, S, part[2 * (p * g.wG + r)], part[2 * (p * g.wG + r) + 1]);
+      lse_s[r] = M + log2f(S);
+    }
+  }
+  __syncthreads();
+
+  // 2. chunk scores of every unit, kFinGroup chunks per warp step
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int spu = (g.cpu + kFinGroup - 1) / kFinGroup;            // warp steps per unit
+  for (int it = warp; it < U * spu; it += kSelRegThreads / 32) {
+    const int u = it / spu;
+    const int ch0 = (it - u * spu) * kFinGroup;
+    const int m = min(kFinGroup, min(g.cpu, C - u * g.cpu) - ch0);
+    if (m <= 0) continue;                                          // past the end of the last unit
+    const int gu = (st.uoff[b] + u) * g.Hkv + h;
+    fin_group<true>(bins + ((int64_t)gu * g.cpu + ch0) * g.wG, g.wG, m, nullptr, rl + (int64_t)gu * 2 * g.wG,
+                    lse_s, A + (int64_t)u * g.cpu + ch0, lane);
+  }
+  __syncthreads();                                                // the scores are visible to the whole CTA
+
+  // 3. selection and index build
+  select_head<ITEMS>(sg, T, A, out, counts + bh);
   pdl_trigger();
 }
 
@@ -276,6 +367,30 @@ cudaError_t launch_select(const Plan& pl, const SelectGeom& sg, const SeqTable& 
   if (pl.C_max <= kSelRegThreads * 16)
     return launch_pdl(select_reg_kernel<16>, grid, dim3(kSelRegThreads), 0, s, sg, st, scores, indices, counts);
   return launch_pdl(select_kernel, grid, dim3(kSelThreads), 0, s, sg, st, scores, indices, counts);
+}
+
+// Whether head_kernel can take the log-sum-exp, finalisation and selection of a
+// call: window rows and a register-resident selection fit one 1024-thread CTA,
+// and the call's (group, sequence, head) CTAs fill at least three quarters of
+// the GPU's SMs over the waves they need (one CTA per SM).
+bool head_path(const Plan& pl, int n_groups, int sms) {
+  if (pl.wG <= 0 || pl.C_max > kSelRegThreads * 16 || sms <= 0) return false;
+  const int64_t heads = (int64_t)pl.B * pl.Hkv * n_groups;
+  const int64_t waves = (heads + sms - 1) / sms;
+  return heads > 0 && 4 * heads >= 3 * waves * sms;
+}
+
+cudaError_t launch_head(const Plan& pl, const ScoreGeom& g, const SelectGeom& sg, const SeqTable& st,
+                        const float* rl, const bin_t* bins, float* scores, int32_t* indices, int32_t* counts,
+                        int n_groups, cudaStream_t s) {
+  const int P = pl.wG < kSelRegThreads ? kSelRegThreads / pl.wG : 1;
+  const size_t smem = (size_t)pl.wG * (P > 1 ? 1 + 2 * P : 1) * sizeof(float);   // at most 16 KB (wG <= 4096)
+  const dim3 grid(pl.B * pl.Hkv, n_groups);
+  if (pl.C_max <= kSelRegThreads * 4)
+    return launch_pdl(head_kernel<4>, grid, dim3(kSelRegThreads), smem, s, g, sg, st, rl, bins, scores, indices,
+                      counts);
+  return launch_pdl(head_kernel<16>, grid, dim3(kSelRegThreads), smem, s, g, sg, st, rl, bins, scores, indices,
+                    counts);
 }
 
 }  // namespace chunkkv

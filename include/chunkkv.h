@@ -259,8 +259,12 @@ uint64_t chunkkv_launch_count(void);
  * records events[i] on its stream at phase boundary i: 0 before the window-row
  * packing, 1 before scoring, 2 before the log-sum-exp, 3 before the
  * finalisation, 4 before the top-k selection, 5 before the gather, 6 after the
- * gather.  A record between two launches ends the programmatic-dependent-launch
- * overlap there, so recorded calls run a little slower than unrecorded ones.
+ * gather.  When one kernel takes the log-sum-exp, the finalisation and the
+ * selection (calls with enough (group, sequence, head) triples to fill the
+ * GPU), boundaries 2 and 3 come before it and 4 after it, so its time shows as
+ * the finalisation's.  A record between two launches ends the
+ * programmatic-dependent-launch overlap there, so recorded calls run a little
+ * slower than unrecorded ones.
  * Returns CHUNKKV_ERR_INVALID_ARG if n_events is neither 0 nor
  * CHUNKKV_PHASE_EVENTS or a handle is NULL (the previous setting then stays).
  */
