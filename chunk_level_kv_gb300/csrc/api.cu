@@ -17,9 +17,10 @@ cudaError_t launch_overlap(const SeqTable& st, int Hkv, int n_cap, int n_lists, 
                            const int32_t* counts, int32_t* inter, int32_t* uni, cudaStream_t s);   // overlap.cu
 cudaError_t launch_pack_q(const Plan& pl, const ScoreGeom& g, const void* const* q_layers, int n_layers,
                           void* qpack, cudaStream_t s);
-cudaError_t launch_score_tc(const Plan& pl, const ScoreGeom& g, const SeqTable& st, const void* const* k_groups,
-                            int n_groups, int64_t slot_bytes, float* rl, bin_t* bins, const void* qpack, int32_t* err,
-                            cudaStream_t s);
+cudaError_t launch_score_tc(const Plan& pl, const ScoreGeom& g, const SeqTable& st, const void* const* q_groups,
+                            const void* const* k_groups, int n_groups, int64_t slot_bytes, float* rl, bin_t* bins,
+                            const void* qpack, int32_t* err, cudaStream_t s);
+bool tc_q_direct(const Plan& pl, const ScoreGeom& g, const void* q);                   // score_tc.cu
 bool head_path(const Plan& pl, int n_groups, int sms);                                 // select.cu
 cudaError_t launch_head(const Plan& pl, const ScoreGeom& g, const SelectGeom& sg, const SeqTable& st,
                         const float* rl, const bin_t* bins, float* scores, int32_t* indices, int32_t* counts,
@@ -207,15 +208,16 @@ ScoreGeom score_geom(const chunkkv_params* p, const Plan& pl) {
 chunkkv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? CHUNKKV_OK : CHUNKKV_ERR_CUDA; }
 
 // Scoring of n_groups reuse groups into consecutive scratch slots from `slots`.
-// q and k hold each group's scoring layer; on the tensor-core path the window
-// rows are already packed from qpack and one persistent launch covers all groups.
+// q and k hold each group's scoring layer; on the tensor-core path one
+// persistent launch covers all groups, reading the window rows from q itself
+// (qpack null) or from their packed copy in qpack.
 cudaError_t run_score_groups(const Plan& pl, const ScoreGeom& g, const SeqTable& st, const void* const* q,
                              const void* const* k, int n_groups, char* slots, const void* qpack, int32_t* err,
                              cudaStream_t s) {
   float* rl = (float*)(slots + pl.off_rl);
   bin_t* bins = (bin_t*)(slots + pl.off_bins);
   const int64_t slot_gs = (int64_t)(pl.slot_bytes / sizeof(float));
-  if (pl.use_tc) return launch_score_tc(pl, g, st, k, n_groups, (int64_t)pl.slot_bytes, rl, bins, qpack, err, s);
+  if (pl.use_tc) return launch_score_tc(pl, g, st, q, k, n_groups, (int64_t)pl.slot_bytes, rl, bins, qpack, err, s);
   for (int i = 0; i < n_groups; ++i) {
     cudaError_t e = launch_score_simt(pl, g, st, q[i], k[i], rl + i * slot_gs,
                                       (bin_t*)((char*)bins + i * pl.slot_bytes), s);
@@ -362,11 +364,14 @@ chunkkv_status chunkkv_score(const chunkkv_params* p, const void* q_win, const v
   char* qpack = base + pl.off_qpack;
   ScoreGeom g = score_geom(p, pl);
   cudaError_t e = cudaSuccess;
-  if (pl.use_tc && pl.wG > 0) {
+  // window rows straight from q_win when a tensor map can address them (w divides 128), else packed first
+  const bool direct = tc_q_direct(pl, g, q_win);
+  if (pl.use_tc && pl.wG > 0 && !direct) {
     const void* ql[1] = {q_win};
     e = launch_pack_q(pl, g, ql, 1, qpack, cs);
   }
-  if (e == cudaSuccess) e = run_score_groups(pl, g, st, &q_win, &k, 1, slot, qpack, (int32_t*)w, cs);
+  if (e == cudaSuccess)
+    e = run_score_groups(pl, g, st, &q_win, &k, 1, slot, direct ? nullptr : qpack, (int32_t*)w, cs);
   if (e == cudaSuccess) e = run_post_score(pl, g, st, slot, chunk_scores, 1, cs);
   return cuda_status(e);
 }
@@ -436,7 +441,8 @@ chunkkv_status chunkkv_compress_layers(const chunkkv_params* p, int32_t n_layers
   float* scores = chunk_scores ? chunk_scores : (float*)(base + pl.off_scores);
   if (chunk_scores) g.scores_gs = (int64_t)pl.B * pl.Hkv * pl.C_max;
   // One stream, every launch chained by programmatic dependent launch:
-  //  1. the window rows of every scoring layer packed in one launch (tensor-core path);
+  //  1. the window rows of every scoring layer packed in one launch (tensor-core path, only
+  //     when the scoring kernel cannot read them from q_win itself);
   //  2. the scoring kernel of each reuse group, back to back, each into its own slot;
   //  3. log-sum-exp and finalisation of all groups in one launch each;
   //  4. top-k selection and index build of every (group, sequence, head) in one launch;
@@ -454,11 +460,15 @@ chunkkv_status chunkkv_compress_layers(const chunkkv_params* p, int32_t n_layers
     qsel[i] = q_win[i * n_reuse];
     ksel[i] = k[i * n_reuse];
   }
+  // window rows straight from q_win when a tensor map can address them (w divides 128), else packed
+  // first (every layer has the same strides and was checked for 16-byte alignment: the first decides)
+  const bool direct = tc_q_direct(pl, g, qsel[0]);
+  const void* qpack = direct ? nullptr : base + pl.off_qpack;
   e = phase_mark(0, cs);
-  if (e == cudaSuccess && pl.use_tc && pl.wG > 0) e = launch_pack_q(pl, g, qsel.data(), n_groups, base + pl.off_qpack, cs);
+  if (e == cudaSuccess && pl.use_tc && pl.wG > 0 && !direct) e = launch_pack_q(pl, g, qsel.data(), n_groups, base + pl.off_qpack, cs);
   if (e == cudaSuccess) e = phase_mark(1, cs);
   if (e == cudaSuccess)
-    e = run_score_groups(pl, g, st, qsel.data(), ksel.data(), n_groups, base + pl.off_slots, base + pl.off_qpack, (int32_t*)w, cs);
+    e = run_score_groups(pl, g, st, qsel.data(), ksel.data(), n_groups, base + pl.off_slots, qpack, (int32_t*)w, cs);
   if (e == cudaSuccess) e = phase_mark(2, cs);
   SelectGeom sg = select_geom(p, pl);
   sg.scores_gs = g.scores_gs;

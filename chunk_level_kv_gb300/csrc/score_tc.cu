@@ -68,6 +68,9 @@ constexpr int kMaxGroups = 32;
 struct TcGeom {
   int32_t B, Hkv, wG, MT, cpu, ku;
   int32_t w;                         // window length (for the causal-window limit)
+  int32_t G;                         // query heads per KV head
+  int32_t q_direct;                  // 1: window rows read from Q_w itself (maps.q[group]), 0: packed (maps.q[0])
+  int32_t qm;                        // query heads per 128-row M tile when q_direct (128 / w)
   int32_t items_pg;                  // work items per group: units x M tiles
   int32_t n_items;                   // items_pg x groups of this launch
   int64_t slot_bytes;                // bytes between the scratch slots of consecutive groups
@@ -75,8 +78,14 @@ struct TcGeom {
   long long timeout;                 // clock64 cycles per wait
 };
 
+// Window rows: either one 4-D map per group over that layer's Q_w itself, (d, w,
+// Hq, B) with a (64, w, 128 / w, 1) box, whose 128 rows are query heads
+// h*G + mt*128/w .. of the M tile with their w window rows each (the packed row
+// order; rows past the head's w*G are other heads' or zero-filled and never
+// written out), or every group's rows packed by pack_q_kernel in one 2-D map
+// (q[0], [rows, 128], row tile `key`) when w does not divide 128.
 struct TcMaps {
-  CUtensorMap q;                     // packed window rows of every group of the launch, [rows, 128]
+  CUtensorMap q[kMaxGroups];
   CUtensorMap k[kMaxGroups];         // keys of each group's layer, [T_total, Hkv, 128]
 };
 
@@ -131,6 +140,13 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
       ::"r"(dst), "l"((uint64_t)map), "r"(bar), "r"(c0), "r"(c1) : "memory");
+}
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
+                                            int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6}], "
+      "[%2];"
+      ::"r"(dst), "l"((uint64_t)map), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3) : "memory");
 }
 // A 3-D tile load with an L2 eviction-priority policy (createpolicy) attached.
 __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
@@ -329,6 +345,21 @@ __device__ __forceinline__ float tile_max(uint32_t taddr, int valid) {
   return m;
 }
 
+// The 128 window rows of an item's M tile into shared memory (two 64-element
+// panels, 128-byte swizzle), completing on bar.
+__device__ __forceinline__ void load_q(const TcMaps& maps, const TcGeom& g, const Item& it, uint32_t sq, uint32_t bar) {
+  mbar_expect_tx(bar, kQBytes);
+  if (g.q_direct) {
+    const CUtensorMap* qm = &maps.q[it.grp];
+    const int hq0 = it.h * g.G + it.mt * g.qm;
+    tma_load_4d(sq, qm, bar, 0, 0, hq0, it.b);
+    tma_load_4d(sq + kPanelQ, qm, bar, 64, 0, hq0, it.b);
+  } else {
+    tma_load_2d(sq, &maps.q[0], bar, 0, it.key * 128);
+    tma_load_2d(sq + kPanelQ, &maps.q[0], bar, 64, it.key * 128);
+  }
+}
+
 // ---------------------------------------------------------------- the kernel
 template <int C, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 2)
@@ -361,7 +392,7 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
     mbar_init(smem_u32(&qt_done[0]), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&maps.q) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&maps.q[0]) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&maps.k[0]) : "memory");
   }
   if (warp == 1) {
@@ -395,10 +426,7 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
         for (int t = 0; t < it.ntile && ok; ++t) {
           if (t == pre && it.key != qkey) {
             if (!wait_bar(ctl, smem_u32(&q_empty[0]), (qc & 1) ^ 1, kDevTimeoutTmaProducer)) { ok = false; break; }
-            const uint32_t qbar = smem_u32(&q_full[0]);
-            mbar_expect_tx(qbar, kQBytes);
-            tma_load_2d(smem_u32(sQ), &maps.q, qbar, 0, it.key * 128);
-            tma_load_2d(smem_u32(sQ + kPanelQ), &maps.q, qbar, 64, it.key * 128);
+            load_q(maps, g, it, smem_u32(sQ), smem_u32(&q_full[0]));
             ++qc;
             qkey = it.key;
           }
@@ -416,10 +444,7 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
         }
         if (ok && it.key != qkey) {          // an item shorter than the prefetch: its Q comes last
           if (!wait_bar(ctl, smem_u32(&q_empty[0]), (qc & 1) ^ 1, kDevTimeoutTmaProducer)) break;
-          const uint32_t qbar = smem_u32(&q_full[0]);
-          mbar_expect_tx(qbar, kQBytes);
-          tma_load_2d(smem_u32(sQ), &maps.q, qbar, 0, it.key * 128);
-          tma_load_2d(smem_u32(sQ + kPanelQ), &maps.q, qbar, 64, it.key * 128);
+          load_q(maps, g, it, smem_u32(sQ), smem_u32(&q_full[0]));
           ++qc;
           qkey = it.key;
         }
@@ -740,13 +765,42 @@ cudaError_t launch_pack_q(const Plan& pl, const ScoreGeom& g, const void* const*
   return cudaSuccess;
 }
 
-// Scores n_groups layers (one per reuse group) in one persistent launch.  Their
-// window rows are packed back to back from qpack (launch_pack_q); group i reads
-// keys k_groups[i] and writes the scratch slot at rl + i * slot_gs and
-// bins + i * slot_gs (slot_gs in floats).
-cudaError_t launch_score_tc(const Plan& pl, const ScoreGeom& g, const SeqTable& st, const void* const* k_groups,
-                            int n_groups, int64_t slot_bytes, float* rl, bin_t* bins, const void* qpack, int32_t* err,
-                            cudaStream_t s) {
+namespace tc {
+// 4-D map over one layer's window queries Q_w [B, w, Hq, d] (see TcMaps).  The
+// stride of an axis of extent 1 is never used and is then set to 16 bytes.
+bool encode_q_direct(EncodeFn enc, CUtensorMap* map, const void* q, const Plan& pl, const ScoreGeom& g) {
+  if (pl.w < 1 || 128 % pl.w != 0) return false;
+  const int64_t ext[3] = {pl.w, (int64_t)pl.Hkv * pl.G, pl.B};
+  const int64_t st[3] = {g.q_stride_w, g.q_stride_h, g.q_stride_b};
+  cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)ext[0], (cuuint64_t)ext[1], (cuuint64_t)ext[2]};
+  cuuint64_t strides[3];
+  for (int i = 0; i < 3; ++i) strides[i] = (cuuint64_t)(st[i] == 0 && ext[i] == 1 ? 16 : st[i] * 2);
+  cuuint32_t box[4] = {64, (cuuint32_t)pl.w, (cuuint32_t)(128 / pl.w), 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(q), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+}  // namespace tc
+
+// Whether the scoring kernel can read the window rows from q itself (w divides
+// 128 and the map encodes), so that no packing launch is needed.
+bool tc_q_direct(const Plan& pl, const ScoreGeom& g, const void* q) {
+  tc::EncodeFn enc = tc::encode_fn();
+  CUtensorMap map;
+  return pl.use_tc && pl.wG > 0 && pl.B > 0 && enc != nullptr && q != nullptr &&
+         tc::encode_q_direct(enc, &map, q, pl, g);
+}
+
+// Scores n_groups layers (one per reuse group) in one persistent launch; group
+// i reads keys k_groups[i] and writes the scratch slot at rl + i * slot_gs and
+// bins + i * slot_gs (slot_gs in floats).  Window rows come from q_groups[i]
+// itself when qpack is null (tc_q_direct said yes), otherwise packed back to
+// back from qpack (launch_pack_q).
+cudaError_t launch_score_tc(const Plan& pl, const ScoreGeom& g, const SeqTable& st, const void* const* q_groups,
+                            const void* const* k_groups, int n_groups, int64_t slot_bytes, float* rl, bin_t* bins,
+                            const void* qpack, int32_t* err, cudaStream_t s) {
+  const bool direct = qpack == nullptr;
   tc::EncodeFn enc = tc::encode_fn();
   if (enc == nullptr) return cudaErrorNotSupported;
   const int MT = pl.tc_mt;
@@ -756,13 +810,16 @@ cudaError_t launch_score_tc(const Plan& pl, const ScoreGeom& g, const SeqTable& 
   for (int g0 = 0; g0 < n_groups; g0 += tc::kMaxGroups) {
     const int n = std::min(tc::kMaxGroups, n_groups - g0);
     static thread_local tc::TcMaps maps;
-    {
+    if (direct) {
+      for (int i = 0; i < n; ++i)
+        if (!tc::encode_q_direct(enc, &maps.q[i], q_groups[g0 + i], pl, g)) return cudaErrorInvalidValue;
+    } else {
       cuuint64_t dims[2] = {(cuuint64_t)tc::kD, (cuuint64_t)(rows_pg * n)};
       cuuint64_t strides[1] = {(cuuint64_t)tc::kD * 2};
       cuuint32_t box[2] = {64, 128};
       cuuint32_t es[2] = {1, 1};
       const void* qg = (const char*)qpack + g0 * rows_pg * tc::kD * 2;
-      if (enc(&maps.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(qg), dims, strides, box, es,
+      if (enc(&maps.q[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(qg), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
@@ -785,6 +842,9 @@ cudaError_t launch_score_tc(const Plan& pl, const ScoreGeom& g, const SeqTable& 
     tg.cpu = pl.cpu;
     tg.ku = pl.ku;
     tg.w = g.w;
+    tg.G = pl.G;
+    tg.q_direct = direct ? 1 : 0;
+    tg.qm = direct ? 128 / pl.w : 0;
     tg.items_pg = g.n_units * MT;
     tg.n_items = tg.items_pg * n;
     tg.slot_bytes = slot_bytes;

@@ -257,7 +257,8 @@ uint64_t chunkkv_launch_count(void);
  *           switches recording off.
  * While set, each chunkkv_compress_layers call made by the same host thread
  * records events[i] on its stream at phase boundary i: 0 before the window-row
- * packing, 1 before scoring, 2 before the log-sum-exp, 3 before the
+ * packing (a phase without a launch when the scoring kernel reads the window
+ * rows from q_win itself: w divides 128), 1 before scoring, 2 before the log-sum-exp, 3 before the
  * finalisation, 4 before the top-k selection, 5 before the gather, 6 after the
  * gather.  When one kernel takes the log-sum-exp, the finalisation and the
  * selection (calls with enough (group, sequence, head) triples to fill the

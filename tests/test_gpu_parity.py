@@ -144,13 +144,14 @@ def test_layer_reuse_groups(ckv, Hq, Hkv, w):
     assert out.indices.shape[0] == 3
 
 
-@pytest.mark.parametrize("B,launches", [(1, 6), (12, 4)])
-def test_one_launch_per_phase(ckv, B, launches):
-    # pack, score (all reuse groups), log-sum-exp, finalize, select, gather (all layers); with 12
-    # sequences x 8 KV heads x 3 reuse groups = 288 heads (two waves of one CTA per SM, 95 % full)
-    # one kernel takes log-sum-exp, finalisation and selection of a head
-    wl = configs.llama_model().with_params(seqlens=(3000,) * B, B=B, n_layers=6, n_reuse=2, L_max=600,
-                                           name=f"phases_B{B}")
+@pytest.mark.parametrize("B,w,Hq,launches", [(1, 32, 32, 5), (1, 48, 40, 6), (12, 32, 32, 3)])
+def test_one_launch_per_phase(ckv, B, w, Hq, launches):
+    # score (all reuse groups), log-sum-exp, finalize, select, gather (all layers).  A packing launch
+    # comes first only when the scoring kernel cannot read the window rows from Q_w through a tensor
+    # map (w does not divide 128).  With 12 sequences x 8 KV heads x 3 reuse groups = 288 heads (two
+    # waves of one CTA per SM, 95 % full) one kernel takes log-sum-exp, finalisation and selection.
+    wl = configs.llama_model().with_params(seqlens=(3000,) * B, B=B, n_layers=6, n_reuse=2, L_max=600, w=w,
+                                           Hq=Hq, name=f"phases_B{B}_w{w}")
     qs, ks, vs, _ = gen.make_all_layers(wl, DEV)
     ckv.compress_layers(qs, ks, vs, wl.cu_seqlens, Hq=wl.Hq, Hkv=wl.Hkv, w=wl.w, c=wl.c, L_max=wl.L_max,
                         n_reuse=wl.n_reuse)
