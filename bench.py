@@ -149,6 +149,17 @@ def traffic_record(workload: str, kernel: str):
         return None
 
 
+def head_path(wl, groups) -> bool:
+    """Whether the library runs log-sum-exp, finalisation and selection as one kernel per head: the
+    same rule as the library's planner (window rows present, at most 16384 chunks per sequence, and
+    the (group, sequence, head) CTAs, one per SM, filling at least three quarters of their waves)."""
+    c_max = max(-(-(wl.cu_seqlens[b + 1] - wl.cu_seqlens[b]) // wl.c) for b in range(wl.B)) if wl.B else 0
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    heads = wl.B * wl.Hkv * groups
+    waves = -(-heads // sms)
+    return wl.w * wl.G > 0 and c_max <= 16384 and heads > 0 and 4 * heads >= 3 * waves * sms
+
+
 def phase_rooflines(wl, counts, phase_ms, peaks, peak_src, path):
     """Roofline of the scoring, finalisation and gather launches of one compress step.
 
@@ -156,7 +167,8 @@ def phase_rooflines(wl, counts, phase_ms, peaks, peak_src, path):
       score:    K of every scoring layer read once (T_total*Hkv*d*elt per group) and
                 2*w*G*T_total*Hkv*d flops; the roof is whichever takes longer at peak
                 (HBM copy bandwidth, or the sustained bf16 tensor rate);
-      finalize: one 16-bit bin per (chunk, window row, KV head) per group read once;
+      finalize: one 16-bit bin per (chunk, window row, KV head) per group read once (the phase is
+                one kernel with the log-sum-exp and the selection when head_path() holds);
       gather:   kept K and V rows read and written (4*kept*d*elt per layer).
     """
     elt = 2 if wl.dtype == "bf16" else 4
@@ -189,7 +201,8 @@ def phase_rooflines(wl, counts, phase_ms, peaks, peak_src, path):
                     "peak_source": f"{peak_src} bf16_tflops_sustained"})
     else:
         out.append(hbm_roof("score", kernel, score_bytes))
-    out.append(hbm_roof("finalize", "finalize_kernel", groups * chunks * wl.Hkv * wl.w * wl.G * 2))
+    fin_kernel = "head_kernel" if head_path(wl, groups) else "finalize_kernel"
+    out.append(hbm_roof("finalize", fin_kernel, groups * chunks * wl.Hkv * wl.w * wl.G * 2))
     out.append(hbm_roof("gather", "gather_kernel", 4 * kept_all * wl.d * elt))
     return out
 
