@@ -163,6 +163,19 @@ def test_one_launch_per_phase(ckv, B, w, Hq, launches):
     assert ckv.chunkkv_status_check(out.workspace) == 0
 
 
+def test_head_kernel_on_a_ragged_batch(ckv):
+    # 12 ragged sequences (one empty, two shorter than the window, several units long) x 8 KV heads x
+    # 3 reuse groups = 288 heads: log-sum-exp, finalisation and selection run as one kernel per head
+    # (three launches per call); checked against the oracle like every other path
+    seqlens = (3000, 1234, 2999, 77, 5, 4096, 0, 800, 3000, 2048, 1500, 999)
+    wl = configs.mistral_ragged().with_params(seqlens=seqlens, B=len(seqlens), n_layers=6, n_reuse=2, L_max=600,
+                                              needles=NeedleSpec(kind="none"), name="head_ragged12")
+    n0 = ckv.chunkkv_launch_count()
+    out, _ = run_and_check(ckv, wl, seqs=[0, 3, 4, 5, 6, 11])
+    assert ckv.chunkkv_launch_count() - n0 == 3                    # score, head_kernel, gather
+    assert not out.counts[:, 6].any()                              # the empty sequence keeps nothing
+
+
 def test_phase_events_mark_every_phase(ckv):
     wl = configs.llama_model().with_params(seqlens=(3000,), n_layers=4, n_reuse=2, L_max=600, name="phase_events")
     qs, ks, vs, _ = gen.make_all_layers(wl, DEV)
