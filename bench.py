@@ -152,12 +152,11 @@ def traffic_record(workload: str, kernel: str):
 def head_path(wl, groups) -> bool:
     """Whether the library runs log-sum-exp, finalisation and selection as one kernel per head: the
     same rule as the library's planner (window rows present, at most 16384 chunks per sequence, and
-    the (group, sequence, head) CTAs, one per SM, filling at least three quarters of their waves)."""
+    the (group, sequence, head) CTAs, one per SM, making one wave over at least 3/4 of the SMs)."""
     c_max = max(-(-(wl.cu_seqlens[b + 1] - wl.cu_seqlens[b]) // wl.c) for b in range(wl.B)) if wl.B else 0
     sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     heads = wl.B * wl.Hkv * groups
-    waves = -(-heads // sms)
-    return wl.w * wl.G > 0 and c_max <= 16384 and heads > 0 and 4 * heads >= 3 * waves * sms
+    return wl.w * wl.G > 0 and c_max <= 16384 and heads <= sms and 4 * heads >= 3 * sms
 
 
 def phase_rooflines(wl, counts, phase_ms, peaks, peak_src, path):
@@ -207,6 +206,20 @@ def phase_rooflines(wl, counts, phase_ms, peaks, peak_src, path):
     return out
 
 
+def workload_of(args):
+    """The workload named on the command line, with the sweep point (--chunk, --budget) and the
+    layer count (--layers) applied."""
+    wl = configs.ALL[args.workload]()
+    c = getattr(args, "chunk", 0) or wl.c
+    L = getattr(args, "budget", 0) or wl.L_max
+    if (c, L) != (wl.c, wl.L_max):
+        base = wl.name.split("_c")[0] if wl.name.startswith("mistral") else wl.name
+        wl = wl.with_params(c=c, L_max=L, name=f"{base}_c{c}_L{L}")
+    if args.layers:
+        wl = wl.with_params(n_layers=args.layers, name=f"{wl.name}_first{args.layers}L")
+    return wl
+
+
 def run_gpu(args):
     import chunk_level_kv_gb300 as ckv
     ws_n, rank, local = dist_env()
@@ -215,9 +228,7 @@ def run_gpu(args):
     if ws_n > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
-    wl = configs.ALL[args.workload]()
-    if args.layers:
-        wl = wl.with_params(n_layers=args.layers, name=f"{wl.name}_first{args.layers}L")
+    wl = workload_of(args)
     qs, ks, vs, _ = gen.make_all_layers(wl, dev)
     p, keep = ckv.params_for(next(q for q in qs if q is not None), ks[0], wl.cu_seqlens, Hkv=wl.Hkv, w=wl.w,
                              c=wl.c, L_max=wl.L_max)
@@ -476,7 +487,7 @@ def run_reference(args):
     ws_n, rank, local = dist_env()
     if rank != 0:
         return
-    wl = configs.ALL[args.workload]()
+    wl = workload_of(args)
     qs, ks = [], []
     q, k, v = gen.make_layer(wl, 0, "cpu")
     qs.append(q)
@@ -515,6 +526,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-diagnostics", action="store_true", help="skip the adjacent-layer overlap measurement")
     ap.add_argument("--layers", type=int, default=0, help="keep only the first N layers (profiling)")
+    ap.add_argument("--chunk", type=int, default=0, help="chunk size c instead of the workload's (a sweep point)")
+    ap.add_argument("--budget", type=int, default=0, help="L_max instead of the workload's (a sweep point)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -30,6 +30,7 @@ namespace {
 
 constexpr size_t kAlign = 256;
 constexpr size_t kHeaderBytes = 256;            // int32 device error word at offset 0
+constexpr int kItemTiles = 2;                   // fixed cost of a scoring work item, in key tiles
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
@@ -118,8 +119,10 @@ chunkkv_status make_plan(const chunkkv_params* p, int n_layers, int n_reuse, Pla
   tc_plan(pl);                                    // may switch to the tensor-core geometry
   if (pl.use_tc) {
     // Unit length for the persistent tensor-core grid: the multiple m of the
-    // base unit that minimises (waves of work items) x (tiles per item) with
-    // two CTAs per SM (304 slots on a GB300); ties go to longer units.
+    // base unit that minimises (waves of work items) x (tiles per item + the
+    // fixed cost of an item, kItemTiles tiles: reference maximum, window-row
+    // reload, pipeline refill) with two CTAs per SM (304 slots on a GB300); ties
+    // go to longer units.
     const int slots = 2 * current_sm_count();
     const int64_t per_unit_items = (int64_t)p->Hkv * pl.tc_mt;
     const int base_tiles = pl.tc_base_chunks * p->c / pl.tc_tile_n;
@@ -133,7 +136,7 @@ chunkkv_status make_plan(const chunkkv_params* p, int n_layers, int n_reuse, Pla
         items += (C + cpu - 1) / cpu * per_unit_items;
       }
       if (items == 0) break;
-      const int64_t cost = (items + slots - 1) / slots * (int64_t)m * base_tiles;
+      const int64_t cost = (items + slots - 1) / slots * ((int64_t)m * base_tiles + kItemTiles);
       if (cost <= best_cost) {
         best_cost = cost;
         pl.cpu = cpu;

@@ -141,14 +141,15 @@ select_kernel(SelectGeom sg, const __grid_constant__ SeqTable st, const float* _
 constexpr int kSelBins = 2048;
 constexpr int kSelRegThreads = 1024;
 
-// Selection and index build of one (sequence, head) by the whole CTA (kSelRegThreads
+// Selection and index build of one (sequence, head) by the whole CTA (THREADS
 // threads): thread t holds the order keys of chunks t*ITEMS .. t*ITEMS+ITEMS-1.
 // A: the head's C chunk scores; out: its kept indices; count: its kept count.
-template <int ITEMS>
+template <int ITEMS, int THREADS = kSelRegThreads>
 __device__ __forceinline__ void select_head(const SelectGeom& sg, int T, const float* A, int32_t* out,
                                             int32_t* count) {
-  using Scan = cub::BlockScan<int, kSelRegThreads>;
-  constexpr int BPT = kSelBins / kSelRegThreads;           // histogram bins per thread in the scan
+  static_assert(kSelBins % THREADS == 0, "whole histogram bins per thread");
+  using Scan = cub::BlockScan<int, THREADS>;
+  constexpr int BPT = kSelBins / THREADS;                  // histogram bins per thread in the scan
   __shared__ typename Scan::TempStorage scan_tmp;
   __shared__ int hist[kSelBins];
   __shared__ uint32_t sh_prefix;
@@ -259,8 +260,9 @@ __device__ __forceinline__ void select_head(const SelectGeom& sg, int T, const f
   if (tid == 0) *count = rec0 + (T - Rs);
 }
 
-template <int ITEMS>
-__global__ void __launch_bounds__(kSelRegThreads)
+// THREADS < kSelRegThreads: several CTAs per SM, for calls with more heads than SMs.
+template <int ITEMS, int THREADS>
+__global__ void __launch_bounds__(THREADS, kSelRegThreads / THREADS)
 select_reg_kernel(SelectGeom sg, const __grid_constant__ SeqTable st, const float* __restrict__ scores,
                   int32_t* __restrict__ indices, int32_t* __restrict__ counts) {
   const int bh = blockIdx.x;
@@ -270,7 +272,7 @@ select_reg_kernel(SelectGeom sg, const __grid_constant__ SeqTable st, const floa
   int32_t* out = indices + blockIdx.y * sg.idx_gs + (int64_t)bh * sg.n_cap;
   counts += blockIdx.y * sg.cnt_gs;
   pdl_wait();
-  select_head<ITEMS>(sg, T, A, out, counts + bh);
+  select_head<ITEMS, THREADS>(sg, T, A, out, counts + bh);
   pdl_trigger();
 }
 
@@ -362,22 +364,37 @@ cudaError_t launch_select(const Plan& pl, const SelectGeom& sg, const SeqTable& 
   const int n = pl.B * pl.Hkv;
   if (n == 0 || n_groups == 0) return cudaSuccess;
   const dim3 grid(n, n_groups);
+  // Each CTA's selection is a chain of block-wide steps; with more heads than SMs, smaller CTAs
+  // (several per SM) overlap the chains of different heads.
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    return cudaErrorInvalidDevice;
+  if ((int64_t)n * n_groups > sms) {
+    if (pl.C_max <= 256 * 8)
+      return launch_pdl(select_reg_kernel<8, 256>, grid, dim3(256), 0, s, sg, st, scores, indices, counts);
+    if (pl.C_max <= 512 * 8)
+      return launch_pdl(select_reg_kernel<8, 512>, grid, dim3(512), 0, s, sg, st, scores, indices, counts);
+  }
   if (pl.C_max <= kSelRegThreads * 4)
-    return launch_pdl(select_reg_kernel<4>, grid, dim3(kSelRegThreads), 0, s, sg, st, scores, indices, counts);
+    return launch_pdl(select_reg_kernel<4, kSelRegThreads>, grid, dim3(kSelRegThreads), 0, s, sg, st, scores, indices,
+                      counts);
   if (pl.C_max <= kSelRegThreads * 16)
-    return launch_pdl(select_reg_kernel<16>, grid, dim3(kSelRegThreads), 0, s, sg, st, scores, indices, counts);
+    return launch_pdl(select_reg_kernel<16, kSelRegThreads>, grid, dim3(kSelRegThreads), 0, s, sg, st, scores,
+                      indices, counts);
   return launch_pdl(select_kernel, grid, dim3(kSelThreads), 0, s, sg, st, scores, indices, counts);
 }
 
 // Whether head_kernel can take the log-sum-exp, finalisation and selection of a
 // call: window rows and a register-resident selection fit one 1024-thread CTA,
-// and the call's (group, sequence, head) CTAs fill at least three quarters of
-// the GPU's SMs over the waves they need (one CTA per SM).
+// and the call's (group, sequence, head) CTAs make one wave that fills at least
+// three quarters of the GPU's SMs (one CTA per SM).  With more heads than SMs
+// the separate kernels are faster: a head's CTA spends a fixed time on its
+// log-sum-exp and selection, wave after wave.
 bool head_path(const Plan& pl, int n_groups, int sms) {
   if (pl.wG <= 0 || pl.C_max > kSelRegThreads * 16 || sms <= 0) return false;
   const int64_t heads = (int64_t)pl.B * pl.Hkv * n_groups;
-  const int64_t waves = (heads + sms - 1) / sms;
-  return heads > 0 && 4 * heads >= 3 * waves * sms;
+  return heads <= sms && 4 * heads >= 3 * (int64_t)sms;
 }
 
 cudaError_t launch_head(const Plan& pl, const ScoreGeom& g, const SelectGeom& sg, const SeqTable& st,
