@@ -375,6 +375,8 @@ cudaError_t launch_select(const Plan& pl, const SelectGeom& sg, const SeqTable& 
       return launch_pdl(select_reg_kernel<8, 256>, grid, dim3(256), 0, s, sg, st, scores, indices, counts);
     if (pl.C_max <= 512 * 8)
       return launch_pdl(select_reg_kernel<8, 512>, grid, dim3(512), 0, s, sg, st, scores, indices, counts);
+    if (pl.C_max <= 512 * 12)
+      return launch_pdl(select_reg_kernel<12, 512>, grid, dim3(512), 0, s, sg, st, scores, indices, counts);
   }
   if (pl.C_max <= kSelRegThreads * 4)
     return launch_pdl(select_reg_kernel<4, kSelRegThreads>, grid, dim3(kSelRegThreads), 0, s, sg, st, scores, indices,
