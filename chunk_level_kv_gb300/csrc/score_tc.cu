@@ -361,7 +361,10 @@ __device__ __forceinline__ void load_q(const TcMaps& maps, const TcGeom& g, cons
 }
 
 // ---------------------------------------------------------------- the kernel
-template <int C, bool CAUSAL>
+// WG > 0: the window rows per KV head are known at compile time (the common
+// shapes), so each bin store of the softmax takes its address as base plus an
+// immediate; WG = 0 reads them from the geometry.
+template <int C, bool CAUSAL, int WG>
 __global__ void __launch_bounds__(kThreads, 2)
 score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_constant__ SeqTable st,
                 float* __restrict__ rl, bin_t* __restrict__ bins, int32_t* __restrict__ err) {
@@ -518,6 +521,7 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
       const Item it = decode_item(g, st, item);
       const int nk = it.nk, ntile = it.ntile;
       const int row = it.mt * 128 + rloc;
+      const int wg = WG > 0 ? WG : g.wG;                            // bin stride between chunks
       const bool write = row < g.wG;
       const bool warp_live = it.mt * 128 + lg * 32 < g.wG;         // whole warp of padding rows: no work
       bin_t* ubins = (bin_t*)((char*)bins + it.grp * g.slot_bytes) + (size_t)it.unit * g.cpu * g.wG + row;
@@ -553,7 +557,7 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
           const int ph = (t * kN) % C;
           const int q = (t * kN) / C;
           const RowState before = s;
-          tile_dispatch<C>(ph, mask, taddr, alpha2, s, ubins + (size_t)q * g.wG, g.wG, valid, write, bpol);
+          tile_dispatch<C>(ph, mask, taddr, alpha2, s, ubins + (size_t)q * wg, wg, valid, write, bpol);
           // every bin is at most the row sum: one test per tile catches any value
           // that outgrew the reference (and inf / NaN)
           const bool over = !(s.l <= kBig);
@@ -572,7 +576,7 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
             s.carry = make_float2(s.carry.x * f, s.carry.y * f);
             R = R2;
             s.negR = make_float2(-R2, -R2);
-            tile_dispatch<C>(ph, mask, taddr, alpha2, s, ubins + (size_t)q * g.wG, g.wG, valid, write, bpol);
+            tile_dispatch<C>(ph, mask, taddr, alpha2, s, ubins + (size_t)q * wg, wg, valid, write, bpol);
           }
         }
         tc_fence_before();
@@ -680,7 +684,7 @@ EncodeFn encode_fn() {
 
 struct DeviceInfo {
   int sms = 0;
-  bool attr_set[32] = {};
+  bool attr_set[40] = {};
 };
 
 DeviceInfo& device_info(int dev) {
@@ -692,7 +696,7 @@ DeviceInfo& device_info(int dev) {
   return d;
 }
 
-template <int C, bool CAUSAL>
+template <int C, bool CAUSAL, int WG>
 cudaError_t launch_c(const TcGeom& tg, const TcMaps& maps, const SeqTable& st, float* rl, bin_t* bins, int32_t* err,
                      int slot, cudaStream_t s) {
   int dev = 0;
@@ -700,7 +704,7 @@ cudaError_t launch_c(const TcGeom& tg, const TcMaps& maps, const SeqTable& st, f
   if (e != cudaSuccess) return e;
   DeviceInfo& di = device_info(dev);
   if (!di.attr_set[slot]) {
-    e = cudaFuncSetAttribute(score_tc_kernel<C, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    e = cudaFuncSetAttribute(score_tc_kernel<C, CAUSAL, WG>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     di.attr_set[slot] = true;
   }
@@ -711,15 +715,23 @@ cudaError_t launch_c(const TcGeom& tg, const TcMaps& maps, const SeqTable& st, f
   const int period = tg.Hkv * tg.MT;
   if (grid >= period) grid -= grid % period;
   grid = std::min(tg.n_items, grid);
-  return launch_pdl(score_tc_kernel<C, CAUSAL>, dim3(grid), dim3(kThreads), (size_t)kSmemBytes, s, maps, tg, st, rl, bins,
-                    err);
+  return launch_pdl(score_tc_kernel<C, CAUSAL, WG>, dim3(grid), dim3(kThreads), (size_t)kSmemBytes, s, maps, tg, st, rl,
+                    bins, err);
 }
 
+// Instances per chunk size: the causal window (any w*G), and without it w*G of
+// 128, 256 and 448 at compile time (LLaMA / Mistral / Qwen-shaped GQA groups
+// with 32- and 64-query windows) or any other w*G at run time.
 template <int C>
 cudaError_t launch_causal(bool causal, const TcGeom& tg, const TcMaps& maps, const SeqTable& st, float* rl,
                           bin_t* bins, int32_t* err, int slot, cudaStream_t s) {
-  return causal ? launch_c<C, true>(tg, maps, st, rl, bins, err, slot + 8, s)
-                : launch_c<C, false>(tg, maps, st, rl, bins, err, slot, s);
+  if (causal) return launch_c<C, true, 0>(tg, maps, st, rl, bins, err, slot + 8, s);
+  switch (tg.wG) {
+    case 128: return launch_c<C, false, 128>(tg, maps, st, rl, bins, err, slot + 16, s);
+    case 256: return launch_c<C, false, 256>(tg, maps, st, rl, bins, err, slot + 24, s);
+    case 448: return launch_c<C, false, 448>(tg, maps, st, rl, bins, err, slot + 32, s);
+    default: return launch_c<C, false, 0>(tg, maps, st, rl, bins, err, slot, s);
+  }
 }
 
 constexpr int kSupportedC[] = {3, 4, 5, 8, 10, 16, 20, 30};
