@@ -52,20 +52,26 @@ __device__ __forceinline__ void lse_merge(float& M, float& S, float Mv, float Sv
 }
 
 constexpr int kFinGroup = 8;                    // chunks one warp reduces at a time
+constexpr int kFinWideGroup = 16;               // the same when one load per chunk covers a lane's rows
+
+// w*G of at most 128 rows in fours: every lane's rows of a chunk are one 8-byte load, so a warp
+// step takes kFinWideGroup chunks to keep as many bytes in flight as the wider row counts do.
+__host__ __device__ __forceinline__ bool fin_wide(int wG) { return (wG & 3) == 0 && wG <= 128; }
 
 // One warp: the scores of chunks 0 .. m-1 (m <= kFinGroup) of a unit, whose bins
 // start at cbase (chunk stride wG), into out[0 .. m-1].  Lanes take consecutive
 // rows (coalesced bin loads), all loads of a step are issued together, and each
 // lane forms the weights of its own rows (from R and lse when LSE, else read from
 // wts); the rows are reduced with shuffles.
-template <bool LSE>
+// KG: chunks of the step (kFinGroup, or kFinWideGroup when fin_wide(wG)).
+template <bool LSE, int KG = kFinGroup>
 __device__ __forceinline__ void fin_group(const bin_t* __restrict__ cbase, int wG, int m, const float* wts,
                                           const float* Rrow, const float* Lrow, float* out, int lane) {
-  constexpr int kG = kFinGroup;
+  constexpr int kG = KG;
   float acc[kG];
 #pragma unroll
   for (int i = 0; i < kG; ++i) acc[i] = 0.f;
-  if ((wG & 7) == 0 && wG >= 256) {
+  if (KG == kFinGroup && (wG & 7) == 0 && wG >= 256) {
     // eight consecutive rows per lane: 16-byte loads of eight bins, kG of them in flight
     for (int r = 8 * lane; r < wG; r += 256) {
       uint4 v[kG];

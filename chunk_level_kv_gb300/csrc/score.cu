@@ -200,8 +200,14 @@ finalize_kernel(ScoreGeom g, const __grid_constant__ SeqTable st, const float* _
   const bin_t* ub = bins + ((int64_t)gu * g.cpu + cb) * g.wG;
   float* out = scores + ((int64_t)b * g.Hkv + h) * g.C_max + (int64_t)u * g.cpu + cb;
   constexpr int kW = kFinThreads / 32;
-  for (int ch0 = warp * kFinGroup; ch0 < nc; ch0 += kW * kFinGroup)
-    fin_group<LSE>(ub + (int64_t)ch0 * g.wG, g.wG, min(kFinGroup, nc - ch0), wts, Rrow, Lrow, out + ch0, lane);
+  if (fin_wide(g.wG)) {
+    for (int ch0 = warp * kFinWideGroup; ch0 < nc; ch0 += kW * kFinWideGroup)
+      fin_group<LSE, kFinWideGroup>(ub + (int64_t)ch0 * g.wG, g.wG, min(kFinWideGroup, nc - ch0), wts, Rrow, Lrow,
+                                    out + ch0, lane);
+  } else {
+    for (int ch0 = warp * kFinGroup; ch0 < nc; ch0 += kW * kFinGroup)
+      fin_group<LSE>(ub + (int64_t)ch0 * g.wG, g.wG, min(kFinGroup, nc - ch0), wts, Rrow, Lrow, out + ch0, lane);
+  }
   pdl_trigger();
 }
 

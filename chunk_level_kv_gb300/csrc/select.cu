@@ -342,6 +342,8 @@ head_kernel(ScoreGeom g, SelectGeom sg, const __grid_constant__ SeqTable st, con
 
   // 2. chunk scores of every unit, kFinGroup chunks per warp step
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // (eight-chunk steps even for small w*G: a head's units are short, and with one CTA per head the
+  // sixteen-chunk steps leave more of each unit's last step empty; measured slower at T = 32768)
   const int spu = (g.cpu + kFinGroup - 1) / kFinGroup;            // warp steps per unit
   for (int it = warp; it < U * spu; it += kSelRegThreads / 32) {
     const int u = it / spu;
