@@ -17,35 +17,32 @@ namespace chunkkv {
 constexpr int kMaxWG = 4096;          // window rows per KV head, w * G
 constexpr int kMaxD = 256;            // head dimension
 
-// Chunk bins are stored as 16-bit unsigned floats: 6 exponent bits and 10
-// mantissa bits, covering [2^-40, 2^24) of the row reference (code 0 is zero).
-// A bin is a sum of 2^(t - R) >= 0 over one chunk, at most the row sum l, which
-// the scoring kernels keep below 2^24; the encoding rounds half up at the 11th
-// significant bit, a relative error of at most 2^-11, and flushes bins below
-// 2^-40 of the reference to zero.
+// Chunk bins are stored as 16-bit unsigned floats: the upper 16 bits, rounded
+// half up at the 11th significant bit (a relative error of at most 2^-11), of the
+// fp32 pattern of the bin's value scaled by 2^-kBinShift.  A bin is a sum of
+// 2^(t - R) >= 0 over one chunk; the scoring kernels form the scaled values
+// directly, as 2^(t - R') with the shifted reference R' = R + kBinShift, which
+// is the reference they also write out.  A bin b in [2^-40, 2^23) of R is then
+// a normal float in [2^-126, 2^-63), whose exponent field (1 .. 63) and top ten
+// mantissa bits are the code; smaller bins become fp32 subnormals or zero (an
+// absolute error of at most 2^-51 of R), and code 0 is zero.  Bins from
+// (1 - 2^-12) 2^23 up would round past 16 bits: the tensor-core kernel keeps the
+// bins it keeps below (1 - 2^-10) 2^23 of R (it rescales a row before its sum
+// passes that), the portable kernel saturates (its bins stay below the chunk
+// length).
 using bin_t = uint16_t;
-constexpr uint32_t kBinExpBias = 87;                  // fp32 exponent field of 2^-40
-__device__ __forceinline__ bin_t bin_encode(float b) {
-  const int code = (int)((__float_as_uint(b) + 0x1000u) >> 13) - (int)(kBinExpBias << 10);
-  return (bin_t)min(max(code, 0), 0xFFFF);
+constexpr int kBinShift = 86;
+// Two integer ops: for scaled bins below 2^-63 (the tensor-core kernel's).
+__device__ __forceinline__ bin_t bin_encode(float v) { return (bin_t)((__float_as_uint(v) + 0x1000u) >> 13); }
+// Saturating at the largest code, for bins without a bound.
+__device__ __forceinline__ bin_t bin_encode_sat(float v) {
+  return (bin_t)min((__float_as_uint(v) + 0x1000u) >> 13, 0xFFFFu);
 }
-// Encoding for bins known to be at most 2^23 (the tensor-core kernel rescales a
-// row before its sum passes that): the exponent bias folds into the rounding add
-// and the arithmetic shift leaves bins below 2^-40 negative, so one clamp suffices.
-__device__ __forceinline__ bin_t bin_encode_bounded(float b) {
-  const int code = ((int)__float_as_uint(b) + (0x1000 - (int)(kBinExpBias << 23))) >> 13;
-  return (bin_t)max(code, 0);
-}
-__device__ __forceinline__ float bin_decode(uint32_t code) {
-  return code == 0 ? 0.f : __uint_as_float((code + (kBinExpBias << 10)) << 13);
-}
-// The two bins packed in a 32-bit word (low half first) for the finalisation's
-// weighted sums: three integer ops a bin, reading code 0 as 2^-40 of the row
-// reference instead of 0 (below the encoding's own flush error).
+// The scaled value of a code.
+__device__ __forceinline__ float bin_decode(uint32_t code) { return __uint_as_float(code << 13); }
+// The two bins packed in a 32-bit word (low half first), two integer ops a bin.
 __device__ __forceinline__ float2 bin_decode2(uint32_t v) {
-  const uint32_t lo = ((v << 13) & 0x1FFFE000u) + (kBinExpBias << 23);
-  const uint32_t hi = ((v >> 3) & 0x1FFFE000u) + (kBinExpBias << 23);
-  return make_float2(__uint_as_float(lo), __uint_as_float(hi));
+  return make_float2(__uint_as_float((v << 13) & 0x1FFFE000u), __uint_as_float((v >> 3) & 0x1FFFE000u));
 }
 
 // Per-sequence table passed by value: token offsets and scoring-unit offsets.

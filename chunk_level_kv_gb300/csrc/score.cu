@@ -84,7 +84,9 @@ score_simt_kernel(const E* __restrict__ q, const E* __restrict__ k, ScoreGeom g,
         }
       }
     }
-    // sweep 2: exponentials relative to the unit maximum, summed per chunk
+    // sweep 2: exponentials relative to the unit maximum, summed per chunk; the
+    // reference is shifted by kBinShift, so the bins are formed in their scale
+    m += kBinShift;
     float acc = 0.f, l = 0.f;
     int cur = 0;
     bin_t* brow = bins + (int64_t)gu * g.cpu * g.wG + r;
@@ -103,7 +105,7 @@ score_simt_kernel(const E* __restrict__ q, const E* __restrict__ k, ScoreGeom g,
           for (int e = 0; e < g.d; ++e) dot = fmaf(qrow[e], kr[e], dot);
           const int ch = (kt + j) / g.c;
           if (ch != cur) {
-            brow[(int64_t)cur * g.wG] = bin_encode(acc);
+            brow[(int64_t)cur * g.wG] = bin_encode_sat(acc);
             acc = 0.f;
             cur = ch;
           }
@@ -114,7 +116,7 @@ score_simt_kernel(const E* __restrict__ q, const E* __restrict__ k, ScoreGeom g,
       }
     }
     if (active) {
-      brow[(int64_t)cur * g.wG] = bin_encode(acc);
+      brow[(int64_t)cur * g.wG] = bin_encode_sat(acc);
       rl[((int64_t)gu * 2 + 0) * g.wG + r] = m;
       rl[((int64_t)gu * 2 + 1) * g.wG + r] = l;
     }

@@ -58,7 +58,10 @@ constexpr uint32_t kIdesc = (1u << 4)                         // D = fp32
                           | (1u << 7) | (1u << 10)           // A = B = bf16
                           | ((uint32_t)(kN >> 3) << 17)      // N
                           | ((uint32_t)(128 >> 4) << 24);    // M
-constexpr float kBig = 8388608.0f;                           // 2^23: rescale threshold (within the bin range)
+// Rescale threshold of a row sum: just under 2^23 of the reference, (1 - 2^-10)
+// 2^(23 - kBinShift) in the scaled values the kernel forms, so that every bin it
+// keeps (at most the row sum) rounds to a code inside 16 bits.
+constexpr float kBig = (1.0f - 1.0f / 1024.0f) / 9223372036854775808.0f;   // (1 - 2^-10) 2^-63
 
 // One launch scores up to kMaxGroups reuse groups (one layer each): items are
 // enumerated group by group, each group with its own key tensor map and its own
@@ -168,7 +171,7 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
 }
 // A bin store that asks L2 to keep the line: the finalisation reads it back soon.
 __device__ __forceinline__ void st_keep(bin_t* ptr, float v, uint64_t policy) {
-  asm volatile("st.global.L2::cache_hint.b16 [%0], %1, %2;" ::"l"(ptr), "h"((unsigned short)bin_encode_bounded(v)), "l"(policy)
+  asm volatile("st.global.L2::cache_hint.b16 [%0], %1, %2;" ::"l"(ptr), "h"((unsigned short)bin_encode(v)), "l"(policy)
                : "memory");
 }
 
@@ -551,7 +554,7 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
             mask = __any_sync(0xffffffffu, valid < kN);
           }
           if (t == 0) {
-            R = tile_max(taddr, valid) * g.alpha;
+            R = tile_max(taddr, valid) * g.alpha + kBinShift;      // shifted reference (bin scale)
             s.negR = make_float2(-R, -R);
           }
           const int ph = (t * kN) % C;
@@ -565,7 +568,7 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
             // those rows move their reference to this tile's maximum, rescale what
             // they already hold and redo the tile (the whole warp takes part because
             // the TMEM loads are warp-collective)
-            const float tm = tile_max(taddr, valid) * g.alpha;
+            const float tm = tile_max(taddr, valid) * g.alpha + kBinShift;
             const float R2 = over ? fmaxf(R, tm) : R;
             const float f = ex2(R - R2);
             if (over && write)
