@@ -58,6 +58,30 @@ constexpr int kFinWideGroup = 16;               // the same when one load per ch
 // step takes kFinWideGroup chunks to keep as many bytes in flight as the wider row counts do.
 __host__ __device__ __forceinline__ bool fin_wide(int wG) { return (wG & 3) == 0 && wG <= 128; }
 
+// Warp sums of N values per lane (N a power of two, 2 <= N <= 32) in N - 1 + 5 - log2 N
+// shuffles instead of 5 N: at each of the first log2 N levels a lane keeps half of its values
+// and adds its partner's copies of them, trading the other half.  Returns the index of the sum
+// the lane ends with, in v[0]: value (lane / (32 / N)), held by 32 / N lanes each.
+template <int N>
+__device__ __forceinline__ int warp_sum_each(float (&v)[N], int lane) {
+  static_assert(N >= 2 && N <= 32 && (N & (N - 1)) == 0, "a power of two up to 32");
+  int base = 0;
+#pragma unroll
+  for (int h = N / 2, o = 16; h >= 1; h >>= 1, o >>= 1) {
+    const bool upper = (lane & o) != 0;                   // keeps the upper half of its values
+#pragma unroll
+    for (int i = 0; i < h; ++i) {
+      const float keep = upper ? v[i + h] : v[i];
+      const float give = upper ? v[i] : v[i + h];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, give, o);
+    }
+    base += upper ? h : 0;
+  }
+#pragma unroll
+  for (int o = 16 / N; o > 0; o >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+  return base;
+}
+
 // One warp: the scores of chunks 0 .. m-1 (m <= kFinGroup) of a unit, whose bins
 // start at cbase (chunk stride wG), into out[0 .. m-1].  Lanes take consecutive
 // rows (coalesced bin loads), all loads of a step are issued together, and each
@@ -114,13 +138,8 @@ __device__ __forceinline__ void fin_group(const bin_t* __restrict__ cbase, int w
       for (int i = 0; i < kG; ++i) acc[i] = fmaf(v[i], wv[0], acc[i]);
     }
   }
-#pragma unroll
-  for (int i = 0; i < kG; ++i) {
-    float a = acc[i];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-    if (lane == 0 && i < m) out[i] = a;
-  }
+  const int ch = warp_sum_each<kG>(acc, lane);
+  if ((lane & (32 / kG - 1)) == 0 && ch < m) out[ch] = acc[0];
 }
 
 }  // namespace chunkkv
