@@ -141,3 +141,58 @@ def test_empty_batch_is_a_no_op(ckv):
     arr = (ctypes.c_void_p * 1)(0)
     assert LIB.chunkkv_compress_layers(ctypes.byref(p), 1, 1, arr, arr, arr, arr, arr, None, None, None,
                                        None, 0, None) == 0
+
+
+def _plan(seqlens, Hq, Hkv, w, c, n_layers, n_reuse, d=128, slots=304, item_tiles=2):
+    """The library's workspace plan replayed for the tensor-core path (bf16, d = 128): the unit
+    length (chunks per unit) that minimises waves x (tiles per item + a fixed item cost of two
+    tiles) over 304 CTA slots, ties to longer units, and the workspace bytes that follow."""
+    from math import gcd
+    align = lambda x: (x + 255) // 256 * 256
+    G = Hq // Hkv
+    wG = w * G
+    Cs = [-(-T // c) for T in seqlens]
+    MT = -(-wG // 128)
+    base = 80 // gcd(80, c)                      # chunks in lcm(80, c) keys
+    base_tiles = base * c // 80
+    per_unit_items = Hkv * MT
+    best = cpu = None
+    for m in range(1, 65):
+        cc = base * m
+        items = sum(-(-C // cc) for C in Cs) * per_unit_items
+        if items == 0:
+            break
+        cost = -(-items // slots) * (m * base_tiles + item_tiles)
+        if best is None or cost <= best:
+            best, cpu = cost, cc
+        if items <= per_unit_items:
+            break
+    units = sum(-(-C // cpu) for C in Cs) * Hkv
+    groups = -(-n_layers // n_reuse)
+    B = len(seqlens)
+    slot = align(units * 2 * wG * 4) + align(units * cpu * wG * 2) + align(B * Hkv * wG * 4)
+    qpack = align(B * Hkv * MT * 128 * d * 2)
+    scores = align(B * Hkv * max(Cs) * 4)
+    return 256 + groups * (slot + qpack + scores), cpu
+
+
+@pytest.mark.parametrize("shape", ["llama_32k", "qwen_128k", "mistral_c3", "mistral_c10", "mistral_c30"])
+def test_planner_unit_length(ckv, shape):
+    # The workspace size follows the planner's unit length: it must match the replayed plan, and
+    # for the ragged 16-prompt batch the fixed item cost must keep units several tiles long (with
+    # a cost of tiles alone the planner picked one-tile units there)
+    import torch
+    from synthetic import configs
+    mistral = configs.mistral_ragged().seqlens
+    case = {"llama_32k": ((32768,), 32, 8, 32, 10, 32, 2), "qwen_128k": ((131072,), 28, 4, 64, 10, 28, 2),
+            "mistral_c3": (mistral, 32, 8, 32, 3, 32, 2), "mistral_c10": (mistral, 32, 8, 32, 10, 32, 2),
+            "mistral_c30": (mistral, 32, 8, 32, 30, 32, 2)}[shape]
+    seqlens, Hq, Hkv, w, c, n_layers, n_reuse = case
+    cu = [0]
+    for T in seqlens:
+        cu.append(cu[-1] + T)
+    p, keep = _p(ckv, cu_seqlens=cu, Hq=Hq, Hkv=Hkv, d=128, w=w, c=c, L_max=256, dtype=torch.bfloat16)
+    want, cpu = _plan(seqlens, Hq, Hkv, w, c, n_layers, n_reuse)
+    assert ckv.chunkkv_workspace_size(p, n_layers, n_reuse) == want
+    if shape.startswith("mistral"):
+        assert cpu * c >= 4 * 80, f"units of {cpu * c} keys"
