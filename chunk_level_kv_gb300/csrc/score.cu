@@ -160,7 +160,8 @@ cudaError_t launch_score_simt(const Plan& pl, const ScoreGeom& g, const SeqTable
 constexpr int kFinThreads = 256;
 constexpr int kFinChunks = 128;                 // chunks per CTA: blockIdx.y tiles a unit
 
-template <bool LSE>
+// WG > 0: w*G known at compile time (bin addresses as immediates), else read from g.
+template <bool LSE, int WG>
 __global__ void __launch_bounds__(kFinThreads, 4)
 finalize_kernel(ScoreGeom g, const __grid_constant__ SeqTable st, const float* __restrict__ rl,
                 const bin_t* __restrict__ bins, const float* __restrict__ lse_rows, float* __restrict__ scores) {
@@ -199,16 +200,17 @@ finalize_kernel(ScoreGeom g, const __grid_constant__ SeqTable st, const float* _
 
   const int nc = min(min(g.cpu, C - u * g.cpu) - cb, kFinChunks);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const bin_t* ub = bins + ((int64_t)gu * g.cpu + cb) * g.wG;
+  const int wg = WG > 0 ? WG : g.wG;
+  const bin_t* ub = bins + ((int64_t)gu * g.cpu + cb) * wg;
   float* out = scores + ((int64_t)b * g.Hkv + h) * g.C_max + (int64_t)u * g.cpu + cb;
   constexpr int kW = kFinThreads / 32;
-  if (fin_wide(g.wG)) {
+  if (fin_wide(wg)) {
     for (int ch0 = warp * kFinWideGroup; ch0 < nc; ch0 += kW * kFinWideGroup)
-      fin_group<LSE, kFinWideGroup>(ub + (int64_t)ch0 * g.wG, g.wG, min(kFinWideGroup, nc - ch0), wts, Rrow, Lrow,
+      fin_group<LSE, kFinWideGroup>(ub + (int64_t)ch0 * wg, wg, min(kFinWideGroup, nc - ch0), wts, Rrow, Lrow,
                                     out + ch0, lane);
   } else {
     for (int ch0 = warp * kFinGroup; ch0 < nc; ch0 += kW * kFinGroup)
-      fin_group<LSE>(ub + (int64_t)ch0 * g.wG, g.wG, min(kFinGroup, nc - ch0), wts, Rrow, Lrow, out + ch0, lane);
+      fin_group<LSE>(ub + (int64_t)ch0 * wg, wg, min(kFinGroup, nc - ch0), wts, Rrow, Lrow, out + ch0, lane);
   }
   pdl_trigger();
 }
@@ -289,16 +291,22 @@ cudaError_t launch_finalize(const Plan& pl, const ScoreGeom& g, const SeqTable& 
   if (g.wG == 0)
     return launch_pdl(zero_scores_kernel, dim3(g.n_units, 1, n_groups), dim3(128), 0, s, g, st, scores);
   dim3 grid(g.n_units, (g.cpu + kFinChunks - 1) / kFinChunks, n_groups);
-  if (lse != nullptr)
-    return launch_pdl(finalize_kernel<true>, grid, dim3(kFinThreads), 0, s, g, st, (const float*)rl, bins, lse,
+  if (lse != nullptr) {
+    // a compile-time instance for w*G = 128 (LLaMA / Mistral-shaped groups with 32-query windows);
+    // one for 448 measured slower than the run-time form
+    if (g.wG == 128)
+      return launch_pdl(finalize_kernel<true, 128>, grid, dim3(kFinThreads), 0, s, g, st, (const float*)rl, bins, lse,
+                        scores);
+    return launch_pdl(finalize_kernel<true, 0>, grid, dim3(kFinThreads), 0, s, g, st, (const float*)rl, bins, lse,
                       scores);
+  }
   const size_t smem = (size_t)g.wG * sizeof(float);
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(finalize_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(finalize_kernel<false, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
   }
-  return launch_pdl(finalize_kernel<false>, grid, dim3(kFinThreads), smem, s, g, st, (const float*)rl, bins, lse,
+  return launch_pdl(finalize_kernel<false, 0>, grid, dim3(kFinThreads), smem, s, g, st, (const float*)rl, bins, lse,
                     scores);
 }
 

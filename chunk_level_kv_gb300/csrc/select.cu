@@ -383,6 +383,9 @@ cudaError_t launch_select(const Plan& pl, const SelectGeom& sg, const SeqTable& 
   if (pl.C_max <= kSelRegThreads * 4)
     return launch_pdl(select_reg_kernel<4, kSelRegThreads>, grid, dim3(kSelRegThreads), 0, s, sg, st, scores, indices,
                       counts);
+  if (pl.C_max <= kSelRegThreads * 13)            // 13 keys a thread spill less than 16 (128K: 13108 chunks)
+    return launch_pdl(select_reg_kernel<13, kSelRegThreads>, grid, dim3(kSelRegThreads), 0, s, sg, st, scores,
+                      indices, counts);
   if (pl.C_max <= kSelRegThreads * 16)
     return launch_pdl(select_reg_kernel<16, kSelRegThreads>, grid, dim3(kSelRegThreads), 0, s, sg, st, scores,
                       indices, counts);
