@@ -281,6 +281,9 @@ def test_layer_overlap_closed_forms():
     assert oracle.layer_overlap(a, a[10:30]) == (20, 100)                       # nested
     assert oracle.layer_overlap(np.arange(0, 10), np.arange(5, 15)) == (5, 15)
     assert oracle.layer_jaccard([], []) == 1.0 and oracle.layer_overlap([], [3]) == (0, 1)
+    # a fractional value: |A ∩ B| = 5 over |A ∪ B| = 15 (not the Dice ratio 2·5 / 20)
+    assert oracle.layer_jaccard(np.arange(0, 10), np.arange(5, 15)) == pytest.approx(1 / 3, rel=1e-15)
+    assert oracle.layer_jaccard(a, a[10:30]) == pytest.approx(0.2, rel=1e-15)
 
 
 def test_layer_overlap_against_merge_counts():
@@ -340,6 +343,28 @@ def test_causal_window_brute_force_50_digits():
              for j in range(T)]
         for j in range(int(lim[r]) + 1):
             want[j] += 1 / sum(mpmath.e ** (s[i] - s[j]) for i in range(int(lim[r]) + 1))
+    assert np.allclose(got, [float(x) for x in want], rtol=1e-13, atol=1e-15)
+
+
+def test_causal_window_group_rows_brute_force_50_digits():
+    # G = 2 query heads share the KV head: the row of (member g, window row q) sits at T - w + q
+    # whatever g is, so each member's rows see the same growing key prefixes
+    rng = np.random.default_rng(12)
+    T, w, G, Hkv, d, h = 8, 3, 2, 2, 3, 1
+    q_win = rng.standard_normal((w, G * Hkv, d))
+    keys = rng.standard_normal((T, d))
+    rows = oracle.group_window_rows(q_win, h, G)
+    got = oracle.key_scores(rows, keys, oracle.window_limits(G * w, T, w))
+    mpmath.mp.dps = 50
+    want = [mpmath.mpf(0)] * T
+    for g in range(G):
+        for qi in range(w):
+            x = q_win[qi, h * G + g]
+            last = T - w + qi
+            s = [sum(mpmath.mpf(float(x[e])) * mpmath.mpf(float(keys[j, e])) for e in range(d)) / mpmath.sqrt(d)
+                 for j in range(last + 1)]
+            for j in range(last + 1):
+                want[j] += 1 / sum(mpmath.e ** (s[i] - s[j]) for i in range(last + 1))
     assert np.allclose(got, [float(x) for x in want], rtol=1e-13, atol=1e-15)
 
 
