@@ -3,9 +3,10 @@
 Chunk scores: |gpu - oracle| <= 1e-5 + 1e-3 |oracle|.
 Kept indices: identical to the oracle's, except when the oracle's k-th and
 (k+1)-th largest chunk scores are closer than that tolerance; then any
-selection of k chunks that holds every chunk clearly above the cut and only
-chunks not clearly below it is accepted, and the index list must be exactly
-the one that selection defines.
+selection of exactly k chunks that holds every chunk clearly above the cut and
+only chunks not clearly below it is accepted, and the index list must be
+exactly the one that selection defines (chunks inside the recent window leave
+no trace in the list, so the check asks that such a selection exists).
 K', V': bit-exact rows of K, V at the GPU's indices.
 """
 from __future__ import annotations
@@ -24,7 +25,7 @@ def f64(t) -> np.ndarray:
 
 def check_scores(got: np.ndarray, want: np.ndarray, what: str = "") -> None:
     got = np.asarray(got[: len(want)], dtype=np.float64)
-    bad = np.abs(got - want) > ATOL + RTOL * np.abs(want)
+    bad = ~(np.abs(got - want) <= ATOL + RTOL * np.abs(want))      # NaN fails too
     if bad.any():
         i = int(np.argmax(bad))
         raise AssertionError(f"{what}: {int(bad.sum())} chunk scores off, first at {i}: "
@@ -55,8 +56,10 @@ def check_indices(got_idx: np.ndarray, A: np.ndarray, T: int, c: int, w: int, L_
     chosen = sorted({j // c for j in got if j < R})
     must = {i for i in range(C) if A[i] > a_k + tol}
     allowed = {i for i in range(C) if A[i] >= a_k1 - tol}
-    ok = (must & visible) <= set(chosen) <= allowed and len(chosen) <= k \
-        and len(must - visible) <= k - len(chosen) \
+    # the selection is chosen plus k - |chosen| chunks inside the window, which the list cannot
+    # show: it exists when the window holds every clear winner it must and enough allowed chunks
+    ok = (must & visible) <= set(chosen) <= allowed \
+        and len(must - visible) <= k - len(chosen) <= len(allowed - visible) \
         and got == oracle.kept_indices(chosen, T, c, w).tolist()
     if not ok:
         raise AssertionError(f"{what}: near-tie at the cut but the selection is not a valid one")
