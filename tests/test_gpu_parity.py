@@ -177,6 +177,41 @@ def test_head_kernel_on_a_ragged_batch(ckv):
     assert not out.counts[:, 4].any()                              # the empty sequence keeps nothing
 
 
+@pytest.mark.parametrize("n_layers", [6, 2])
+def test_outputs_beyond_counts_are_left_unwritten(ckv, n_layers):
+    # rows at or beyond counts[b][h] of indices / k_out / v_out and chunk scores at or beyond C_b are left
+    # unwritten: sentinels placed there survive a call, with the fused head kernel (6 layers: 120 heads)
+    # and with separate log-sum-exp, finalisation and selection launches (2 layers: 40 heads)
+    seqlens = (3000, 77, 5, 4096, 0)
+    wl = configs.mistral_ragged().with_params(seqlens=seqlens, B=len(seqlens), n_layers=n_layers, n_reuse=2,
+                                              L_max=600, needles=NeedleSpec(kind="none"), name="unwritten")
+    qs, ks, vs, _ = gen.make_all_layers(wl, DEV)
+    p, keep = ckv.params_for(qs[0], ks[0], wl.cu_seqlens, Hkv=wl.Hkv, w=wl.w, c=wl.c, L_max=wl.L_max)
+    n_cap, C_max = ckv.chunkkv_out_capacity(p)
+    groups = -(-wl.n_layers // wl.n_reuse)
+    ko = [torch.full((wl.B, wl.Hkv, n_cap, wl.d), -3.5, dtype=ks[0].dtype, device=DEV) for _ in range(wl.n_layers)]
+    vo = [torch.full_like(x, 7.25) for x in ko]
+    idx = torch.full((groups, wl.B, wl.Hkv, n_cap), -7, dtype=torch.int32, device=DEV)
+    cnt = torch.full((groups, wl.B, wl.Hkv), -1, dtype=torch.int32, device=DEV)
+    sc = torch.full((groups, wl.B, wl.Hkv, C_max), float("nan"), device=DEV)
+    ws = torch.zeros(ckv.chunkkv_workspace_size(p, wl.n_layers, wl.n_reuse), dtype=torch.uint8, device=DEV)
+    ckv.chunkkv_compress_layers(p, wl.n_reuse, qs, ks, vs, ko, vo, idx, cnt, sc, ws)
+    torch.cuda.synchronize()
+    del keep
+    assert ckv.chunkkv_status_check(ws) == 0
+    idx, cnt, sc = idx.cpu(), cnt.cpu(), sc.cpu()
+    for g in range(groups):
+        for b, T in enumerate(seqlens):
+            C = -(-T // wl.c)
+            for h in range(wl.Hkv):
+                n = int(cnt[g, b, h])
+                assert 0 <= n <= n_cap and (n > 0) == (T > 0)
+                assert (idx[g, b, h, n:] == -7).all() and (idx[g, b, h, :n] >= 0).all()
+                assert not torch.isnan(sc[g, b, h, :C]).any() and torch.isnan(sc[g, b, h, C:]).all()
+                for layer in range(g * wl.n_reuse, min((g + 1) * wl.n_reuse, wl.n_layers)):
+                    assert (ko[layer][b, h, n:] == -3.5).all() and (vo[layer][b, h, n:] == 7.25).all()
+
+
 def test_phase_events_mark_every_phase(ckv):
     wl = configs.llama_model().with_params(seqlens=(3000,), n_layers=4, n_reuse=2, L_max=600, name="phase_events")
     qs, ks, vs, _ = gen.make_all_layers(wl, DEV)
