@@ -367,8 +367,9 @@ chunkkv_status chunkkv_score(const chunkkv_params* p, const void* q_win, const v
   char* qpack = base + pl.off_qpack;
   ScoreGeom g = score_geom(p, pl);
   cudaError_t e = cudaSuccess;
-  // window rows straight from q_win when a tensor map can address them (w divides 128), else packed first
-  const bool direct = tc_q_direct(pl, g, q_win);
+  // window rows straight from q_win when a tensor map can address them (w divides 128 and q_win is
+  // device memory), else packed first with plain loads (q_win may be host memory the GPU addresses)
+  const bool direct = tc_q_direct(pl, g, q_win) && device_memory(q_win);
   if (pl.use_tc && pl.wG > 0 && !direct) {
     const void* ql[1] = {q_win};
     e = launch_pack_q(pl, g, ql, 1, qpack, cs);
@@ -463,9 +464,11 @@ chunkkv_status chunkkv_compress_layers(const chunkkv_params* p, int32_t n_layers
     qsel[i] = q_win[i * n_reuse];
     ksel[i] = k[i * n_reuse];
   }
-  // window rows straight from q_win when a tensor map can address them (w divides 128), else packed
-  // first (every layer has the same strides and was checked for 16-byte alignment: the first decides)
-  const bool direct = tc_q_direct(pl, g, qsel[0]);
+  // window rows straight from q_win when a tensor map can address them (w divides 128, every scoring
+  // layer's q_win in device memory), else packed first with plain loads; every layer has the same
+  // strides and was checked for 16-byte alignment, so the first decides the map's shape
+  bool direct = tc_q_direct(pl, g, qsel[0]);
+  for (int i = 0; direct && i < n_groups; ++i) direct = device_memory(qsel[i]);
   const void* qpack = direct ? nullptr : base + pl.off_qpack;
   e = phase_mark(0, cs);
   if (e == cudaSuccess && pl.use_tc && pl.wG > 0 && !direct) e = launch_pack_q(pl, g, qsel.data(), n_groups, base + pl.off_qpack, cs);

@@ -120,8 +120,10 @@ chunkkv_status chunkkv_workspace_size(const chunkkv_params* p, int32_t n_layers,
  * Window scores per chunk for one layer (ChunkKV §4.1 Algorithm 1 steps 1-3,
  * with the probabilities of Kara §2 Eq. (1)):
  *   A[b][h][i] = sum over g < G, q < w, j in chunk i of softmax_j(Q_w[b,q,h*G+g,:] . K[b,j,h,:] / sqrt(d))
- * q_win: addressable; k: device when chunkkv_score_path(p) is 1 (tensor
- * cores), else addressable; layouts above.  chunk_scores: device, written for
+ * q_win: addressable (on the tensor-core path device Q_w is read through a
+ * tensor map when w divides 128, host Q_w is first packed with plain loads);
+ * k: device when chunkkv_score_path(p) is 1 (tensor cores), else addressable;
+ * layouts above.  chunk_scores: device, written for
  * i < C_b.  ws: device workspace of ws_bytes >= chunkkv_workspace_size(p, 1, 1).
  */
 chunkkv_status chunkkv_score(const chunkkv_params* p, const void* q_win, const void* k,
@@ -157,7 +159,8 @@ chunkkv_status chunkkv_gather(const chunkkv_params* p, int32_t n_layers, const i
  * group g = l / n_reuse; every layer l gathers its own K, V with group
  * l / n_reuse.
  *   q_win: HOST array of n_layers addressable pointers (entries of layers
- *          with l % n_reuse != 0 are not read and may be NULL);
+ *          with l % n_reuse != 0 are not read and may be NULL; as for
+ *          chunkkv_score, host Q_w costs one packing launch);
  *   k, v, k_out, v_out: HOST arrays of n_layers addressable pointers, except
  *          that k[l] of a scoring layer (l % n_reuse == 0) is device memory
  *          when chunkkv_score_path(p) is 1;

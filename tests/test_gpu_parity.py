@@ -484,6 +484,22 @@ def test_compress_with_host_resident_kv(ckv):
     assert e.value.code == 1                  # CHUNKKV_ERR_INVALID_ARG, nothing launched
 
 
+def test_window_queries_in_pinned_host_memory(ckv):
+    # Q_w may be host memory the GPU addresses.  With w dividing 128 the scoring kernel reads device Q_w
+    # through a tensor map; host Q_w goes through the packing kernel's plain loads instead (one launch
+    # more).  Checked against the oracle like every other path.
+    wl = configs.llama_model().with_params(seqlens=(3000, 1234), B=2, n_layers=4, n_reuse=2, L_max=600,
+                                           name="host_q")
+    qs, ks, vs, spans = gen.make_all_layers(wl, DEV)
+    hq = [None if q is None else q.cpu().pin_memory() for q in qs]
+    n0 = ckv.chunkkv_launch_count()
+    run_and_check(ckv, wl, qs=hq, ks=ks, vs=vs, spans=spans)
+    host_launches = ckv.chunkkv_launch_count() - n0
+    n0 = ckv.chunkkv_launch_count()
+    run_and_check(ckv, wl, qs=qs, ks=ks, vs=vs, spans=spans)
+    assert host_launches == ckv.chunkkv_launch_count() - n0 + 1
+
+
 def test_score_entry_point_alone(ckv):
     wl = configs.llama_layer().with_params(seqlens=(5000, 3000), B=2, name="score_only")
     q, k, v, _ = gen.make_all_layers(wl, DEV)
