@@ -177,6 +177,18 @@ def test_head_kernel_on_a_ragged_batch(ckv):
     assert not out.counts[:, 4].any()                              # the empty sequence keeps nothing
 
 
+def test_head_kernel_with_more_than_4096_chunks(ckv):
+    # one wave of 15 sequences x 8 KV heads = 120 heads whose longest sequence has 4334 chunks of 3
+    # tokens: the fused head kernel with 16 selection keys a thread (three launches per call)
+    rng = np.random.default_rng(77)
+    seqlens = (13000,) + tuple(int(x) for x in rng.integers(0, 3000, size=14))
+    wl = configs.mistral_ragged().with_params(seqlens=seqlens, B=len(seqlens), c=3, L_max=900, n_layers=2,
+                                              n_reuse=2, needles=NeedleSpec(kind="none"), name="head_c3_4334")
+    n0 = ckv.chunkkv_launch_count()
+    run_and_check(ckv, wl, seqs=[0, 1, 14])
+    assert ckv.chunkkv_launch_count() - n0 == 3                    # score, head_kernel, gather
+
+
 @pytest.mark.parametrize("n_layers", [6, 2])
 def test_outputs_beyond_counts_are_left_unwritten(ckv, n_layers):
     # rows at or beyond counts[b][h] of indices / k_out / v_out and chunk scores at or beyond C_b are left
@@ -380,6 +392,45 @@ def test_select_is_bit_exact_on_given_scores(ckv):
             n = int(counts[b, h])
             assert n == len(want)
             assert np.array_equal(indices[b, h, :n].cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("many_heads,C_max", [
+    (False, 4096), (False, 4097), (False, 13312), (False, 13313), (False, 16384), (False, 16385),
+    (True, 2048), (True, 2049), (True, 4096), (True, 4097), (True, 6144), (True, 6145)])
+def test_select_instances_at_their_limits(ckv, many_heads, C_max):
+    # the selection's instance follows the chunk capacity and whether the heads fit one wave: 4, 13 or
+    # 16 keys a thread at 1024 threads and the general kernel above 16384 chunks; with more heads than
+    # SMs, 8 / 8 / 12 keys at 256 / 512 / 512 threads up to 6144 chunks.  Each limit and the next size,
+    # bit-exact against the oracle on ragged sequences (one empty, one with a ragged last chunk
+    # straddling the window), half of the heads with many tied scores
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    rng = np.random.default_rng(C_max + 7 * many_heads)
+    Hkv, c, w = 4, 2, 17
+    B = sms // Hkv + 2 if many_heads else 3
+    lens = rng.integers(0, C_max * c + 1, size=B)
+    lens[0], lens[1], lens[2] = C_max * c, 0, C_max * c - 1
+    cu = [0] + list(itertools.accumulate(int(x) for x in lens))
+    L_max = C_max * c * 3 // 10
+    p, keep = ckv.make_params(cu_seqlens=cu, Hq=Hkv, Hkv=Hkv, d=64, w=w, c=c, L_max=L_max, dtype=torch.bfloat16)
+    n_cap, c_max = ckv.chunkkv_out_capacity(p)
+    assert c_max == C_max
+    scores = rng.standard_normal((B, Hkv, C_max)).astype(np.float32)
+    scores[:, ::2] = rng.integers(-3, 6, size=(B, (Hkv + 1) // 2, C_max)).astype(np.float32) * 0.125
+    indices = torch.full((B, Hkv, n_cap), -1, dtype=torch.int32, device=DEV)
+    counts = torch.zeros(B, Hkv, dtype=torch.int32, device=DEV)
+    ckv.chunkkv_select(p, torch.from_numpy(scores).to(DEV), indices, counts)
+    torch.cuda.synchronize()
+    del keep
+    indices, counts = indices.cpu().numpy(), counts.cpu().numpy()
+    for b in sorted({0, 1, 2, B - 1, int(rng.integers(3, B))} if B > 3 else {0, 1, 2}):
+        T = int(lens[b])
+        C = -(-T // c)
+        for h in range(Hkv):
+            A = scores[b, h, :C].astype(np.float64)
+            want = oracle.kept_indices(oracle.top_chunks(A, oracle.n_select(T, c, L_max)), T, c, w)
+            n = int(counts[b, h])
+            assert n == len(want), (b, h)
+            assert np.array_equal(indices[b, h, :n], want), (b, h)
 
 
 def test_gather_is_bit_exact(ckv):
