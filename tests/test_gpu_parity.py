@@ -80,6 +80,8 @@ def test_tiny_fp32_exact(ckv):
     (5000, 10, 48, 40, 8, 500),      # window rows 240: two M tiles in one CTA, the second partly padding
     (2500, 5, 40, 32, 4, 300),       # window rows 320: three M tiles, the last CTA's second tile all padding
     (3333, 16, 64, 16, 2, 512),      # window rows 512: four full M tiles, c = 16
+    (3001, 4, 64, 32, 8, 300),       # c = 4, window rows 256 (the compile-time w*G = 256 instance)
+    (2050, 8, 32, 32, 8, 256),       # c = 8, window rows 128
 ])
 def test_bf16_shapes(ckv, T, c, w, Hq, Hkv, L_max):
     wl = configs.llama_layer().with_params(seqlens=(T,), c=c, w=w, Hq=Hq, Hkv=Hkv, L_max=L_max,
