@@ -130,7 +130,9 @@ def test_maximum_window_rows(ckv):
     run_and_check(ckv, wl)
 
 
-@pytest.mark.parametrize("d,dtype", [(64, "bf16"), (256, "bf16"), (256, "f32")])
+# d = 96 bf16 and d = 80 f32 give 12 and 20 sixteen-byte vectors a row: the gather's kernel for
+# rows that are not a power-of-two number of vectors
+@pytest.mark.parametrize("d,dtype", [(64, "bf16"), (256, "bf16"), (256, "f32"), (96, "bf16"), (80, "f32")])
 def test_other_head_dims_portable_path(ckv, d, dtype):
     wl = configs.llama_layer().with_params(seqlens=(900,), d=d, dtype=dtype, Hq=8, Hkv=2, w=8, L_max=100,
                                            name=f"d{d}_{dtype}")
