@@ -181,6 +181,20 @@ def test_head_kernel_on_a_ragged_batch(ckv):
     assert not out.counts[:, 4].any()                              # the empty sequence keeps nothing
 
 
+@pytest.mark.parametrize("w", [32, 48])
+def test_more_layers_than_one_launch_takes(ckv, w):
+    # 70 layers scored one by one (N_reuse = 1): 70 reuse groups take three scoring launches of at most
+    # 32 groups, 70 layers take two gather launches of at most 64, and with w = 48 (window rows packed
+    # first) two packing launches of at most 64 layers; the groups on both sides of every boundary are
+    # checked against the oracle, with the K' and V' of their layers
+    wl = configs.llama_model().with_params(seqlens=(700, 301), B=2, Hq=8, Hkv=2, w=w, n_layers=70, n_reuse=1,
+                                           L_max=200, needles=NeedleSpec(kind="none"), name=f"layers70_w{w}")
+    n0 = ckv.chunkkv_launch_count()
+    run_and_check(ckv, wl, layers_to_check=[0, 31, 32, 63, 64, 69])
+    packs = 0 if 128 % w == 0 else 2
+    assert ckv.chunkkv_launch_count() - n0 == packs + 3 + 3 + 2     # pack, score, lse / finalize / select, gather
+
+
 def test_head_kernel_with_more_than_4096_chunks(ckv):
     # one wave of 15 sequences x 8 KV heads = 120 heads whose longest sequence has 4334 chunks of 3
     # tokens: the fused head kernel with 16 selection keys a thread (three launches per call)
