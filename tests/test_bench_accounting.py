@@ -1,0 +1,76 @@
+"""bench.py's algorithmic amounts, the numerators of its throughput and roofline figures (CPU only).
+
+Per step the scoring reads K of every scoring layer once (T_total * Hkv * d * elt a group) and does
+2 * w * G * T_total * Hkv * d flops; the finalisation reads one 16-bit bin per (chunk, window row,
+KV head) a group; the gather reads and writes the kept K and V rows of every layer.  The figures
+below are those amounts written out by hand for the two bench workloads, with the kept counts the
+capacity rule gives (min(T, floor(L_max / c) * c + min(w, T)) rows a head).
+"""
+import numpy as np
+import pytest
+import torch
+
+import bench
+from synthetic import configs
+
+PEAKS = {"hbm_gbs": 6770.1, "bf16_tflops": 1917.0, "bf16_tflops_sustained": 1713.4}
+
+
+def _full_counts(wl):
+    groups = -(-wl.n_layers // wl.n_reuse)
+    cnt = np.zeros((groups, wl.B, wl.Hkv), dtype=np.int32)
+    for b, T in enumerate(wl.seqlens):
+        cnt[:, b, :] = min(T, (wl.L_max // wl.c) * wl.c + min(wl.w, T))
+    return torch.from_numpy(cnt)
+
+
+@pytest.mark.parametrize("head", [True, False])
+def test_llama3_32k_amounts(monkeypatch, head):
+    wl = configs.llama_model()
+    assert (wl.n_layers, wl.n_reuse, wl.T_total, wl.Hkv, wl.d, wl.w, wl.G, wl.c) == (32, 2, 32768, 8, 128, 32, 4, 10)
+    counts = _full_counts(wl)
+    assert int(counts[0, 0, 0]) == 655 * 10 + 32
+    monkeypatch.setattr(bench, "head_path", lambda wl, groups: head)
+    ms = {"score": 0.2, "finalize": 0.05, "gather": 0.3}
+    score, fin, gather = bench.phase_rooflines(wl, counts, ms, PEAKS, "measured", 1)
+    assert score["algorithmic_bytes"] == 16 * 32768 * 8 * 128 * 2                 # 1.074 GB
+    assert score["bound"] == "hbm"                  # 137 GF take 80 us at the tensor roof, 1.07 GB 159 us
+    assert fin["algorithmic_bytes"] == 16 * 3277 * 8 * 32 * 4 * 2                  # 107 MB
+    assert fin["kernel"] == ("head_kernel" if head else "finalize_kernel")
+    assert gather["algorithmic_bytes"] == 4 * 32 * 8 * 6582 * 128 * 2              # 1.725 GB
+    for r in (score, fin, gather):
+        assert r["achieved"] == pytest.approx(r["algorithmic_bytes"] / (ms[r["phase"]] * 1e-3) / 1e9, abs=0.006)
+        assert r["frac"] == pytest.approx(r["achieved"] / PEAKS["hbm_gbs"], abs=1e-4)
+    q_bytes = 16 * 32 * 32 * 128 * 2
+    assert bench.algorithmic_bytes(wl, counts) == score["algorithmic_bytes"] + q_bytes + gather["algorithmic_bytes"]
+
+
+def test_qwen2_128k_scoring_is_tensor_bound(monkeypatch):
+    wl = configs.qwen_128k()
+    assert (wl.n_layers, wl.n_reuse, wl.T_total, wl.Hkv, wl.w, wl.G, wl.c) == (28, 2, 131072, 4, 64, 7, 10)
+    monkeypatch.setattr(bench, "head_path", lambda wl, groups: False)
+    ms = {"score": 0.8, "finalize": 0.1, "gather": 0.25}
+    score, fin, gather = bench.phase_rooflines(wl, _full_counts(wl), ms, PEAKS, "measured", 1)
+    flops = 2.0 * 14 * 64 * 7 * 131072 * 4 * 128                                   # 842 GF
+    assert score["bound"] == "tensor" and score["algorithmic_flops"] == flops
+    assert flops / (PEAKS["bf16_tflops_sustained"] * 1e12) > score["algorithmic_bytes"] / (PEAKS["hbm_gbs"] * 1e9)
+    assert score["achieved"] == pytest.approx(flops / 0.8e-3 / 1e12, abs=0.006)
+    assert score["frac"] == pytest.approx(score["achieved"] / PEAKS["bf16_tflops_sustained"], abs=1e-4)
+    assert fin["kernel"] == "finalize_kernel"
+    assert fin["algorithmic_bytes"] == 14 * 13108 * 4 * 64 * 7 * 2                 # 0.66 GB
+    kept = (131072 * 10 // 100) // 10 * 10 + 64
+    # 1.51 GB at full capacity; the bench's own counts are smaller where a selected chunk overlaps the
+    # recent window (1.48 GB measured)
+    assert gather["algorithmic_bytes"] == 4 * 28 * 4 * kept * 128 * 2
+
+
+def test_portable_path_is_reported_against_hbm(monkeypatch):
+    wl = configs.llama_model().with_params(n_layers=2)
+    monkeypatch.setattr(bench, "head_path", lambda wl, groups: False)
+    ms = {"score": 1.0, "finalize": 0.1, "gather": 0.1}
+    score = bench.phase_rooflines(wl, _full_counts(wl), ms, PEAKS, "measured", 0)[0]
+    assert score["kernel"] == "score_simt_kernel" and score["bound"] == "hbm"
+
+
+def test_job_rate_counts_every_rank():
+    assert bench.job_rate(100.0, 4, 2.0) == pytest.approx(200000.0)
