@@ -33,8 +33,10 @@
  *    memory.  The kernels then move only the kept rows across the host link
  *    (NVLink-C2C on Grace systems) instead of a staging copy of whole
  *    layers.  Keys read by the tensor-core scoring kernel go through a TMA
- *    tensor map and must be device memory; a host pointer there is rejected
- *    with CHUNKKV_ERR_INVALID_ARG before anything is launched.
+ *    tensor map and must be device memory (cudaMalloc or a stream-ordered
+ *    pool; cudaPointerGetAttributes type cudaMemoryTypeDevice); a host or
+ *    managed pointer there is rejected with CHUNKKV_ERR_INVALID_ARG before
+ *    anything is launched.
  *  - Every call is asynchronous on the given stream (0 = legacy default).
  *  - Arguments are checked on the host before anything is launched; a bad
  *    argument returns an error code and launches nothing.  A failed launch
