@@ -5,7 +5,8 @@ Each case runs a path that the workloads of test_gpu_parity.py do not reach: a s
 (c = 4 with w*G = 256 at compile time, c = 8), the gather for rows that are not a power-of-two
 number of 16-byte vectors, every selection instance at its chunk limit and one above, the fused
 head kernel's 16-key instance, scoring / packing / gather launches split over many layers, host
-window queries, and the outputs the header leaves unwritten.
+window queries, the outputs the header leaves unwritten, and rows whose values outgrow their
+first-tile reference (the scoring kernel's rescale).
 """
 import itertools
 
@@ -163,3 +164,31 @@ def test_window_queries_in_pinned_host_memory(ckv):
     n0 = ckv.chunkkv_launch_count()
     run_and_check(ckv, wl, qs=qs, ks=ks, vs=vs, spans=spans)
     assert host_launches == ckv.chunkkv_launch_count() - n0 + 1
+
+
+def _rescale_inputs(T, Hq, Hkv, w, d, spike_every, spike_at, seed=5):
+    """Window queries half along a per-head direction u and half against it (alternating window rows),
+    low-magnitude keys, and every spike_every keys (from spike_at) a key of length 34 along u."""
+    g = torch.Generator().manual_seed(seed)
+    G = Hq // Hkv
+    u = torch.randn(Hkv, d, generator=g, dtype=torch.float64)
+    u /= u.norm(dim=1, keepdim=True)
+    sign = torch.where(torch.arange(w) % 2 == 0, 1.0, -1.0).double()
+    q = torch.randn(1, w, Hq, d, generator=g, dtype=torch.float64)
+    q += 10.0 * sign[None, :, None, None] * u.repeat_interleave(G, 0)[None, None]
+    k = 0.3 * torch.randn(T, Hkv, d, generator=g, dtype=torch.float64)
+    pos = torch.arange(spike_at, T - w, spike_every)
+    k[pos] = 34.0 * u[None]
+    v = torch.randn(T, Hkv, d, generator=g, dtype=torch.float64)
+    return q, k, v, pos
+
+
+def test_rows_that_outgrow_their_first_tile_reference(ckv):
+    # The scoring kernel takes a row's reference from the first key tile of a work item; when a later
+    # tile outgrows it by 2^23 the row moves its reference and rescales the bins it already wrote.
+    # Rows along u meet a key about 30 (natural-log units) above their first tile's maximum past the
+    # first tile of every work item; rows against u do not, so each warp holds both kinds.
+    wl = configs.llama_layer().with_params(needles=NeedleSpec(kind="none"), name="rescale")
+    q, k, v, _ = _rescale_inputs(wl.T_total, wl.Hq, wl.Hkv, wl.w, wl.d, 240, 150)
+    qs, ks, vs = [x.to(torch.bfloat16).to(DEV) for x in (q, k, v)]
+    run_and_check(ckv, wl, qs=[qs], ks=[ks], vs=[vs])
