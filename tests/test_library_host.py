@@ -196,3 +196,28 @@ def test_planner_unit_length(ckv, shape):
     assert ckv.chunkkv_workspace_size(p, n_layers, n_reuse) == want
     if shape.startswith("mistral"):
         assert cpu * c >= 4 * 80, f"units of {cpu * c} keys"
+
+
+def test_rescale_inputs_cross_the_threshold(ckv):
+    # The GPU test of the scoring kernel's rescale relies on two facts checked here on the CPU: the
+    # library plans 240-key work items for one 8192-token LLaMA-shaped layer (so the planted key at
+    # offset 150 of every item lies in its second tile), and with bf16 inputs that key stands more
+    # than 23 bits above the first tile's maximum for the rows along u, and far below for the others.
+    import math
+    import torch
+    from synthetic import configs
+    from test_gpu_parity_limits import _rescale_inputs
+    wl = configs.llama_layer()
+    p, keep = _p(ckv, cu_seqlens=[0, wl.T_total], Hq=wl.Hq, Hkv=wl.Hkv, d=wl.d, w=wl.w, c=wl.c,
+                 L_max=wl.L_max, dtype=torch.bfloat16)
+    want, cpu = _plan((wl.T_total,), wl.Hq, wl.Hkv, wl.w, wl.c, 1, 1)
+    assert ckv.chunkkv_workspace_size(p, 1, 1) == want and cpu * wl.c == 240
+    q, k, _, pos = _rescale_inputs(wl.T_total, wl.Hq, wl.Hkv, wl.w, wl.d, 240, 150)
+    q, k = q.to(torch.bfloat16).double(), k.to(torch.bfloat16).double()
+    G = wl.Hq // wl.Hkv
+    for h in range(wl.Hkv):
+        rows = torch.cat([q[0, :, h * G + g, :] for g in range(G)], 0)                 # (member, window row)
+        s = rows @ k[:, h, :].T / math.sqrt(wl.d) * (1 / math.log(2))                # base-2 logits
+        for u0 in range(0, wl.T_total - 240, 240):
+            lift = s[:, u0 + 150] - s[:, u0:u0 + 80].max(dim=1).values
+            assert lift[0::2].min() > 23 and lift[1::2].max() < -23
