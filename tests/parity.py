@@ -1,12 +1,11 @@
 """Comparison rules between the CUDA library and the CPU oracle.
 
 Chunk scores: |gpu - oracle| <= 1e-5 + 1e-3 |oracle|.
-Kept indices: identical to the oracle's, except when the oracle's k-th and
-(k+1)-th largest chunk scores are closer than that tolerance; then any
-selection of exactly k chunks that holds every chunk clearly above the cut and
-only chunks not clearly below it is accepted, and the index list must be
-exactly the one that selection defines (chunks inside the recent window leave
-no trace in the list, so the check asks that such a selection exists).
+Kept indices: identical to the oracle's, or the list of a selection of exactly
+k chunks that is the top-k of some scores each within that tolerance of the
+oracle's (the GPU selects exactly on its own scores, which check_scores holds
+to that tolerance); chunks inside the recent window leave no trace in the
+list, so the check asks that such a selection exists.
 K', V': bit-exact rows of K, V at the GPU's indices.
 """
 from __future__ import annotations
@@ -34,7 +33,14 @@ def check_scores(got: np.ndarray, want: np.ndarray, what: str = "") -> None:
 
 def check_indices(got_idx: np.ndarray, A: np.ndarray, T: int, c: int, w: int, L_max: int,
                   what: str = "") -> str:
-    """Returns 'exact' or 'near-tie' (accepted); raises on a mismatch."""
+    """Returns 'exact' or 'near-tie' (accepted); raises on a mismatch.
+
+    A list other than the oracle's passes when it is the list of a selection S of exactly k chunks
+    that is the top-k of some scores each within the chunk-score tolerance of the oracle's, i.e.
+    min over S of (A_i + tol_i) >= max over the other chunks of (A_j - tol_j).  Chunks inside the
+    recent window leave no trace in the list; the best of them (largest A) fill the slots the list
+    leaves, which is the choice that makes the condition easiest to meet.
+    """
     got = [int(x) for x in got_idx]
     k = oracle.n_select(T, c, L_max)
     sel = oracle.top_chunks(A, k)
@@ -42,27 +48,22 @@ def check_indices(got_idx: np.ndarray, A: np.ndarray, T: int, c: int, w: int, L_
     if got == want:
         return "exact"
     C = len(A)
-    srt = np.sort(A)[::-1]
     if not (0 < k < C):
         raise AssertionError(f"{what}: index list differs (k={k}, C={C}, no tie possible)")
-    a_k, a_k1 = srt[k - 1], srt[k]
-    tol = ATOL + RTOL * abs(a_k)
-    if a_k - a_k1 >= tol:
-        raise AssertionError(f"{what}: index list differs from the oracle and the cut is clear "
-                             f"({a_k!r} vs {a_k1!r}); first difference "
-                             f"{next((i for i, (x, y) in enumerate(zip(got, want)) if x != y), None)}")
     R = max(0, T - w)
-    visible = {i for i in range(C) if i * c < R}
     chosen = sorted({j // c for j in got if j < R})
-    must = {i for i in range(C) if A[i] > a_k + tol}
-    allowed = {i for i in range(C) if A[i] >= a_k1 - tol}
-    # the selection is chosen plus k - |chosen| chunks inside the window, which the list cannot
-    # show: it exists when the window holds every clear winner it must and enough allowed chunks
-    ok = (must & visible) <= set(chosen) <= allowed \
-        and len(must - visible) <= k - len(chosen) <= len(allowed - visible) \
-        and got == oracle.kept_indices(chosen, T, c, w).tolist()
-    if not ok:
-        raise AssertionError(f"{what}: near-tie at the cut but the selection is not a valid one")
+    hidden = sorted((i for i in range(C) if i * c >= R), key=lambda i: -A[i])
+    fill = k - len(chosen)
+    if fill < 0 or fill > len(hidden) or got != oracle.kept_indices(chosen, T, c, w).tolist():
+        raise AssertionError(f"{what}: index list is not the list of any {k} chunks; first difference "
+                             f"{next((i for i, (x, y) in enumerate(zip(got, want)) if x != y), None)}")
+    S = set(chosen) | set(hidden[:fill])
+    tol = ATOL + RTOL * np.abs(A)
+    low = min(A[i] + tol[i] for i in S)
+    high = max(A[j] - tol[j] for j in range(C) if j not in S)
+    if low < high:
+        raise AssertionError(f"{what}: selection differs from the oracle's beyond the score tolerance "
+                             f"(weakest kept {low!r} < strongest dropped {high!r})")
     return "near-tie"
 
 

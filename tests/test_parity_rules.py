@@ -113,3 +113,38 @@ def test_gather_rows_must_match_bit_for_bit():
         check_gather(bad, k, idx)
     with pytest.raises(AssertionError):
         check_gather(k[torch.as_tensor(idx[:-1] + 1)], k, idx[:-1])      # rows one token off
+
+
+def test_near_tie_rule_against_brute_force():
+    # On small cases every subset of chunks gives a candidate list.  The rule must accept exactly
+    # the lists of the k-chunk selections that scores within the tolerance can produce.  Built here
+    # by construction: raise the selection's scores by their tolerance and lower the others by
+    # theirs; the selection is reachable iff it is then the oracle's top-k.
+    import itertools
+    rng = np.random.default_rng(31)
+    n_near = 0
+    for trial in range(60):
+        c = int(rng.integers(1, 4))
+        C = int(rng.integers(2, 8))
+        T = C * c - int(rng.integers(0, c))                   # ragged last chunk when c > 1
+        w = int(rng.integers(0, 2 * c + 1))
+        L_max = int(rng.integers(c, C * c))
+        k = oracle.n_select(T, c, L_max)
+        # scores on a coarse grid with offsets inside and outside the tolerance
+        A = rng.integers(0, 3, size=C) + rng.choice([0.0, 3e-4, 4e-3], size=C)
+        tol = ATOL + RTOL * np.abs(A)
+        valid = set()
+        for Sv in itertools.combinations(range(C), k):
+            up = np.array([A[i] + tol[i] if i in Sv else A[i] - tol[i] for i in range(C)])
+            if oracle.top_chunks(up, k) == list(Sv):
+                valid.add(tuple(_kept(list(Sv), T, c, w).tolist()))
+        for r in range(C + 1):
+            for S in itertools.combinations(range(C), r):
+                got = _kept(list(S), T, c, w)
+                try:
+                    verdict = check_indices(got, A, T, c, w, L_max)
+                except AssertionError:
+                    verdict = None
+                assert (verdict is not None) == (tuple(got.tolist()) in valid), (A, k, S, T, c, w)
+                n_near += verdict == "near-tie"
+    assert n_near > 20                          # the cases reach the near-tie branch often
