@@ -192,3 +192,15 @@ def test_rows_that_outgrow_their_first_tile_reference(ckv):
     q, k, v, _ = _rescale_inputs(wl.T_total, wl.Hq, wl.Hkv, wl.w, wl.d, 240, 150)
     qs, ks, vs = [x.to(torch.bfloat16).to(DEV) for x in (q, k, v)]
     run_and_check(ckv, wl, qs=[qs], ks=[ks], vs=[vs])
+
+
+def test_causal_window_through_the_head_kernel(ckv):
+    # 5 ragged sequences (one empty, two shorter than the window) x 8 KV heads x 3 reuse groups = 120
+    # heads take the fused head kernel; with the causal window, rows at negative positions see no key
+    # and carry an empty (R, sum) pair into its log-sum-exp
+    seqlens = (3000, 77, 5, 4096, 0)
+    wl = configs.mistral_ragged().with_params(seqlens=seqlens, B=len(seqlens), n_layers=6, n_reuse=2, L_max=600,
+                                              needles=NeedleSpec(kind="none"), name="causal_head")
+    n0 = ckv.chunkkv_launch_count()
+    run_and_check(ckv, wl, causal=True)
+    assert ckv.chunkkv_launch_count() - n0 == 3                    # score, head_kernel, gather
