@@ -126,15 +126,24 @@ def test_model_matches_the_oracle_on_plain_random_inputs():
     assert worst < 0.5
 
 
-def test_model_with_a_late_maximum_and_short_chunks():
-    # keys whose logits rise steadily through each item (every tile above the last), c = 3 with a
-    # ragged last chunk and a ragged last item
-    rng = np.random.default_rng(3)
+def _ramp_case(seed=3):
+    # rows sharing a component along v and keys whose logits climb along v key by key (about 15 bits
+    # a tile for most rows), so that most rows outgrow their first-tile reference in every item
+    rng = np.random.default_rng(seed)
     d = 128
-    rows = rng.standard_normal((64, d))
-    ramp = np.linspace(0, 40, 1001)[:, None]
-    keys = rng.standard_normal((1001, d)) + ramp * rows.mean(axis=0)[None, :] / 4
+    v = rng.standard_normal(d)
+    v /= np.linalg.norm(v)
+    rows = rng.standard_normal((64, d)) + 3.0 * v[None, :]
+    keys = rng.standard_normal((1001, d)) + 0.5 * np.arange(1001)[:, None] * v[None, :]
+    return rows, keys
+
+
+def test_model_with_a_climbing_maximum_and_short_chunks():
+    # c = 3 with a ragged last chunk and a ragged last item; the planted fault shows the rescale is hit
+    rows, keys = _ramp_case()
     _check(rows, keys, 3, 240)
+    with pytest.raises(AssertionError):
+        _check(rows, keys, 3, 240, rescale_codes=False)
 
 
 def test_model_with_flat_and_peaked_rows():
