@@ -1,11 +1,13 @@
 """Comparison rules between the CUDA library and the CPU oracle.
 
 Chunk scores: |gpu - oracle| <= 1e-5 + 1e-3 |oracle|.
-Kept indices: identical to the oracle's, or the list of a selection of exactly
-k chunks that is the top-k of some scores each within that tolerance of the
-oracle's (the GPU selects exactly on its own scores, which check_scores holds
-to that tolerance); chunks inside the recent window leave no trace in the
-list, so the check asks that such a selection exists.
+Kept indices: identical to the oracle's, except when the oracle's k-th and
+(k+1)-th largest chunk scores differ by less than that tolerance; then the list
+of any selection of exactly k chunks that is the top-k of some scores each
+within that tolerance of the oracle's is accepted (the GPU selects exactly on
+its own scores, which check_scores holds to that tolerance); chunks inside the
+recent window leave no trace in the list, so the check asks that such a
+selection exists.
 K', V': bit-exact rows of K, V at the GPU's indices.
 """
 from __future__ import annotations
@@ -35,11 +37,12 @@ def check_indices(got_idx: np.ndarray, A: np.ndarray, T: int, c: int, w: int, L_
                   what: str = "") -> str:
     """Returns 'exact' or 'near-tie' (accepted); raises on a mismatch.
 
-    A list other than the oracle's passes when it is the list of a selection S of exactly k chunks
-    that is the top-k of some scores each within the chunk-score tolerance of the oracle's, i.e.
-    min over S of (A_i + tol_i) >= max over the other chunks of (A_j - tol_j).  Chunks inside the
-    recent window leave no trace in the list; the best of them (largest A) fill the slots the list
-    leaves, which is the choice that makes the condition easiest to meet.
+    A list other than the oracle's passes only at a near-tie, when the oracle's k-th and (k+1)-th
+    largest chunk scores differ by less than the chunk-score tolerance, and only when it is the list
+    of a selection S of exactly k chunks that is the top-k of some scores each within that tolerance
+    of the oracle's: min over S of (A_i + tol_i) >= max over the other chunks of (A_j - tol_j).
+    Chunks inside the recent window leave no trace in the list; the best of them (largest A) fill
+    the slots the list leaves, which is the choice that makes the condition easiest to meet.
     """
     got = [int(x) for x in got_idx]
     k = oracle.n_select(T, c, L_max)
@@ -50,6 +53,12 @@ def check_indices(got_idx: np.ndarray, A: np.ndarray, T: int, c: int, w: int, L_
     C = len(A)
     if not (0 < k < C):
         raise AssertionError(f"{what}: index list differs (k={k}, C={C}, no tie possible)")
+    srt = np.sort(A)[::-1]
+    a_k, a_k1 = srt[k - 1], srt[k]
+    if a_k - a_k1 >= ATOL + RTOL * abs(a_k):
+        raise AssertionError(f"{what}: index list differs from the oracle and the cut is clear "
+                             f"({a_k!r} vs {a_k1!r}); first difference "
+                             f"{next((i for i, (x, y) in enumerate(zip(got, want)) if x != y), None)}")
     R = max(0, T - w)
     chosen = sorted({j // c for j in got if j < R})
     hidden = sorted((i for i in range(C) if i * c >= R), key=lambda i: -A[i])

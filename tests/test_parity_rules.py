@@ -116,10 +116,11 @@ def test_gather_rows_must_match_bit_for_bit():
 
 
 def test_near_tie_rule_against_brute_force():
-    # On small cases every subset of chunks gives a candidate list.  The rule must accept exactly
-    # the lists of the k-chunk selections that scores within the tolerance can produce.  Built here
-    # by construction: raise the selection's scores by their tolerance and lower the others by
-    # theirs; the selection is reachable iff it is then the oracle's top-k.
+    # On small cases every subset of chunks gives a candidate list.  The rule must accept the
+    # oracle's list and, when the oracle's k-th and (k+1)-th scores differ by less than the
+    # tolerance, exactly the lists of the k-chunk selections that scores within the tolerance can
+    # produce.  Built here by construction: raise the selection's scores by their tolerance and
+    # lower the others by theirs; the selection is reachable iff it is then the oracle's top-k.
     import itertools
     rng = np.random.default_rng(31)
     n_near = 0
@@ -133,8 +134,10 @@ def test_near_tie_rule_against_brute_force():
         # scores on a coarse grid with offsets inside and outside the tolerance
         A = rng.integers(0, 3, size=C) + rng.choice([0.0, 3e-4, 4e-3], size=C)
         tol = ATOL + RTOL * np.abs(A)
-        valid = set()
-        for Sv in itertools.combinations(range(C), k):
+        srt = np.sort(A)[::-1]
+        near = 0 < k < C and srt[k - 1] - srt[k] < ATOL + RTOL * abs(srt[k - 1])
+        valid = {tuple(_kept(oracle.top_chunks(A, k), T, c, w).tolist())}
+        for Sv in itertools.combinations(range(C), k) if near else ():
             up = np.array([A[i] + tol[i] if i in Sv else A[i] - tol[i] for i in range(C)])
             if oracle.top_chunks(up, k) == list(Sv):
                 valid.add(tuple(_kept(list(Sv), T, c, w).tolist()))
