@@ -6,9 +6,14 @@ inputs resident in HBM.  value = algorithmic bytes / device time, where the
 algorithmic bytes are the keys read by every scoring layer plus the kept K and
 V rows read and written on every layer (plus the window queries).
 
---impl reference times the CPU oracle on the host cores on a bounded sample
-of the same workload (one scoring layer of a few heads per step) and reports
-the same metric.
+The default workload is the largest single-GPU configuration, the Qwen2-7B-
+shaped 28-layer model with T = 131072 (qwen_128k); the LLaMA-3-8B-shaped
+32-layer model with T = 32768 is measured in the same run and reported as a
+secondary line object.
+
+--impl reference times the CPU oracle, single-threaded, on the host on a
+bounded sample of the same workload (whole heads of the first scoring layer
+per step) and reports the same metric.
 """
 from __future__ import annotations
 
@@ -25,6 +30,22 @@ import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
+
+
+def _oracle_process() -> bool:
+    """Whether this process only times the CPU oracle (the reference arm, or the child process of the
+    cpu_baseline leg): those run the oracle single-threaded, so every BLAS / OpenMP pool is held to one
+    thread before numpy loads."""
+    argv = sys.argv[1:]
+    ref = any(a == "--impl=reference" or (a == "--impl" and i + 1 < len(argv) and argv[i + 1] == "reference")
+              for i, a in enumerate(argv))
+    return ref or "--cpu-baseline-child" in argv
+
+
+if _oracle_process():
+    for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS",
+               "NUMEXPR_NUM_THREADS", "VECLIB_MAXIMUM_THREADS"):
+        os.environ[_v] = "1"
 
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
@@ -159,16 +180,19 @@ def head_path(wl, groups) -> bool:
     return wl.w * wl.G > 0 and c_max <= 16384 and heads <= sms and 4 * heads >= 3 * sms
 
 
-def phase_rooflines(wl, counts, phase_ms, peaks, peak_src, path):
+def phase_rooflines(wl, counts, phase_ms, peaks, peak_src, path, ex2_rate=None):
     """Roofline of the scoring, finalisation and gather launches of one compress step.
 
     Algorithmic amounts per launch (all layers / reuse groups of the step):
-      score:    K of every scoring layer read once (T_total*Hkv*d*elt per group) and
-                2*w*G*T_total*Hkv*d flops; the roof is whichever takes longer at peak
-                (HBM copy bandwidth, or the sustained bf16 tensor rate);
+      score:    K of every scoring layer read once (T_total*Hkv*d*elt per group),
+                2*w*G*T_total*Hkv*d flops and one base-2 exponential per logit
+                (w*G*T_total*Hkv per group); the roof is whichever takes longest at peak:
+                HBM copy bandwidth, the sustained bf16 tensor rate, or the exponential rate
+                that chunkkv_probe_ex2 measured on this GPU (ex2_rate, exponentials/s);
       finalize: one 16-bit bin per (chunk, window row, KV head) per group read once (the phase is
                 one kernel with the log-sum-exp and the selection when head_path() holds);
       gather:   kept K and V rows read and written (4*kept*d*elt per layer).
+    Returns (rooflines of the three phases, every roof of the scoring phase).
     """
     elt = 2 if wl.dtype == "bf16" else 4
     groups = -(-wl.n_layers // wl.n_reuse)
@@ -177,7 +201,6 @@ def phase_rooflines(wl, counts, phase_ms, peaks, peak_src, path):
     chunks = sum(-(-(wl.cu_seqlens[b + 1] - wl.cu_seqlens[b]) // wl.c) for b in range(wl.B))
     hbm = peaks["hbm_gbs"]
     tensor = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
-    out = []
 
     def hbm_roof(phase, kernel, nbytes):
         ms = phase_ms[phase]
@@ -189,21 +212,87 @@ def phase_rooflines(wl, counts, phase_ms, peaks, peak_src, path):
 
     score_bytes = groups * wl.T_total * wl.Hkv * wl.d * elt
     score_flops = 2.0 * groups * wl.w * wl.G * wl.T_total * wl.Hkv * wl.d
+    score_exps = float(groups * wl.w * wl.G * wl.T_total * wl.Hkv)
     kernel = "score_tc_kernel" if path == 1 else "score_simt_kernel"
-    if path == 1 and score_flops / (tensor * 1e12) > score_bytes / (hbm * 1e9):
-        ms = phase_ms["score"]
+    ms = phase_ms["score"]
+    score_roofs = [dict(hbm_roof("score", kernel, score_bytes), ideal_ms=round(score_bytes / (hbm * 1e9) * 1e3, 5))]
+    if path == 1:
         ach = score_flops / (ms * 1e-3) / 1e12
-        out.append({"phase": "score", "kernel": kernel, "bound": "tensor", "achieved": round(ach, 2),
-                    "peak": tensor, "unit": "TFLOP/s", "frac": round(ach / tensor, 4),
-                    "traffic": traffic_record(wl.name, kernel), "algorithmic_flops": score_flops,
-                    "algorithmic_bytes": int(score_bytes), "avg_launch_ms": round(ms, 5),
-                    "peak_source": f"{peak_src} bf16_tflops_sustained"})
-    else:
-        out.append(hbm_roof("score", kernel, score_bytes))
+        score_roofs.append({"phase": "score", "kernel": kernel, "bound": "tensor", "achieved": round(ach, 2),
+                            "peak": tensor, "unit": "TFLOP/s", "frac": round(ach / tensor, 4),
+                            "traffic": traffic_record(wl.name, kernel), "algorithmic_flops": score_flops,
+                            "algorithmic_bytes": int(score_bytes), "avg_launch_ms": round(ms, 5),
+                            "ideal_ms": round(score_flops / (tensor * 1e12) * 1e3, 5),
+                            "peak_source": f"{peak_src} bf16_tflops_sustained"})
+    if ex2_rate:
+        ach = score_exps / (ms * 1e-3) / 1e9
+        peak = ex2_rate["exp_per_s"] / 1e9
+        score_roofs.append({"phase": "score", "kernel": kernel, "bound": "sfu", "achieved": round(ach, 2),
+                            "peak": round(peak, 2), "unit": "Gexp/s", "frac": round(ach / peak, 4),
+                            "traffic": traffic_record(wl.name, kernel), "algorithmic_exps": score_exps,
+                            "algorithmic_bytes": int(score_bytes), "avg_launch_ms": round(ms, 5),
+                            "ideal_ms": round(score_exps / ex2_rate["exp_per_s"] * 1e3, 5),
+                            "peak_source": "measured here: chunkkv_probe_ex2 (ex2.approx.ftz.f32)"})
+    out = [max(score_roofs, key=lambda r: r["ideal_ms"])]         # the roof that takes longest binds
     fin_kernel = "head_kernel" if head_path(wl, groups) else "finalize_kernel"
     out.append(hbm_roof("finalize", fin_kernel, groups * chunks * wl.Hkv * wl.w * wl.G * 2))
     out.append(hbm_roof("gather", "gather_kernel", 4 * kept_all * wl.d * elt))
+    return out, score_roofs
+
+
+def ex2_probe(ckv, dev, gpu_index: int):
+    """Exponential rate of this GPU: chunkkv_probe_ex2 over 8 CTAs of 256 threads per SM, launches back
+    to back for about half a second (median of the per-launch event times), with the SM clock sampled
+    meanwhile."""
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    blocks, iters = 8 * sms, 2048
+    sink = torch.empty(blocks * 256, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    n_exp = ckv.chunkkv_probe_ex2(sink, blocks, iters)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(gpu_index)
+    sampler.start()
+    time.sleep(0.3)
+    evs = []
+    t_end = time.perf_counter() + 0.6
+    while time.perf_counter() < t_end or len(evs) < 20:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        ckv.chunkkv_probe_ex2(sink, blocks, iters)
+        e1.record(stream)
+        evs.append((e0, e1))
+        if len(evs) % 50 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = statistics.median(a.elapsed_time(b) for a, b in evs)
+    rate = n_exp / (ms * 1e-3)
+    out = {"exp_per_s": rate, "launch_ms": round(ms, 5), "exps_per_launch": n_exp, "launches": len(evs),
+           "sm_mhz": clocks.get("sm_mhz"), "reasons": clocks.get("reasons")}
+    if clocks.get("sm_mhz"):
+        out["exp_per_clk_per_sm"] = round(rate / (clocks["sm_mhz"] * 1e6) / sms, 2)
     return out
+
+
+def link_probe(dev, nbytes: int = 1 << 30):
+    """Host link bandwidth with pinned host memory: one 1 GiB cudaMemcpyAsync each way (best of 3)."""
+    h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    res = {}
+    for name, dst, src in (("h2d", d, h), ("d2h", h, d)):
+        best = None
+        for _ in range(3):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            dst.copy_(src, non_blocking=True)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1)
+            best = ms if best is None else min(best, ms)
+        res[f"{name}_GBps"] = round(nbytes / (best * 1e-3) / 1e9, 1)
+    del h, d
+    return res
 
 
 def workload_of(args):
@@ -220,15 +309,10 @@ def workload_of(args):
     return wl
 
 
-def run_gpu(args):
-    import chunk_level_kv_gb300 as ckv
-    ws_n, rank, local = dist_env()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if ws_n > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-    wl = workload_of(args)
+def device_timing(ckv, wl, args, dev, local, ws_n, peaks, peak_src, ex2_rate):
+    """Warm-up, then K timed compress steps (CUDA events on the launching stream, inputs resident in
+    HBM), then K more steps with the library's phase events.  Returns the inputs, outputs and the
+    measured figures of the workload."""
     qs, ks, vs, _ = gen.make_all_layers(wl, dev)
     p, keep = ckv.params_for(next(q for q in qs if q is not None), ks[0], wl.cu_seqlens, Hkv=wl.Hkv, w=wl.w,
                              c=wl.c, L_max=wl.L_max)
@@ -270,18 +354,17 @@ def run_gpu(args):
         times.append((e0, e1))
     torch.cuda.synchronize()
     launches = ckv.chunkkv_launch_count() - launches0        # library kernels in the timed region
+    if ws_n > 1:
+        torch.distributed.barrier()
     clocks = sampler.stop()
     ms = [a.elapsed_time(b) for a, b in times]
     ckv.chunkkv_status_check(ws)
     step_ms = slowest_rank(sum(ms) / len(ms), ws_n)
     nbytes = algorithmic_bytes(wl, cnt)
-    value = job_rate(nbytes, ws_n, step_ms) / 1e9
-    tokens_s = job_rate(wl.T_total, ws_n, step_ms)
 
     # ---- device time of each phase inside the same compress call: K more steps with the library's
     # phase events recorded on its stream (a record between two launches ends their overlap, so these
     # steps are not the headline ones)
-    peaks, peak_src = measured_peaks()
     path = ckv.chunkkv_score_path(p)
     n_ev = len(ckv.PHASES) + 1
     phase_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
@@ -294,8 +377,47 @@ def run_gpu(args):
     torch.cuda.synchronize()
     phase_ms = {name: sum(evs[i].elapsed_time(evs[i + 1]) for evs in phase_evs) / len(phase_evs)
                 for i, name in enumerate(ckv.PHASES)}
-    roofs = phase_rooflines(wl, cnt, phase_ms, peaks, peak_src, path)
+    roofs, score_roofs = phase_rooflines(wl, cnt, phase_ms, peaks, peak_src, path, ex2_rate)
     dominant = max(roofs, key=lambda r: phase_ms[r["phase"]])
+    value = job_rate(nbytes, ws_n, step_ms) / 1e9
+    return {"wl": wl, "p": p, "keep": keep, "qs": qs, "ks": ks, "vs": vs, "ko": ko, "vo": vo, "idx": idx,
+            "cnt": cnt, "ws": ws, "n_cap": n_cap, "step": step, "stream": stream, "l2_note": l2_note,
+            "launches": launches, "clocks": clocks, "step_ms": step_ms, "nbytes": nbytes, "value": value,
+            "tokens_s": job_rate(wl.T_total, ws_n, step_ms), "phase_ms": phase_ms, "roofs": roofs,
+            "score_roofs": score_roofs, "dominant": dominant}
+
+
+def run_gpu(args):
+    import chunk_level_kv_gb300 as ckv
+    ws_n, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws_n > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    peaks, peak_src = measured_peaks()
+    ex2_rate = ex2_probe(ckv, dev, local)
+
+    secondary = None
+    if args.secondary != "none" and args.secondary != args.workload:
+        sec_args = argparse.Namespace(**vars(args))
+        sec_args.workload, sec_args.chunk, sec_args.budget = args.secondary, 0, 0
+        t = device_timing(ckv, workload_of(sec_args), args, dev, local, ws_n, peaks, peak_src, ex2_rate)
+        secondary = {"workload": t["wl"].name, "value": round(t["value"], 3), "unit": UNIT,
+                     "ms_per_step": round(t["step_ms"], 4), "hbm_roof_frac": round(t["value"] / ws_n / peaks["hbm_gbs"], 4),
+                     "tokens_per_s": round(t["tokens_s"], 1), "algorithmic_bytes_per_step": t["nbytes"],
+                     "phases_ms": {k: round(v, 5) for k, v in t["phase_ms"].items()}, "roofline": t["dominant"],
+                     "roofline_score": t["score_roofs"], "gpu_launches": int(t["launches"]), "clocks": t["clocks"],
+                     "config": {"B": t["wl"].B, "T_total": t["wl"].T_total, "layers": t["wl"].n_layers,
+                                "n_reuse": t["wl"].n_reuse, "Hq": t["wl"].Hq, "Hkv": t["wl"].Hkv, "w": t["wl"].w,
+                                "c": t["wl"].c, "L_max": t["wl"].L_max, "l2": t["l2_note"]}}
+        del t
+        torch.cuda.empty_cache()
+
+    t = device_timing(ckv, workload_of(args), args, dev, local, ws_n, peaks, peak_src, ex2_rate)
+    wl, p, qs, ks, vs, ko, vo = t["wl"], t["p"], t["qs"], t["ks"], t["vs"], t["ko"], t["vo"]
+    idx, cnt, ws, n_cap, step, stream = t["idx"], t["cnt"], t["ws"], t["n_cap"], t["step"], t["stream"]
+    step_ms, nbytes, value, phase_ms = t["step_ms"], t["nbytes"], t["value"], t["phase_ms"]
 
     # ---- §4.2 observation behind Algorithm 2: adjacent-layer overlap of the kept lists with every layer
     # scored (n_reuse = 1), and the device time of the overlap kernel
@@ -408,6 +530,7 @@ def run_gpu(args):
             row * (sum(kept) + sum(n for layer, n in enumerate(kept) if layer % wl.n_reuse != 0))
         d2h = nbytes_of([hidx, hcnt]) + 2 * row * sum(kept)
         e2e = {"value": round(nbytes * ws_n / (e2e_ms * 1e-3) / 1e9, 3), "unit": UNIT,
+               "link_probe": link_probe(dev),
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms, 4),
                "transfers": "window queries and scoring-layer keys copied in (two device buffer sets); "
                             "kept K/V rows read from and K'/V' written to pinned host memory by the gather "
@@ -423,7 +546,7 @@ def run_gpu(args):
 
     cpu = None
     if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(wl, qs, ks, budget_s=args.cpu_seconds)
+        cpu = cpu_baseline(args, budget_s=args.cpu_seconds)
 
     if ws_n > 1:
         torch.distributed.barrier()
@@ -436,37 +559,68 @@ def run_gpu(args):
         "config": {"workload": wl.name, "B": wl.B, "T": list(wl.seqlens) if wl.B <= 4 else "ragged",
                    "T_total": wl.T_total, "layers": wl.n_layers, "n_reuse": wl.n_reuse, "Hq": wl.Hq,
                    "Hkv": wl.Hkv, "d": wl.d, "w": wl.w, "c": wl.c, "L_max": wl.L_max,
-                   "l2": l2_note, "parallelism": f"replicas x{ws_n}"},
-        "tokens_per_s": round(tokens_s, 1),
+                   "l2": t["l2_note"], "parallelism": f"replicas x{ws_n}"},
+        "tokens_per_s": round(t["tokens_s"], 1),
         "algorithmic_bytes_per_step": nbytes,
         "hbm_roof_frac": round(value / ws_n / peaks["hbm_gbs"], 4),
-        "roofline": dominant,
-        "roofline_score": next(r for r in roofs if r["phase"] == "score"),
+        "roofline": t["dominant"],
+        "roofline_score": t["score_roofs"],
+        "ex2_probe": ex2_rate,
         "phases_ms": {k: round(v, 5) for k, v in phase_ms.items()},
+        "secondary": secondary,
         "layer_overlap": overlap,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "e2e_staged": e2e_staged,
-        "gpu_launches": int(launches),
-        "clocks": clocks,
+        "gpu_launches": int(t["launches"]),
+        "clocks": t["clocks"],
     }
     print(json.dumps(line), flush=True)
 
 
-def cpu_baseline(wl, qs, ks, budget_s: float = 15.0):
-    """The oracle as it stands on this host: Algorithm 1 for whole heads of scoring layer 0."""
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.machine()
+
+
+def pin_one_core() -> int:
+    """Restrict this process to the first core it may run on; returns that core."""
+    if not hasattr(os, "sched_getaffinity"):
+        return -1
+    core = min(os.sched_getaffinity(0))
+    os.sched_setaffinity(0, {core})
+    return core
+
+
+def oracle_sample(wl, q, k, budget_s: float) -> dict:
+    """The oracle as it stands, in this process: Algorithm 1 for whole (sequence, KV head) pairs of the
+    first scoring layer (q: [B, w, Hq, d], k: [T_total, Hkv, d] torch CPU tensors), until budget_s."""
     import oracle
-    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    q = qs[0].detach().to("cpu", torch.float32).numpy().astype(np.float64)
+    qf = q.detach().to("cpu", torch.float32).numpy().astype(np.float64)
     cu = wl.cu_seqlens
     elt = 2 if wl.dtype == "bf16" else 4
     done_bytes, done_tokens, heads = 0, 0, 0
     t0 = time.perf_counter()
     for b in range(wl.B):
-        kb = ks[0][cu[b]:cu[b + 1]].detach().to("cpu", torch.float32).numpy().astype(np.float64)
+        kb = k[cu[b]:cu[b + 1]].detach().to("cpu", torch.float32).numpy().astype(np.float64)
         T = cu[b + 1] - cu[b]
         for h in range(wl.Hkv):
-            A, sel, idx = oracle.chunkkv_head(oracle.group_window_rows(q[b], h, wl.G), kb[:, h], wl.c, wl.w,
+            A, sel, idx = oracle.chunkkv_head(oracle.group_window_rows(qf[b], h, wl.G), kb[:, h], wl.c, wl.w,
                                               wl.L_max)
             oracle.gather(kb[:, h], idx)
             done_bytes += T * wl.d * elt + 2 * len(idx) * wl.d * elt
@@ -477,29 +631,57 @@ def cpu_baseline(wl, qs, ks, budget_s: float = 15.0):
         if time.perf_counter() - t0 > budget_s:
             break
     dt = time.perf_counter() - t0
-    return {"value": round(done_bytes / dt / 1e9, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
+    return {"value": round(done_bytes / dt / 1e9, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"Algorithm 1 on {heads} (sequence, KV head) pairs of scoring layer 0 "
                       f"({done_tokens} tokens, {dt:.1f} s), fp64 numpy, K read + kept K/V counted "
-                      f"like the GPU metric", "threads": "numpy/BLAS default"}
+                      f"like the GPU metric",
+            "threads": 1, "cpu_model": cpu_model()}
+
+
+def cpu_baseline(args, budget_s: float = 15.0) -> dict:
+    """The oracle timed on one host core: a child process of this script (BLAS and OpenMP pools at one
+    thread, affinity to one core) generates the first scoring layer of the same workload on the CPU and
+    runs oracle_sample on it."""
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-baseline-child", "--workload", args.workload,
+           "--cpu-seconds", str(budget_s)]
+    if args.chunk:
+        cmd += ["--chunk", str(args.chunk)]
+    if args.budget:
+        cmd += ["--budget", str(args.budget)]
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=budget_s * 4 + 300)
+    lines = [x for x in r.stdout.splitlines() if x.startswith("{")]
+    if r.returncode != 0 or not lines:
+        return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle",
+                "error": (r.stderr or r.stdout)[-400:]}
+    return json.loads(lines[-1])
+
+
+def run_cpu_baseline_child(args):
+    core = pin_one_core()
+    wl = workload_of(args)
+    q, k, v = gen.make_layer(wl, 0, "cpu")
+    res = oracle_sample(wl, q, k, args.cpu_seconds)
+    res["core"] = core
+    print(json.dumps(res), flush=True)
 
 
 def run_reference(args):
+    """The reference arm: the oracle, single-threaded on one host core, timed step by step on a bounded
+    sample of the workload (whole heads of the first scoring layer)."""
     ws_n, rank, local = dist_env()
     if rank != 0:
         return
+    core = pin_one_core()
     wl = workload_of(args)
-    qs, ks = [], []
     q, k, v = gen.make_layer(wl, 0, "cpu")
-    qs.append(q)
-    ks.append(k)
     per_step = min(args.cpu_seconds, 150.0 / max(1, args.steps + args.warmup))   # whole run ~ 2.5 min
     for _ in range(args.warmup):
-        cpu_baseline(wl, qs, ks, budget_s=per_step / 4)
+        oracle_sample(wl, q, k, budget_s=per_step / 4)
     vals = []
     t0 = time.perf_counter()
     last = None
     for _ in range(args.steps):
-        last = cpu_baseline(wl, qs, ks, budget_s=per_step)
+        last = oracle_sample(wl, q, k, budget_s=per_step)
         vals.append(last["value"])
     wall = time.perf_counter() - t0
     value = statistics.mean(vals)
@@ -509,8 +691,8 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": wl.name, "B": wl.B, "T_total": wl.T_total, "layers": wl.n_layers,
                    "n_reuse": wl.n_reuse, "w": wl.w, "c": wl.c, "L_max": wl.L_max},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": last["cores"], "kind": "oracle",
-                         "sample": last["sample"]},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "threads": 1, "kind": "oracle",
+                         "sample": last["sample"], "cpu_model": last["cpu_model"], "core": core},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -522,7 +704,9 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
-    ap.add_argument("--workload", choices=sorted(configs.ALL), default="llama_model")
+    ap.add_argument("--workload", choices=sorted(configs.ALL), default="qwen_128k")
+    ap.add_argument("--secondary", default="llama_model",
+                    help="a second workload timed in the same run (device time only); 'none' to skip")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-diagnostics", action="store_true", help="skip the adjacent-layer overlap measurement")
     ap.add_argument("--layers", type=int, default=0, help="keep only the first N layers (profiling)")
@@ -530,10 +714,13 @@ def main():
     ap.add_argument("--budget", type=int, default=0, help="L_max instead of the workload's (a sweep point)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-baseline-child", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.cpu_baseline_child:
+        run_cpu_baseline_child(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gpu(args)

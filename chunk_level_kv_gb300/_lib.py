@@ -8,6 +8,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libchunkkv.
 
 MAX_BATCH = 1024
 MAX_GATHER_LAYERS = 64
+PROBE_THREADS, PROBE_CHAINS = 256, 16          # CHUNKKV_PROBE_THREADS, CHUNKKV_PROBE_CHAINS
 
 STATUS = {
     0: "CHUNKKV_OK",
@@ -53,6 +54,7 @@ def _load():
         "chunkkv_set_phase_events": [pp, i32],
         "chunkkv_selftest_wait_timeout": [vp, sz, vp],
         "chunkkv_layer_overlap": [P, i32, vp, vp, vp, vp, vp],
+        "chunkkv_probe_ex2": [vp, i32, i32, vp],
     }
     for name, args in sigs.items():
         fn = getattr(lib, name)

@@ -11,7 +11,7 @@ from dataclasses import dataclass
 
 import torch
 
-from ._lib import BF16, F32, LIB, MAX_GATHER_LAYERS, STATUS, Params
+from ._lib import BF16, F32, LIB, MAX_GATHER_LAYERS, PROBE_CHAINS, PROBE_THREADS, STATUS, Params
 
 _DT = {torch.float32: F32, torch.bfloat16: BF16}
 
@@ -168,6 +168,16 @@ def chunkkv_selftest_wait_timeout(ws) -> None:
            LIB.chunkkv_selftest_wait_timeout(_ptr(ws), ws.numel() * ws.element_size(), _stream(ws.device)))
 
 
+def chunkkv_probe_ex2(sink, blocks: int, iters: int) -> int:
+    """Exponential-unit throughput probe on the current stream: launches `blocks` CTAs whose threads
+    evaluate `iters` rounds of independent base-2 exponentials (the scoring kernels' instruction).
+    sink: float32 device tensor of at least blocks * PROBE_THREADS elements.  Returns the number of
+    exponentials the launch evaluates (time it with events)."""
+    assert sink.numel() >= blocks * PROBE_THREADS and sink.dtype == torch.float32
+    _check("chunkkv_probe_ex2", LIB.chunkkv_probe_ex2(_ptr(sink), blocks, iters, _stream(sink.device)))
+    return blocks * PROBE_THREADS * PROBE_CHAINS * iters
+
+
 def chunkkv_status_check(ws) -> int:
     """Synchronises the current stream and reports a device-side wait that gave up (raises)."""
     code = ctypes.c_int32()
@@ -217,7 +227,7 @@ def compress_layers(q_win, k, v, cu_seqlens, *, Hq: int, Hkv: int, w: int, c: in
 __all__ = [
     "ChunkKVError", "CompressResult", "Params", "MAX_GATHER_LAYERS", "PHASES", "PHASE_EVENTS",
     "chunkkv_compress_layers", "chunkkv_gather", "chunkkv_launch_count", "chunkkv_layer_overlap",
-    "chunkkv_out_capacity", "chunkkv_score", "chunkkv_score_noalloc", "chunkkv_score_path", "chunkkv_select",
-    "chunkkv_selftest_wait_timeout", "chunkkv_set_phase_events", "chunkkv_status_check",
+    "chunkkv_out_capacity", "chunkkv_probe_ex2", "chunkkv_score", "chunkkv_score_noalloc", "chunkkv_score_path",
+    "chunkkv_select", "chunkkv_selftest_wait_timeout", "chunkkv_set_phase_events", "chunkkv_status_check",
     "chunkkv_workspace_size", "compress_layers", "make_params", "params_for",
 ]

@@ -28,7 +28,10 @@
 namespace chunkkv {
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;    // 16 MiB
+// the size the header states (CHUNKKV_NOALLOC_SCRATCH_BYTES), so that the limit
+// this file enforces is the documented one
+constexpr size_t kNoAllocScratchBytes = CHUNKKV_NOALLOC_SCRATCH_BYTES;
+static_assert(kNoAllocScratchBytes == (size_t(16) << 20), "16 MiB of static scratch");
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];

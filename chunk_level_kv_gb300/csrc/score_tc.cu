@@ -70,6 +70,7 @@ constexpr int kMaxGroups = 32;
 
 struct TcGeom {
   int32_t B, Hkv, wG, MT, cpu, ku;
+  int32_t c;                         // chunk size (the instances with C = 0 read it here)
   int32_t w;                         // window length (for the causal-window limit)
   int32_t G;                         // query heads per KV head
   int32_t q_direct;                  // 1: window rows read from Q_w itself (maps.q[group]), 0: packed (maps.q[0])
@@ -249,6 +250,22 @@ __device__ __forceinline__ bool wait_bar(const Ctl& ctl, uint32_t bar, uint32_t 
   }
 }
 
+// Wait for a phase of an asynchronous operation that this CTA started (a TMA copy
+// or a commit of its MMAs) after the CTA gave up: unlike wait_bar it ignores the
+// abort flag, since the point is to let that operation land before the shared
+// memory and TMEM it writes are released.  Bounded by `limit` cycles; returns
+// false if the phase did not complete in time.
+__device__ __forceinline__ bool drain_phase(uint32_t bar, uint32_t parity, long long limit) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity))
+    if (clock64() - t0 > limit) return false;
+  return true;
+}
+
+// Cycles a drain waits for one phase (about 50 ms at 2 GHz; a TMA copy or an MMA
+// normally lands within microseconds).
+constexpr long long kDrainCycles = 100000000LL;
+
 // ---------------------------------------------------------------- softmax side
 // Per-row state of the item being processed.
 struct RowState {
@@ -262,11 +279,11 @@ struct RowState {
 // exponents, two MUFU ex2 evaluate them and one packed add accumulates them; the
 // pair's two lanes are folded when a chunk ends (compile-time positions).  bin
 // points at bins[(gu*cpu + q)*wG + row], q being the unit-local chunk that holds
-// the tile's column 0.
+// the tile's column 0.  C = 1 (token-level chunks) stores every column as a bin.
 template <int C, int PH, int SEG, bool MASK>
 __device__ __forceinline__ void tile_seg(const uint32_t (&r)[16], float2 alpha2, RowState& s, bin_t* bin, int wG,
                                          int valid, bool write, uint64_t pol) {
-  static_assert(C >= 2, "pairs hold at most one chunk end");
+  static_assert(C >= 1, "compile-time chunk sizes");
   float2 acc = s.carry;
 #pragma unroll
   for (int p = 0; p < 8; ++p) {
@@ -278,7 +295,13 @@ __device__ __forceinline__ void tile_seg(const uint32_t (&r)[16], float2 alpha2,
       e.x = (c0 < valid) ? e.x : 0.f;
       e.y = (c0 + 1 < valid) ? e.y : 0.f;
     }
-    if ((PH + c0 + 1) % C == 0) {               // a chunk ends at the pair's first column
+    if constexpr (C == 1) {
+      if (write) {
+        st_keep(bin + (size_t)c0 * wG, e.x, pol);
+        st_keep(bin + (size_t)(c0 + 1) * wG, e.y, pol);
+      }
+      s.l += e.x + e.y;
+    } else if ((PH + c0 + 1) % C == 0) {        // a chunk ends at the pair's first column
       const float bsum = (acc.x + acc.y) + e.x;
       if (write) st_keep(bin + (size_t)((PH + c0 + 1) / C - 1) * wG, bsum, pol);
       s.l += bsum;
@@ -305,31 +328,85 @@ __device__ __forceinline__ void tile_segs(const uint32_t (&r)[kN / 16][16], floa
   }
 }
 
+// The same for a chunk size known only at run time (c >= 2): `pos` columns of
+// the chunk holding column 0 precede the tile, and the chunk ends are found by
+// counting (the count is the same in every lane, so the branches are uniform).
+template <bool MASK>
+__device__ __forceinline__ void tile_cols_rt(const uint32_t (&r)[kN / 16][16], float2 alpha2, RowState& s, bin_t* bin,
+                                             int wG, int valid, bool write, uint64_t pol, int c, int pos) {
+  float2 acc = s.carry;
+#pragma unroll
+  for (int sg = 0; sg < kN / 16; ++sg) {
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+      const int c0 = sg * 16 + 2 * p;
+      const float2 x = make_float2(__uint_as_float(r[sg][2 * p]), __uint_as_float(r[sg][2 * p + 1]));
+      const float2 t = __ffma2_rn(x, alpha2, s.negR);
+      float2 e = make_float2(ex2(t.x), ex2(t.y));
+      if (MASK) {
+        e.x = (c0 < valid) ? e.x : 0.f;
+        e.y = (c0 + 1 < valid) ? e.y : 0.f;
+      }
+      if (pos + 1 == c) {                         // a chunk ends at the pair's first column
+        const float bsum = (acc.x + acc.y) + e.x;
+        if (write) st_keep(bin, bsum, pol);
+        bin += wG;
+        s.l += bsum;
+        acc = make_float2(0.f, e.y);
+        pos = 1;
+      } else if (pos + 2 == c) {                  // a chunk ends at the pair's second column
+        acc = __fadd2_rn(acc, e);
+        const float bsum = acc.x + acc.y;
+        if (write) st_keep(bin, bsum, pol);
+        bin += wG;
+        s.l += bsum;
+        acc = make_float2(0.f, 0.f);
+        pos = 0;
+      } else {
+        acc = __fadd2_rn(acc, e);
+        pos += 2;
+      }
+    }
+  }
+  s.carry = acc;
+}
+
 // One tile of kN columns: the whole row segment is loaded from TMEM first
 // (kN/16 x16 loads, one wait), so the column pairs are independent work that
 // the scheduler can interleave freely.
 template <int C, int PH, bool MASK>
 __device__ __forceinline__ void tile_phase(uint32_t taddr, float2 alpha, RowState& s, bin_t* bin, int wG, int valid,
-                                           bool write, uint64_t pol) {
+                                           bool write, uint64_t pol, int c, int ph) {
   uint32_t r[kN / 16][16];
 #pragma unroll
   for (int sg = 0; sg < kN / 16; ++sg) tmem_ld16(taddr + 16 * sg, r[sg]);
 #pragma unroll
   for (int sg = 0; sg < kN / 16; ++sg) tmem_wait16(r[sg]);
-  tile_segs<C, PH, 0, MASK>(r, alpha, s, bin, wG, valid, write, pol);
+  if constexpr (C == 0)
+    tile_cols_rt<MASK>(r, alpha, s, bin, wG, valid, write, pol, c, ph);
+  else
+    tile_segs<C, PH, 0, MASK>(r, alpha, s, bin, wG, valid, write, pol);
 }
 
+// C > 0: the tile phases ph = (t * kN) mod C are the multiples of gcd(kN, C)
+// below C, each a compile-time instance; C = 0 (chunk size c known at run time)
+// passes the phase on.
 template <int C, int PH = 0>
 __device__ __forceinline__ void tile_dispatch(int ph, bool mask, uint32_t taddr, float2 alpha, RowState& s, bin_t* bin,
-                                              int wG, int valid, bool write, uint64_t pol) {
-  if constexpr (PH < C) {
+                                              int wG, int valid, bool write, uint64_t pol, int c) {
+  if constexpr (C == 0) {
+    if (mask)
+      tile_phase<0, 0, true>(taddr, alpha, s, bin, wG, valid, write, pol, c, ph);
+    else
+      tile_phase<0, 0, false>(taddr, alpha, s, bin, wG, valid, write, pol, c, ph);
+  } else if constexpr (PH < C) {
     if (ph == PH) {
       if (mask)
-        tile_phase<C, PH, true>(taddr, alpha, s, bin, wG, valid, write, pol);
+        tile_phase<C, PH, true>(taddr, alpha, s, bin, wG, valid, write, pol, c, ph);
       else
-        tile_phase<C, PH, false>(taddr, alpha, s, bin, wG, valid, write, pol);
+        tile_phase<C, PH, false>(taddr, alpha, s, bin, wG, valid, write, pol, c, ph);
     } else {
-      tile_dispatch<C, PH + gcd_c(kN, C)>(ph, mask, taddr, alpha, s, bin, wG, valid, write, pol);
+      tile_dispatch<C, PH + gcd_c(kN, C)>(ph, mask, taddr, alpha, s, bin, wG, valid, write, pol, c);
     }
   }
 }
@@ -387,7 +464,8 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
   uint64_t* t_full = k_empty + kStagesK;                       // [kStagesT]
   uint64_t* t_empty = t_full + kStagesT;                       // [kStagesT]
   uint64_t* qt_done = t_empty + kStagesT;                      // [1] MMAs of the old TMEM window tile / its copy done
-  uint32_t* tmem_slot = (uint32_t*)(qt_done + 1);
+  uint64_t* drained = qt_done + 1;                             // [1] all MMAs done (teardown after a give-up)
+  uint32_t* tmem_slot = (uint32_t*)(drained + 1);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -396,6 +474,7 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
     for (int i = 0; i < kStagesK; ++i) { mbar_init(smem_u32(&k_full[i]), 1); mbar_init(smem_u32(&k_empty[i]), 1); }
     for (int i = 0; i < kStagesT; ++i) { mbar_init(smem_u32(&t_full[i]), 1); mbar_init(smem_u32(&t_empty[i]), 128); }
     mbar_init(smem_u32(&qt_done[0]), 1);
+    mbar_init(smem_u32(drained), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&maps.q[0]) : "memory");
@@ -411,12 +490,15 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const Ctl ctl{err, abort_flag, g.timeout};
+  // copies issued by the producer (key tiles, window-row tiles): after a give-up
+  // the teardown waits for the last phase armed on each of their barriers
+  uint32_t kc = 0, qc = 0;
+  const int cc = C > 0 ? C : g.c;                      // chunk size
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
       pdl_wait();                                      // the packed window rows come from the previous launch
-      uint32_t kc = 0, qc = 0;
       int qkey = -1;                                   // (group, sequence, head, M tile) of the loaded Q
       // keys: normal priority, since the CTAs of the other M tiles of the same
       // (unit, head) read each key tile too (evict-first cost re-reads from HBM)
@@ -459,7 +541,7 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
-      uint32_t kc = 0, qc = 0, tc = 0, qtc = 0;
+      uint32_t kc = 0, qc = 0, tc = 0, qtc = 0;        // this warp's own counts of the same phases
       int qkey = -1;
       const uint32_t qaddr = smem_u32(sQ);
       for (int item = blockIdx.x; item < g.n_items && !*abort_flag; item += gridDim.x) {
@@ -557,10 +639,10 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
             R = tile_max(taddr, valid) * g.alpha + kBinShift;      // shifted reference (bin scale)
             s.negR = make_float2(-R, -R);
           }
-          const int ph = (t * kN) % C;
-          const int q = (t * kN) / C;
+          const int ph = (t * kN) % cc;
+          const int q = (t * kN) / cc;
           const RowState before = s;
-          tile_dispatch<C>(ph, mask, taddr, alpha2, s, ubins + (size_t)q * wg, wg, valid, write, bpol);
+          tile_dispatch<C>(ph, mask, taddr, alpha2, s, ubins + (size_t)q * wg, wg, valid, write, bpol, cc);
           // every bin is at most the row sum: one test per tile catches any value
           // that outgrew the reference (and inf / NaN)
           const bool over = !(s.l <= kBig);
@@ -579,7 +661,7 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
             s.carry = make_float2(s.carry.x * f, s.carry.y * f);
             R = R2;
             s.negR = make_float2(-R2, -R2);
-            tile_dispatch<C>(ph, mask, taddr, alpha2, s, ubins + (size_t)q * wg, wg, valid, write, bpol);
+            tile_dispatch<C>(ph, mask, taddr, alpha2, s, ubins + (size_t)q * wg, wg, valid, write, bpol, cc);
           }
         }
         tc_fence_before();
@@ -589,9 +671,9 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
       if (!ok) break;
       if (warp_live && write) {
         // the item ended inside a chunk (last, partial chunk of the sequence)
-        if ((ntile * kN) % C != 0) {
+        if ((ntile * kN) % cc != 0) {
           const float cs = s.carry.x + s.carry.y;
-          const int ch = (ntile * kN) / C;
+          const int ch = (ntile * kN) / cc;
           if (ch < g.cpu) ubins[(size_t)ch * g.wG] = bin_encode(cs);
           s.l += cs;
         }
@@ -603,15 +685,35 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
 
   // ------------------------------------------------ teardown
   pdl_trigger();
-  if (*abort_flag) {
-    // let copies and MMAs already in flight land before the shared memory and TMEM go away
-    const long long t0 = clock64();
-    while (clock64() - t0 < 200000) {
-    }
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (*abort_flag) {
+    // A role gave up: copies and MMAs this CTA started may still be in flight, and
+    // they must land before its shared memory and TMEM are released.  The producer
+    // waits for the last phase it armed on every key stage and on the window-row
+    // stage; the MMA issuer commits everything it issued to one more barrier and
+    // waits for it.  Only if one of those bounded waits runs out does the CTA fall
+    // back to a fixed pause.
+    bool landed = true;
+    if (warp == 0 && lane == 0) {
+      for (uint32_t i = kc > kStagesK ? kc - kStagesK : 0; i < kc; ++i)
+        landed &= drain_phase(smem_u32(&k_full[i % kStagesK]), (i / kStagesK) & 1, kDrainCycles);
+      if (qc > 0) landed &= drain_phase(smem_u32(&q_full[0]), (qc - 1) & 1, kDrainCycles);
+    }
+    if (warp == 1 && lane == 0) {
+      tc_commit(smem_u32(drained));
+      landed &= drain_phase(smem_u32(drained), 0, kDrainCycles);
+    }
+    if (!landed) {
+      const long long t0 = clock64();
+      while (clock64() - t0 < kDrainCycles) {
+      }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  }
   if (warp == 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
 }
@@ -649,22 +751,39 @@ __global__ void pack_q_kernel(const __grid_constant__ PackArgs pa, ScoreGeom g, 
   pdl_trigger();
 }
 
-// Failure-path self test: one thread waits, through the same bounded wait as the
-// scoring kernel's roles, on an mbarrier phase that nothing completes.  The wait
-// runs out after `timeout` clock64 cycles, records kDevTimeoutSelftest in the
-// workspace error word and raises the CTA abort flag; the kernel then returns.
+// Failure-path self test: one thread starts a real asynchronous copy (64 bytes
+// of the workspace header, bytes 128..191, into shared memory by the bulk-copy
+// engine), then waits, through the same bounded wait as the scoring kernel's
+// roles, on an mbarrier phase that nothing completes.  The wait runs out after
+// `timeout` clock64 cycles, records kDevTimeoutSelftest in the workspace error
+// word and raises the CTA abort flag; the thread then drains the copy the way
+// the scoring kernel's teardown does (a bounded wait on the copy's own barrier
+// phase) and writes what landed to header bytes 64..127, so that a caller can
+// see that the drain waited for the copy before the kernel returned.
 __global__ void wait_selftest_kernel(int32_t* err, long long timeout) {
   __shared__ uint64_t bar;
+  __shared__ uint64_t copied;
   __shared__ int abort_flag;
+  __shared__ __align__(16) uint8_t buf[64];
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&bar), 1);                 // one arrival expected, none made
+    mbar_init(smem_u32(&copied), 1);
     abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
   if (threadIdx.x == 0) {
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(err) + 128;
+    mbar_expect_tx(smem_u32(&copied), 64);
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], 64, [%2];"
+        ::"r"(smem_u32(buf)), "l"((uint64_t)src), "r"(smem_u32(&copied)) : "memory");
     const Ctl ctl{err, (volatile int*)&abort_flag, timeout};
     if (wait_bar(ctl, smem_u32(&bar), 0, kDevTimeoutSelftest)) atomicExch(err, 0x7FFFFFFF);   // must not happen
+    if (drain_phase(smem_u32(&copied), 0, kDrainCycles)) {
+      uint8_t* dst = reinterpret_cast<uint8_t*>(err) + 64;
+      for (int i = 0; i < 64; ++i) dst[i] = buf[i];
+    }
   }
 }
 
@@ -687,7 +806,7 @@ EncodeFn encode_fn() {
 
 struct DeviceInfo {
   int sms = 0;
-  bool attr_set[40] = {};
+  bool attr_set[64] = {};                       // per kernel instance (launch_c's slot)
 };
 
 DeviceInfo& device_info(int dev) {
@@ -724,28 +843,34 @@ cudaError_t launch_c(const TcGeom& tg, const TcMaps& maps, const SeqTable& st, f
 
 // Instances per chunk size: the causal window (any w*G), and without it w*G of
 // 128, 256 and 448 at compile time (LLaMA / Mistral / Qwen-shaped GQA groups
-// with 32- and 64-query windows) or any other w*G at run time.
+// with 32- and 64-query windows) or any other w*G at run time.  `slot` numbers
+// the chunk size's five instances for the one-time shared-memory attribute.
 template <int C>
 cudaError_t launch_causal(bool causal, const TcGeom& tg, const TcMaps& maps, const SeqTable& st, float* rl,
                           bin_t* bins, int32_t* err, int slot, cudaStream_t s) {
-  if (causal) return launch_c<C, true, 0>(tg, maps, st, rl, bins, err, slot + 8, s);
+  if (causal) return launch_c<C, true, 0>(tg, maps, st, rl, bins, err, 5 * slot + 1, s);
   switch (tg.wG) {
-    case 128: return launch_c<C, false, 128>(tg, maps, st, rl, bins, err, slot + 16, s);
-    case 256: return launch_c<C, false, 256>(tg, maps, st, rl, bins, err, slot + 24, s);
-    case 448: return launch_c<C, false, 448>(tg, maps, st, rl, bins, err, slot + 32, s);
-    default: return launch_c<C, false, 0>(tg, maps, st, rl, bins, err, slot, s);
+    case 128: return launch_c<C, false, 128>(tg, maps, st, rl, bins, err, 5 * slot + 2, s);
+    case 256: return launch_c<C, false, 256>(tg, maps, st, rl, bins, err, 5 * slot + 3, s);
+    case 448: return launch_c<C, false, 448>(tg, maps, st, rl, bins, err, 5 * slot + 4, s);
+    default: return launch_c<C, false, 0>(tg, maps, st, rl, bins, err, 5 * slot, s);
   }
 }
 
-constexpr int kSupportedC[] = {3, 4, 5, 8, 10, 16, 20, 30};
-
-int c_slot(int c) {
-  for (int i = 0; i < (int)(sizeof(kSupportedC) / sizeof(int)); ++i)
-    if (kSupportedC[i] == c) return i;
-  return -1;
+// Token-level chunks (c = 1) and chunk sizes without an instance of their own
+// (C = 0: c read at run time): the causal window or any w*G.
+template <int C>
+cudaError_t launch_any_wg(bool causal, const TcGeom& tg, const TcMaps& maps, const SeqTable& st, float* rl,
+                          bin_t* bins, int32_t* err, int slot, cudaStream_t s) {
+  if (causal) return launch_c<C, true, 0>(tg, maps, st, rl, bins, err, 5 * slot + 1, s);
+  return launch_c<C, false, 0>(tg, maps, st, rl, bins, err, 5 * slot, s);
 }
 
 int lcm_i(int a, int b) { return a / gcd_c(a, b) * b; }
+
+// Largest chunk size the tensor-core path takes: its units are whole tiles and
+// whole chunks, lcm(80, c) keys at least.
+constexpr int kMaxTcChunk = 4096;
 
 }  // namespace tc
 
@@ -753,7 +878,9 @@ void tc_plan(Plan& pl) {
   pl.use_tc = 0;
   pl.tc_mt = 0;
   pl.tc_base_chunks = 0;
-  if (!(pl.elt == 2 && pl.d == tc::kD && pl.wG > 0 && tc::c_slot(pl.c) >= 0)) return;
+  // bf16 keys of head dimension 128 and any chunk size up to kMaxTcChunk (larger
+  // chunks would make a whole-tile unit very long); the rest runs the SIMT kernel
+  if (!(pl.elt == 2 && pl.d == tc::kD && pl.wG > 0 && pl.c >= 1 && pl.c <= tc::kMaxTcChunk)) return;
   // Units are whole tiles and whole chunks: multiples of lcm(80, c) keys.  The
   // multiplier is chosen by the planner (balance over the persistent grid).
   pl.use_tc = 1;
@@ -856,6 +983,7 @@ cudaError_t launch_score_tc(const Plan& pl, const ScoreGeom& g, const SeqTable& 
     tg.MT = MT;
     tg.cpu = pl.cpu;
     tg.ku = pl.ku;
+    tg.c = pl.c;
     tg.w = g.w;
     tg.G = pl.G;
     tg.q_direct = direct ? 1 : 0;
@@ -867,16 +995,21 @@ cudaError_t launch_score_tc(const Plan& pl, const ScoreGeom& g, const SeqTable& 
     tg.timeout = 4000000000LL;     // about two seconds of clock64 cycles per wait
     float* rlg = (float*)((char*)rl + g0 * slot_bytes);
     bin_t* bg = (bin_t*)((char*)bins + g0 * slot_bytes);
+    // compile-time instances (the chunk ends of every tile phase are constants) for
+    // the common chunk sizes; any other c >= 2 runs the C = 0 instance
+    const bool causal = g.causal != 0;
     cudaError_t e = cudaErrorNotSupported;
     switch (pl.c) {
-      case 3: e = tc::launch_causal<3>(g.causal != 0, tg, maps, st, rlg, bg, err, 0, s); break;
-      case 4: e = tc::launch_causal<4>(g.causal != 0, tg, maps, st, rlg, bg, err, 1, s); break;
-      case 5: e = tc::launch_causal<5>(g.causal != 0, tg, maps, st, rlg, bg, err, 2, s); break;
-      case 8: e = tc::launch_causal<8>(g.causal != 0, tg, maps, st, rlg, bg, err, 3, s); break;
-      case 10: e = tc::launch_causal<10>(g.causal != 0, tg, maps, st, rlg, bg, err, 4, s); break;
-      case 16: e = tc::launch_causal<16>(g.causal != 0, tg, maps, st, rlg, bg, err, 5, s); break;
-      case 20: e = tc::launch_causal<20>(g.causal != 0, tg, maps, st, rlg, bg, err, 6, s); break;
-      case 30: e = tc::launch_causal<30>(g.causal != 0, tg, maps, st, rlg, bg, err, 7, s); break;
+      case 1: e = tc::launch_any_wg<1>(causal, tg, maps, st, rlg, bg, err, 8, s); break;
+      case 3: e = tc::launch_causal<3>(causal, tg, maps, st, rlg, bg, err, 0, s); break;
+      case 4: e = tc::launch_causal<4>(causal, tg, maps, st, rlg, bg, err, 1, s); break;
+      case 5: e = tc::launch_causal<5>(causal, tg, maps, st, rlg, bg, err, 2, s); break;
+      case 8: e = tc::launch_causal<8>(causal, tg, maps, st, rlg, bg, err, 3, s); break;
+      case 10: e = tc::launch_causal<10>(causal, tg, maps, st, rlg, bg, err, 4, s); break;
+      case 16: e = tc::launch_causal<16>(causal, tg, maps, st, rlg, bg, err, 5, s); break;
+      case 20: e = tc::launch_causal<20>(causal, tg, maps, st, rlg, bg, err, 6, s); break;
+      case 30: e = tc::launch_causal<30>(causal, tg, maps, st, rlg, bg, err, 7, s); break;
+      default: e = tc::launch_any_wg<0>(causal, tg, maps, st, rlg, bg, err, 9, s); break;
     }
     if (e != cudaSuccess) return e;
   }

@@ -231,15 +231,35 @@ chunkkv_status chunkkv_layer_overlap(const chunkkv_params* p, int32_t n_lists, c
 
 /*
  * Self test of the failure path (a test aid; no counterpart in the pages).
- * Launches one thread that waits, through the same bounded wait as the
+ * Launches one thread that first starts an asynchronous bulk copy of ws bytes
+ * 128..191 into shared memory, then waits, through the same bounded wait as the
  * tensor-core scoring kernel, on a barrier that nothing completes.  The wait
- * gives up after about a millisecond, records device code 0x1FF in the error
- * word of ws and the kernel returns, leaving the context usable; a following
- * chunkkv_status_check(ws, ...) then returns CHUNKKV_ERR_TIMEOUT with that code.
- *   ws: device workspace of at least 256 bytes (its error word is written).
+ * gives up after about a millisecond and records device code 0x1FF in the error
+ * word of ws; the thread then drains its copy as the scoring kernel's teardown
+ * does after a give-up (a bounded wait on the copy's own barrier phase, never a
+ * fixed pause) and writes the 64 bytes that landed to ws bytes 64..127.  The
+ * kernel returns and leaves the context usable; a following
+ * chunkkv_status_check(ws, ...) returns CHUNKKV_ERR_TIMEOUT with that code.
+ *   ws: device workspace of at least 256 bytes (bytes 0..3 and 64..127 are written).
  * Returns CHUNKKV_ERR_INVALID_ARG for a NULL, misaligned or too small ws.
  */
 chunkkv_status chunkkv_selftest_wait_timeout(void* ws, size_t ws_bytes, chunkkv_stream_t stream);
+
+/*
+ * Throughput probe of the exponential unit (a measurement aid; no counterpart in
+ * the pages).  The scoring kernels evaluate one base-2 exponential
+ * (ex2.approx.ftz.f32) per window logit; this call launches `blocks` CTAs of
+ * CHUNKKV_PROBE_THREADS threads, each thread evaluating `iters` rounds of
+ * CHUNKKV_PROBE_CHAINS independent exponentials of that instruction, i.e.
+ * blocks * CHUNKKV_PROBE_THREADS * CHUNKKV_PROBE_CHAINS * iters of them in all.
+ * Timing the call (events on `stream`) gives the exponential rate that bounds
+ * the scoring phase.
+ *   sink: device, blocks * CHUNKKV_PROBE_THREADS floats (one result per thread).
+ * Returns CHUNKKV_ERR_INVALID_ARG for a NULL sink or a non-positive count.
+ */
+#define CHUNKKV_PROBE_THREADS 256
+#define CHUNKKV_PROBE_CHAINS 16
+chunkkv_status chunkkv_probe_ex2(float* sink, int32_t blocks, int32_t iters, chunkkv_stream_t stream);
 
 /* Static description of a status code. */
 const char* chunkkv_status_string(chunkkv_status s);

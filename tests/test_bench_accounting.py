@@ -32,7 +32,7 @@ def test_llama3_32k_amounts(monkeypatch, head):
     assert int(counts[0, 0, 0]) == 655 * 10 + 32
     monkeypatch.setattr(bench, "head_path", lambda wl, groups: head)
     ms = {"score": 0.2, "finalize": 0.05, "gather": 0.3}
-    score, fin, gather = bench.phase_rooflines(wl, counts, ms, PEAKS, "measured", 1)
+    (score, fin, gather), _ = bench.phase_rooflines(wl, counts, ms, PEAKS, "measured", 1)
     assert score["algorithmic_bytes"] == 16 * 32768 * 8 * 128 * 2                 # 1.074 GB
     assert score["bound"] == "hbm"                  # 137 GF take 80 us at the tensor roof, 1.07 GB 159 us
     assert fin["algorithmic_bytes"] == 16 * 3277 * 8 * 32 * 4 * 2                  # 107 MB
@@ -50,7 +50,7 @@ def test_qwen2_128k_scoring_is_tensor_bound(monkeypatch):
     assert (wl.n_layers, wl.n_reuse, wl.T_total, wl.Hkv, wl.w, wl.G, wl.c) == (28, 2, 131072, 4, 64, 7, 10)
     monkeypatch.setattr(bench, "head_path", lambda wl, groups: False)
     ms = {"score": 0.8, "finalize": 0.1, "gather": 0.25}
-    score, fin, gather = bench.phase_rooflines(wl, _full_counts(wl), ms, PEAKS, "measured", 1)
+    (score, fin, gather), _ = bench.phase_rooflines(wl, _full_counts(wl), ms, PEAKS, "measured", 1)
     flops = 2.0 * 14 * 64 * 7 * 131072 * 4 * 128                                   # 842 GF
     assert score["bound"] == "tensor" and score["algorithmic_flops"] == flops
     assert flops / (PEAKS["bf16_tflops_sustained"] * 1e12) > score["algorithmic_bytes"] / (PEAKS["hbm_gbs"] * 1e9)
@@ -68,8 +68,28 @@ def test_portable_path_is_reported_against_hbm(monkeypatch):
     wl = configs.llama_model().with_params(n_layers=2)
     monkeypatch.setattr(bench, "head_path", lambda wl, groups: False)
     ms = {"score": 1.0, "finalize": 0.1, "gather": 0.1}
-    score = bench.phase_rooflines(wl, _full_counts(wl), ms, PEAKS, "measured", 0)[0]
+    score = bench.phase_rooflines(wl, _full_counts(wl), ms, PEAKS, "measured", 0)[0][0]
     assert score["kernel"] == "score_simt_kernel" and score["bound"] == "hbm"
+
+
+@pytest.mark.parametrize("rate,bound", [(10.0e12, "tensor"), (5.0e12, "sfu")])
+def test_exponential_roof_of_the_128k_scoring(monkeypatch, rate, bound):
+    # one base-2 exponential per logit: 14 scoring layers x 448 window rows x 131072 keys x 4 KV heads
+    # (3.29 G).  At 10 T exp/s they take 329 us, under the 491 us of the sustained tensor roof; at
+    # 5 T exp/s they take 658 us and the exponential unit binds.
+    wl = configs.qwen_128k()
+    monkeypatch.setattr(bench, "head_path", lambda wl, groups: False)
+    ms = {"score": 0.8, "finalize": 0.1, "gather": 0.25}
+    (score, _, _), every = bench.phase_rooflines(wl, _full_counts(wl), ms, PEAKS, "measured", 1,
+                                                 {"exp_per_s": rate})
+    exps = 14 * 448 * 131072 * 4
+    sfu = next(r for r in every if r["bound"] == "sfu")
+    assert sfu["algorithmic_exps"] == exps and sfu["unit"] == "Gexp/s"
+    assert sfu["ideal_ms"] == pytest.approx(exps / rate * 1e3, abs=1e-5)
+    assert sfu["achieved"] == pytest.approx(exps / 0.8e-3 / 1e9, abs=0.006)
+    assert sfu["frac"] == pytest.approx(exps / 0.8e-3 / rate, abs=1e-4)
+    assert [r["bound"] for r in every] == ["hbm", "tensor", "sfu"]
+    assert score["bound"] == bound and score["ideal_ms"] == max(r["ideal_ms"] for r in every)
 
 
 def test_job_rate_counts_every_rank():

@@ -81,3 +81,14 @@ def test_reference_arm_prints_one_json_line():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "GB/s"
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
+    assert d["cpu_baseline"]["cores"] == 1 and d["cpu_baseline"]["threads"] == 1 and d["cpu_baseline"]["cpu_model"]
+
+
+def test_cpu_baseline_leg_runs_the_oracle_on_one_core():
+    # the GPU arm's cpu_baseline leg: a child process with every BLAS / OpenMP pool at one thread,
+    # pinned to one core, timing the oracle on the first scoring layer of the same workload
+    import bench
+    args = bench.main.__globals__["argparse"].Namespace(workload="tiny", chunk=0, budget=0)
+    d = bench.cpu_baseline(args, budget_s=0.5)
+    assert d["kind"] == "oracle" and d["value"] > 0 and d["cores"] == 1 and d["threads"] == 1
+    assert "scoring layer 0" in d["sample"]

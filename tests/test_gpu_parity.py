@@ -80,11 +80,28 @@ def test_tiny_fp32_exact(ckv):
     (5000, 10, 48, 40, 8, 500),      # window rows 240: two M tiles in one CTA, the second partly padding
     (2500, 5, 40, 32, 4, 300),       # window rows 320: three M tiles, the last CTA's second tile all padding
     (3333, 16, 64, 16, 2, 512),      # window rows 512: four full M tiles, c = 16
+    (2345, 15, 32, 32, 8, 450),      # c = 15 (the notes' ablation): chunk size read at run time
+    (1999, 2, 32, 28, 4, 200),       # c = 2, window rows 224: a chunk end in every column pair
+    (4100, 100, 16, 16, 4, 1000),    # c = 100: chunks spanning tiles, a whole-tile unit of 400 keys
+    (3000, 1, 32, 28, 4, 256),       # token-level selection on 224 window rows (two M tiles)
 ])
 def test_bf16_shapes(ckv, T, c, w, Hq, Hkv, L_max):
     wl = configs.llama_layer().with_params(seqlens=(T,), c=c, w=w, Hq=Hq, Hkv=Hkv, L_max=L_max,
                                            name=f"bf16_T{T}_c{c}_w{w}_G{Hq // Hkv}")
+    p, keep = ckv.make_params(cu_seqlens=wl.cu_seqlens, Hq=wl.Hq, Hkv=wl.Hkv, d=wl.d, w=wl.w, c=wl.c,
+                              L_max=wl.L_max, dtype=torch.bfloat16)
+    assert ckv.chunkkv_score_path(p) == 1          # every chunk size up to 4096 on the tensor cores
     run_and_check(ckv, wl)
+
+
+@pytest.mark.parametrize("c", [1, 7, 15])
+def test_tensor_core_chunk_sizes_on_a_ragged_batch(ckv, c):
+    # token-level chunks and chunk sizes read at run time, over ragged sequences (empty, shorter than
+    # the window, shorter than one tile, several units) and two reuse groups, with the causal window too
+    wl = configs.mistral_ragged().with_params(seqlens=(1000, 0, 20, 2500, 7, 333), B=6, n_layers=3,
+                                              L_max=256, c=c, name=f"ragged_tc_c{c}")
+    run_and_check(ckv, wl)
+    run_and_check(ckv, wl.with_params(name=f"ragged_tc_c{c}_causal"), causal=True)
 
 
 def test_ragged_batch_with_degenerate_sequences(ckv):
@@ -200,10 +217,15 @@ def test_bounded_wait_gives_up_and_reports(ckv):
     from chunk_level_kv_gb300._lib import LIB
     from chunk_level_kv_gb300.api import _stream
     ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
+    pattern = torch.arange(64, dtype=torch.uint8, device=DEV) * 3 + 7
+    ws[128:192] = pattern                                 # what the self test copies asynchronously
     ckv.chunkkv_selftest_wait_timeout(ws)
     code = ctypes.c_int32()
     st = LIB.chunkkv_status_check(ctypes.c_void_p(ws.data_ptr()), _stream(ws.device), ctypes.byref(code))
     assert st == 5 and code.value == 0x1FF                 # CHUNKKV_ERR_TIMEOUT, the self-test site
+    # after giving up, the kernel waited for its own copy to land before it returned (the teardown
+    # drain of the scoring kernel): the copied bytes are what it wrote back
+    assert torch.equal(ws[64:128], pattern)
     assert ckv.chunkkv_status_check(ws) == 0              # the word was cleared ...
     wl = configs.tiny()                                   # ... and the context still computes
     out, verdicts = run_and_check(ckv, wl)
@@ -504,7 +526,8 @@ def mistral_inputs():
 def test_tensor_core_path_is_selected_for_bf16_d128(ckv):
     # the shapes of the LLaMA / Mistral / Qwen workloads run the tcgen05 kernel
     for wl in (configs.llama_layer(), configs.llama_model(), configs.qwen_128k(),
-               configs.mistral_ragged(c=3), configs.mistral_ragged(c=30)):
+               configs.mistral_ragged(c=3), configs.mistral_ragged(c=30),
+               configs.llama_layer().with_params(c=1), configs.llama_layer().with_params(c=15)):
         p, keep = ckv.make_params(cu_seqlens=wl.cu_seqlens, Hq=wl.Hq, Hkv=wl.Hkv, d=wl.d, w=wl.w, c=wl.c,
                                   L_max=wl.L_max, dtype=torch.bfloat16)
         assert ckv.chunkkv_score_path(p) == 1, wl.name
