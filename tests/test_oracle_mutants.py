@@ -35,6 +35,8 @@ def _pin_calls(mod):
     for name, fn in sorted(vars(mod).items()):
         if not (name.startswith("test_") and callable(fn)):
             continue
+        if name.endswith("_full_size"):
+            continue               # the full-size needle pins repeat the 8K one at 10-30x the cost
         marks = [m for m in getattr(fn, "pytestmark", []) if m.name == "parametrize"]
         if not marks:
             calls.append((name, fn))

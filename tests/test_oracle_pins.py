@@ -208,6 +208,34 @@ def test_needle_spans_are_found_llama_layer():
                 assert sel & set(full), (h, s, e)
 
 
+@pytest.mark.parametrize("name", ["llama_model", "qwen_128k", "mistral_ragged"])
+def test_needle_spans_are_found_full_size(name):
+    # the same on the first layer of the 32K and 128K models and of the 16-sequence ragged batch:
+    # in every sequence and KV head, every needle span at least one chunk long contains a selected
+    # chunk (the heads run in parallel threads: numpy releases the interpreter lock in its loops)
+    from concurrent.futures import ThreadPoolExecutor
+    wl = getattr(configs, name)()
+    spans = gen.needle_spans(wl)
+    q, k, v = gen.make_layer(wl, 0, "cpu", spans=spans[0])
+    qf = q.float().numpy()
+    cu = wl.cu_seqlens
+    n_checked = 0
+    with ThreadPoolExecutor(max_workers=8) as ex:
+        for b in range(wl.B):
+            kf = k[cu[b]:cu[b + 1]].float().numpy()
+            T = cu[b + 1] - cu[b]
+            assert oracle.n_select(T, wl.c, wl.L_max) >= len(spans[0][b])
+            sels = ex.map(lambda h: set(oracle.chunkkv_head(oracle.group_window_rows(qf[b], h, wl.G), kf[:, h],
+                                                             wl.c, wl.w, wl.L_max)[1]), range(wl.Hkv))
+            for h, sel in enumerate(sels):
+                for (s, e) in spans[0][b]:
+                    full = [i for i in range(-(-s // wl.c), e // wl.c) if (i + 1) * wl.c <= e]
+                    if full:
+                        assert sel & set(full), (name, b, h, s, e)
+                        n_checked += 1
+    assert n_checked >= wl.B * wl.Hkv * 5
+
+
 def _layers(n_layers, T=40, Hkv=2, G=2, w=4, d=8, seed=0):
     rng = np.random.default_rng(seed)
     qs = [rng.normal(size=(1, w, Hkv * G, d)) for _ in range(n_layers)]
