@@ -40,6 +40,17 @@ form the rest supports):
       window query q (0 <= q < w) sits at sequence position T - w + q and sees
       only keys j <= T - w + q; a query whose position is negative (T < w) sees
       no key and adds nothing.
+  R12 Incremental compression during decoding (the notes keep the compressed
+      cache through decoding, §5.6; Kara §2 Eqs. (2)-(3) compress again when
+      the cache reaches its threshold).  A cache of one (sequence, KV head)
+      holds n_prev positions kept by earlier passes followed by n_new tokens
+      decoded since.  A pass re-scores only the new tail: the window rows
+      attend to every key of the cache (the softmax of Eq. (1) runs over all
+      n_prev + n_new keys), the tail is cut into chunks from its first token,
+      Algorithm 1 steps 2-6 run on the tail alone (k = floor(L / c) of its
+      chunks plus its last w tokens, L being the pass's budget for the tail),
+      and the kept tail positions are appended to the n_prev kept ones, which
+      stay as they are.
 """
 from __future__ import annotations
 
@@ -153,6 +164,25 @@ def chunkkv_head(rows: np.ndarray, keys: np.ndarray, c: int, w: int, L_max: int,
 def gather(x: np.ndarray, idx: np.ndarray) -> np.ndarray:
     """K' = index_select(K, indices) (ChunkKV §4.1 Algorithm 1 step 6)."""
     return x[idx]
+
+
+# ---------------------------------------------------------------- decoding (reading R12)
+
+def tail_key_scores(rows: np.ndarray, keys: np.ndarray, n_prev: int) -> np.ndarray:
+    """a_j of the tail keys j >= n_prev of a cache, each window row's softmax running over all of
+    the cache's keys (Kara §2 Eq. (1) over the whole cache; reading R12)."""
+    return key_scores(rows, keys)[n_prev:]
+
+
+def compress_tail_head(rows: np.ndarray, keys: np.ndarray, n_prev: int, c: int, w: int, L_tail: int):
+    """One incremental pass over the cache of one (sequence, KV head) (reading R12): the tail
+    [n_prev, T) is chunked from its first token and Algorithm 1 steps 2-6 (ChunkKV §4.1) select
+    from it with budget L_tail.  Returns (A over the tail's chunks, selected tail chunks, the
+    appended cache positions n_prev + i, ascending)."""
+    n_new = keys.shape[0] - n_prev
+    A = chunk_scores(tail_key_scores(rows, keys, n_prev), c)
+    sel = top_chunks(A, n_select(n_new, c, L_tail))
+    return A, sel, n_prev + kept_indices(sel, n_new, c, w)
 
 
 # ---------------------------------------------------------------- Algorithm 2

@@ -6,7 +6,8 @@ oracle's own calls (chunkkv_head, compress_layers) see it too.  The mistakes are
 restatement of ChunkKV §4.1 Algorithm 1 and §4.2 Algorithm 2 (with the probabilities of Kara §2
 Eq. (1)) could plausibly contain: a dropped or wrong scale, a softmax over the wrong axis, a sum
 read as a mean, the GQA group dropped or mis-indexed, the short last chunk lost, an off-by-one in
-the budget, the tie rule or the recent window, the wrong layer reused, a causal limit off by one.
+the budget, the tie rule or the recent window, the wrong layer reused, a causal limit off by one, and, for the incremental pass during decoding,
+the softmax over the tail alone, the tail chunked on the cache's grid, or tail-local positions.
 """
 import importlib.util
 import math
@@ -189,6 +190,28 @@ def gather_prefix(x, idx):                             # the first len(idx) rows
     return x[: len(idx)]
 
 
+def tail_normalised_over_tail(rows, keys, n_prev):    # the softmax over the new tail only
+    return ORIG["key_scores"](rows, keys[n_prev:])
+
+
+def tail_chunks_from_cache_start(rows, keys, n_prev, c, w, L_tail):   # tail chunks on the cache's chunk grid
+    a = ORIG["key_scores"](rows, keys)
+    first = n_prev // c
+    A = ORIG["chunk_scores"](a, c)[first:]
+    n_new = keys.shape[0] - n_prev
+    sel = ORIG["top_chunks"](A, ORIG["n_select"](n_new, c, L_tail))
+    keep = set()
+    for i in sel:
+        keep.update(range((first + i) * c, min((first + i) * c + c, keys.shape[0])))
+    keep.update(range(max(n_prev, keys.shape[0] - w), keys.shape[0]))
+    return A, sel, np.array(sorted(keep), dtype=np.int64)
+
+
+def tail_positions_not_offset(rows, keys, n_prev, c, w, L_tail):       # tail-local positions returned
+    A, sel, idx = ORIG["compress_tail_head"](rows, keys, n_prev, c, w, L_tail)
+    return A, sel, idx - n_prev
+
+
 MUTANTS = {
     "key_scores": [ks_scale_by_d, ks_unscaled, ks_softmax_over_rows, ks_mean_over_rows, ks_raw_logits,
                    ks_limits_ignored],
@@ -202,6 +225,8 @@ MUTANTS = {
     "layer_overlap": [overlap_sum_of_sizes],
     "layer_jaccard": [jaccard_dice],
     "gather": [gather_prefix],
+    "tail_key_scores": [tail_normalised_over_tail],
+    "compress_tail_head": [tail_chunks_from_cache_start, tail_positions_not_offset],
 }
 CASES = [(name, fn) for name, fns in MUTANTS.items() for fn in fns]
 

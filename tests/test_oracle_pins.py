@@ -405,3 +405,79 @@ def test_causal_window_rows_before_the_sequence_add_nothing():
     a = oracle.key_scores(rows, keys, lim)
     assert math.isclose(a.sum(), 3.0, rel_tol=1e-14)          # only the three rows at 0, 1, 2 count
     assert np.allclose(a, oracle.key_scores(rows[2:], keys, lim[2:]), rtol=0, atol=1e-15)
+
+
+# ---------------------------------------------------------------- decoding: incremental pass (reading R12)
+
+def test_tail_pass_with_no_kept_prefix_is_algorithm_1():
+    # n_prev = 0: the whole cache is new, and the pass is ChunkKV §4.1 Algorithm 1 on it
+    q, k, G, c = _rand_case(4, T=83)
+    rows = oracle.group_window_rows(q, 1, G)
+    A, sel, idx = oracle.compress_tail_head(rows, k[:, 1], 0, c, 5, 30)
+    A0, sel0, idx0 = oracle.chunkkv_head(rows, k[:, 1], c, 5, 30)
+    assert np.array_equal(A, A0) and sel == sel0 and idx.tolist() == idx0.tolist()
+
+
+def test_tail_pass_zero_keys_closed_form():
+    # K = 0: p = 1 / (n_prev + n_new) for every key of the cache, so a tail chunk scores
+    # w G |chunk| / (n_prev + n_new), chunks counted from the tail's first token (last one short)
+    n_prev, n_new, c, w, G, d = 41, 23, 5, 3, 2, 4
+    q = np.random.default_rng(2).normal(size=(w, G, d))
+    A, sel, idx = oracle.compress_tail_head(oracle.group_window_rows(q, 0, G), np.zeros((n_prev + n_new, d)),
+                                            n_prev, c, w, 10)
+    assert np.allclose(A, [w * G * s / (n_prev + n_new) for s in (5, 5, 5, 5, 3)], rtol=1e-14)
+    # all full tail chunks tie: the two lowest are kept, then the last w tokens of the tail
+    assert sel == [0, 1]
+    assert idx.tolist() == list(range(n_prev, n_prev + 10)) + list(range(n_prev + n_new - w, n_prev + n_new))
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_tail_pass_brute_force_50_digits(seed):
+    # every window row normalised over the whole cache, tail tokens binned from the tail's start
+    rng = np.random.default_rng(30 + seed)
+    n_prev, n_new = int(rng.integers(0, 9)), int(rng.integers(1, 9))
+    d, R, c = int(rng.integers(1, 4)), int(rng.integers(1, 4)), int(rng.integers(1, 4))
+    rows, keys = rng.normal(size=(R, d)) * 2, rng.normal(size=(n_prev + n_new, d)) * 2
+    A, _, _ = oracle.compress_tail_head(rows, keys, n_prev, c, 1, c)
+    mpmath.mp.dps = 50
+    T = n_prev + n_new
+    want = [mpmath.mpf(0)] * (-(-n_new // c))
+    for r in range(R):
+        s = [sum(mpmath.mpf(float(rows[r, e])) * mpmath.mpf(float(keys[j, e])) for e in range(d)) / mpmath.sqrt(d)
+             for j in range(T)]
+        for j in range(n_prev, T):
+            want[(j - n_prev) // c] += 1 / sum(mpmath.e ** (s[i] - s[j]) for i in range(T))
+    assert np.allclose(A, [float(x) for x in want], rtol=1e-12, atol=1e-15)
+
+
+def test_tail_pass_normalises_over_the_whole_cache():
+    # Hand-built: row 0 attends mostly to a kept key (logit 10/sqrt 2), row 1 does not.  Over the
+    # whole cache, tail token y (favoured by row 1) outscores x (favoured by row 0):
+    #   row 0: Z = e^7.07 + e^1.41 + 2  -> p(x) = 0.0035, p(y) = 0.0008
+    #   row 1: Z = 3 + e^0.85           -> p(x) = 0.187,  p(y) = 0.438
+    # so A(y) = 0.44 > A(x) = 0.19; normalised over the tail alone, x would win (0.90 vs 0.70).
+    rows = np.array([[2.0, 0.0], [0.0, 2.0]])
+    keys = np.array([[5.0, 0.0],      # kept by an earlier pass
+                     [1.0, 0.0],      # x
+                     [0.0, 0.6],      # y
+                     [0.0, 0.0]])     # the most recent token (forced in by w = 1)
+    A, sel, idx = oracle.compress_tail_head(rows, keys, 1, 1, 1, 1)
+    z0 = math.exp(10 / math.sqrt(2)) + math.exp(2 / math.sqrt(2)) + 2
+    z1 = 3 + math.exp(1.2 / math.sqrt(2))
+    want = [math.exp(2 / math.sqrt(2)) / z0 + 1 / z1, 1 / z0 + math.exp(1.2 / math.sqrt(2)) / z1, 1 / z0 + 1 / z1]
+    assert np.allclose(A, want, rtol=1e-13)
+    assert sel == [1] and idx.tolist() == [2, 3]
+
+
+@pytest.mark.parametrize("n_prev,n_new,c,w,L", [(30, 47, 7, 5, 20), (0, 10, 3, 2, 0), (12, 3, 4, 6, 8),
+                                               (5, 64, 8, 8, 100)])
+def test_tail_pass_kept_positions_characterised(n_prev, n_new, c, w, L):
+    q, k, G, _ = _rand_case(5, T=n_prev + n_new)
+    rows = oracle.group_window_rows(q, 0, G)
+    A, sel, idx = oracle.compress_tail_head(rows, k[:, 0], n_prev, c, w, L)
+    C = -(-n_new // c)
+    assert len(A) == C and len(sel) == min(L // c, C)
+    idx = idx.tolist()
+    assert all(b > a for a, b in zip(idx, idx[1:])) and all(n_prev <= j < n_prev + n_new for j in idx)
+    for t in range(n_new):   # tail token t appended  <=>  its tail chunk was selected or it is recent
+        assert ((n_prev + t) in idx) == ((t // c) in sel or t >= n_new - w)
