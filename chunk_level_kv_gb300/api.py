@@ -150,6 +150,27 @@ def chunkkv_compress_layers(p: Params, n_reuse: int, q_win, k, v, k_out, v_out, 
                                        ws.numel() * ws.element_size(), _stream(counts.device)))
 
 
+def _n_prev_array(n_prev):
+    return (ctypes.c_int32 * max(len(n_prev), 1))(*[int(x) for x in n_prev])
+
+
+def chunkkv_tail_sizes(p: Params, n_prev):
+    """(n_cap_max, C_max, workspace bytes) of an incremental pass (chunkkv_compress_tail)."""
+    n_cap, c_max, ws = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_size_t()
+    _check("chunkkv_tail_sizes", LIB.chunkkv_tail_sizes(ctypes.byref(p), _n_prev_array(n_prev), ctypes.byref(n_cap),
+                                                        ctypes.byref(c_max), ctypes.byref(ws)))
+    return n_cap.value, c_max.value, ws.value
+
+
+def chunkkv_compress_tail(p: Params, n_prev, q_win, k, v, k_out, v_out, indices, counts, chunk_scores, ws) -> None:
+    """One incremental pass during decoding: n_prev (host ints, one per sequence) positions of each
+    cache are kept as they are, the rest is the new tail to compress (tail positions in indices)."""
+    _check("chunkkv_compress_tail",
+           LIB.chunkkv_compress_tail(ctypes.byref(p), _n_prev_array(n_prev), _ptr(q_win), _ptr(k), _ptr(v),
+                                     _ptr(k_out), _ptr(v_out), _ptr(indices), _ptr(counts), _ptr(chunk_scores),
+                                     _ptr(ws), ws.numel() * ws.element_size(), _stream(counts.device)))
+
+
 def chunkkv_layer_overlap(p: Params, indices, counts):
     """(inter, union) int32 [n_lists - 1, B, Hkv]: overlap counts of adjacent kept index lists
     (indices [n_lists, B, Hkv, n_cap], counts [n_lists, B, Hkv] as chunkkv_compress_layers writes)."""
@@ -224,9 +245,30 @@ def compress_layers(q_win, k, v, cu_seqlens, *, Hq: int, Hkv: int, w: int, c: in
     return CompressResult(k_out, v_out, indices, counts, scores, workspace)
 
 
+def compress_tail(q_win, k, v, cu_seqlens, n_prev, *, Hq: int, Hkv: int, w: int, c: int, L_tail: int,
+                  return_scores: bool = False, workspace=None) -> CompressResult:
+    """Allocate outputs with torch and run chunkkv_compress_tail (one layer) on the current stream.
+    The result's indices / counts / chunk_scores carry a leading group axis of 1, like compress_layers'."""
+    p, keep = params_for(q_win, k, cu_seqlens, Hkv=Hkv, w=w, c=c, L_max=L_tail)
+    assert p.Hq == Hq
+    n_cap, c_max, ws_bytes = chunkkv_tail_sizes(p, n_prev)
+    B = len(cu_seqlens) - 1
+    dev, d = k.device, k.shape[2]
+    k_out = torch.empty(B, Hkv, n_cap, d, dtype=k.dtype, device=dev)
+    v_out = torch.empty(B, Hkv, n_cap, d, dtype=k.dtype, device=dev)
+    indices = torch.empty(1, B, Hkv, max(n_cap, 1), dtype=torch.int32, device=dev)
+    counts = torch.empty(1, B, Hkv, dtype=torch.int32, device=dev)
+    scores = torch.empty(1, B, Hkv, max(c_max, 1), dtype=torch.float32, device=dev) if return_scores else None
+    if workspace is None:
+        workspace = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    chunkkv_compress_tail(p, n_prev, q_win, k, v, k_out, v_out, indices, counts, scores, workspace)
+    del keep
+    return CompressResult([k_out], [v_out], indices, counts, scores, workspace)
+
+
 __all__ = [
     "ChunkKVError", "CompressResult", "Params", "MAX_GATHER_LAYERS", "PHASES", "PHASE_EVENTS",
-    "chunkkv_compress_layers", "chunkkv_gather", "chunkkv_launch_count", "chunkkv_layer_overlap",
+    "chunkkv_compress_layers", "chunkkv_compress_tail", "chunkkv_tail_sizes", "compress_tail", "chunkkv_gather", "chunkkv_launch_count", "chunkkv_layer_overlap",
     "chunkkv_out_capacity", "chunkkv_probe_ex2", "chunkkv_score", "chunkkv_score_noalloc", "chunkkv_score_path",
     "chunkkv_select", "chunkkv_selftest_wait_timeout", "chunkkv_set_phase_events", "chunkkv_status_check",
     "chunkkv_workspace_size", "compress_layers", "make_params", "params_for",

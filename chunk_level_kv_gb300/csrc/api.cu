@@ -499,6 +499,113 @@ chunkkv_status chunkkv_compress_layers(const chunkkv_params* p, int32_t n_layers
   return cuda_status(e);
 }
 
+// ----------------------------------------------------------------- incremental pass during decoding
+namespace chunkkv {
+namespace {
+
+// The two tables of an incremental pass (reading R12): `pv` describes 2B sequences, 2b the kept
+// prefix of cache b and 2b + 1 its new tail, on which the scoring, the log-sum-exp and the
+// finalisation run (keys of the prefix count in each row's normaliser only); `pt` describes the B
+// tails alone, which the selection and the output layout use.
+struct TailTables {
+  chunkkv_params pv, pt;
+  int32_t cu_v[2 * CHUNKKV_MAX_BATCH + 1];
+  int32_t cu_t[CHUNKKV_MAX_BATCH + 1];
+};
+
+chunkkv_status tail_tables(const chunkkv_params* p, const int32_t* n_prev, TailTables& t) {
+  chunkkv_status s = check_params(p);
+  if (s != CHUNKKV_OK) return s;
+  if (p->causal_window) return CHUNKKV_ERR_UNSUPPORTED;
+  if (p->B > 0 && n_prev == nullptr) return CHUNKKV_ERR_INVALID_ARG;
+  if (2 * p->B > CHUNKKV_MAX_BATCH || (int64_t)2 * p->B * p->Hkv > 65535) return CHUNKKV_ERR_UNSUPPORTED;
+  t.cu_t[0] = 0;
+  for (int b = 0; b < p->B; ++b) {
+    const int T = p->cu_seqlens[b + 1] - p->cu_seqlens[b];
+    if (n_prev[b] < 0 || n_prev[b] > T) return CHUNKKV_ERR_INVALID_ARG;
+    t.cu_v[2 * b] = p->cu_seqlens[b];
+    t.cu_v[2 * b + 1] = p->cu_seqlens[b] + n_prev[b];
+    t.cu_t[b + 1] = t.cu_t[b] + (T - n_prev[b]);
+  }
+  t.cu_v[2 * p->B] = p->B > 0 ? p->cu_seqlens[p->B] : 0;
+  t.pv = *p;
+  t.pv.B = 2 * p->B;
+  t.pv.cu_seqlens = t.cu_v;
+  t.pt = *p;
+  t.pt.cu_seqlens = t.cu_t;
+  return CHUNKKV_OK;
+}
+
+}  // namespace
+}  // namespace chunkkv
+
+chunkkv_status chunkkv_tail_sizes(const chunkkv_params* p, const int32_t* n_prev, int32_t* n_cap_max,
+                                  int32_t* C_max, size_t* ws_bytes) {
+  static thread_local TailTables t;
+  chunkkv_status s = tail_tables(p, n_prev, t);
+  if (s != CHUNKKV_OK) return s;
+  Plan pv, pt;
+  if ((s = make_plan(&t.pv, 1, 1, pv, nullptr)) != CHUNKKV_OK) return s;
+  if ((s = make_plan(&t.pt, 1, 1, pt, nullptr)) != CHUNKKV_OK) return s;
+  if (n_cap_max) *n_cap_max = pt.n_cap;
+  if (C_max) *C_max = pt.C_max;
+  if (ws_bytes) *ws_bytes = pv.total_bytes;
+  return CHUNKKV_OK;
+}
+
+chunkkv_status chunkkv_compress_tail(const chunkkv_params* p, const int32_t* n_prev, const void* q_win,
+                                     const void* k, const void* v, void* k_out, void* v_out, int32_t* indices,
+                                     int32_t* counts, float* chunk_scores, void* ws, size_t ws_bytes,
+                                     chunkkv_stream_t stream) {
+  static thread_local TailTables t;
+  static thread_local SeqTable st_v, st_t;
+  chunkkv_status s = tail_tables(p, n_prev, t);
+  if (s != CHUNKKV_OK) return s;
+  Plan pv, pt;
+  if ((s = make_plan(&t.pv, 1, 1, pv, &st_v)) != CHUNKKV_OK) return s;
+  if ((s = make_plan(&t.pt, 1, 1, pt, &st_t)) != CHUNKKV_OK) return s;
+  if (pt.B * pt.Hkv == 0) return CHUNKKV_OK;
+  if ((pv.wG > 0 && (!q_win || !aligned16(q_win))) || !k || !v || !k_out || !v_out || !counts || !ws ||
+      !aligned16(k) || !aligned16(v) || !aligned16(k_out) || !aligned16(v_out) || !aligned16(ws))
+    return CHUNKKV_ERR_INVALID_ARG;
+  if (pt.n_cap > 0 && !indices) return CHUNKKV_ERR_INVALID_ARG;
+  if (ws_bytes < pv.total_bytes) return CHUNKKV_ERR_WORKSPACE_TOO_SMALL;
+  if (pv.use_tc && !device_memory(k)) return CHUNKKV_ERR_INVALID_ARG;
+  cudaStream_t cs = (cudaStream_t)stream;
+  char* w = (char*)ws;
+  char* base = w + pv.header_bytes;
+  char* slot = base + pv.off_slots;
+  ScoreGeom g = score_geom(&t.pv, pv);
+  g.pair = 1;
+  g.C_max = pt.C_max;                       // chunk scores of the tails only, [B, Hkv, C_max]
+  float* scores = chunk_scores ? chunk_scores : (float*)(base + pv.off_scores);
+  cudaError_t e = cudaSuccess;
+  const bool direct = tc_q_direct(pv, g, q_win) && device_memory(q_win);
+  char* qpack = direct ? nullptr : base + pv.off_qpack;
+  if (pv.use_tc && pv.wG > 0 && !direct) {
+    const void* ql[1] = {q_win};
+    e = launch_pack_q(pv, g, ql, 1, qpack, cs);
+  }
+  if (e == cudaSuccess) e = run_score_groups(pv, g, st_v, &q_win, &k, 1, slot, qpack, (int32_t*)w, cs);
+  if (e == cudaSuccess) e = run_post_score(pv, g, st_v, slot, scores, 1, cs);
+  if (e == cudaSuccess) e = launch_select(pt, select_geom(&t.pt, pt), st_t, scores, indices, counts, 1, cs);
+  if (e == cudaSuccess && pt.n_cap > 0) {
+    // every (cache, head) of the paired table; the kept prefixes append nothing
+    GatherGeom gg = gather_geom(&t.pt, pt);
+    gg.pair = 1;
+    GatherArgs ga;
+    ga.n_layers = 1;
+    ga.k[0] = k;
+    ga.v[0] = v;
+    ga.ko[0] = k_out;
+    ga.vo[0] = v_out;
+    Plan pg = pt;
+    pg.B = pv.B;
+    e = launch_gather(pg, gg, st_v, ga, indices, counts, cs);
+  }
+  return cuda_status(e);
+}
+
 chunkkv_status chunkkv_set_phase_events(void* const* events, int32_t n_events) {
   if (n_events == 0) {
     t_phase_n = 0;

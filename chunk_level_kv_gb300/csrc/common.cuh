@@ -64,6 +64,10 @@ struct ScoreGeom {
   int32_t C_max;      // chunk capacity of the score array
   float alpha;        // log2(e) / sqrt(d): logits are handled as base-2 exponents
   int32_t causal;     // window query q sees keys 0 .. T - w + q only (chunkkv_params.causal_window)
+  // 1: the sequences come in pairs (2i = the kept prefix of cache i, 2i + 1 = its new tail) for an
+  // incremental pass during decoding: both read the window rows of cache i, the row log-sum-exp
+  // spans both, and only the tail has chunk scores (at index i)
+  int32_t pair;
   int64_t q_stride_b, q_stride_w, q_stride_h;
   int64_t kv_stride_t, kv_stride_h;
   // Distance (in floats) between the buffers of consecutive reuse groups, for the
@@ -89,6 +93,7 @@ struct GatherArgs {
 struct GatherGeom {
   int32_t Hkv, d, elt, n_cap;
   int32_t n_reuse, l0;                          // layer l0 + i of a launch uses group (l0 + i) / n_reuse
+  int32_t pair;                                 // paired sequences (see ScoreGeom): only tails, lists at i
   int64_t kv_stride_t, kv_stride_h;
   int64_t idx_gs, cnt_gs;                       // per-group strides of indices / counts
 };

@@ -35,22 +35,24 @@ gather_kernel(GatherGeom gg, const __grid_constant__ SeqTable st, const __grid_c
   const int layer = y / nbh;
   const int bh = y - layer * nbh;
   const int b = bh / gg.Hkv, h = bh - b * gg.Hkv;
+  if (gg.pair && !(b & 1)) return;                       // a kept prefix: nothing to append
+  const int obh = gg.pair ? (b >> 1) * gg.Hkv + h : bh;  // its list and output rows
   const int grp = (gg.l0 + layer) / gg.n_reuse;          // the index list this layer uses
   indices += grp * gg.idx_gs;
   counts += grp * gg.cnt_gs;
   pdl_wait();
-  const int cnt = min(max(counts[bh], 0), gg.n_cap);     // never beyond the output rows
+  const int cnt = min(max(counts[obh], 0), gg.n_cap);    // never beyond the output rows
   const int T = st.cu[b + 1] - st.cu[b];
   const int vpr_shift = __ffs(gg.d * gg.elt / 16) - 1;        // vectors per row (a power of two)
   const int vpr = 1 << vpr_shift;
   const int total = T > 0 ? cnt << vpr_shift : 0;
-  const int32_t* idx = indices + (int64_t)bh * gg.n_cap;
+  const int32_t* idx = indices + (int64_t)obh * gg.n_cap;
   const char* kl = (const char*)ga.k[layer];
   const char* vl = (const char*)ga.v[layer];
   const int64_t row_stride = gg.kv_stride_t * gg.elt;
   const int64_t head_off = ((int64_t)st.cu[b] * gg.kv_stride_t + (int64_t)h * gg.kv_stride_h) * gg.elt;
-  uint4* ko = (uint4*)((char*)ga.ko[layer] + (int64_t)bh * gg.n_cap * gg.d * gg.elt);
-  uint4* vo = (uint4*)((char*)ga.vo[layer] + (int64_t)bh * gg.n_cap * gg.d * gg.elt);
+  uint4* ko = (uint4*)((char*)ga.ko[layer] + (int64_t)obh * gg.n_cap * gg.d * gg.elt);
+  uint4* vo = (uint4*)((char*)ga.vo[layer] + (int64_t)obh * gg.n_cap * gg.d * gg.elt);
 
   const int step = gridDim.x * blockDim.x;
   for (int base = blockIdx.x * blockDim.x * kGatherUnroll + threadIdx.x; base < total;
@@ -87,17 +89,19 @@ gather_any_kernel(GatherGeom gg, const __grid_constant__ SeqTable st, const __gr
   const int layer = blockIdx.y / nbh;
   const int bh = blockIdx.y - layer * nbh;
   const int b = bh / gg.Hkv, h = bh - b * gg.Hkv;
+  if (gg.pair && !(b & 1)) return;
+  const int obh = gg.pair ? (b >> 1) * gg.Hkv + h : bh;
   const int grp = (gg.l0 + layer) / gg.n_reuse;
   indices += grp * gg.idx_gs;
   counts += grp * gg.cnt_gs;
   pdl_wait();
   const int vpr = gg.d * gg.elt / 16;
   const int T = st.cu[b + 1] - st.cu[b];
-  const int total = T > 0 ? min(max(counts[bh], 0), gg.n_cap) * vpr : 0;
-  const int32_t* idx = indices + (int64_t)bh * gg.n_cap;
+  const int total = T > 0 ? min(max(counts[obh], 0), gg.n_cap) * vpr : 0;
+  const int32_t* idx = indices + (int64_t)obh * gg.n_cap;
   const int64_t head_off = ((int64_t)st.cu[b] * gg.kv_stride_t + (int64_t)h * gg.kv_stride_h) * gg.elt;
-  uint4* ko = (uint4*)((char*)ga.ko[layer] + (int64_t)bh * gg.n_cap * gg.d * gg.elt);
-  uint4* vo = (uint4*)((char*)ga.vo[layer] + (int64_t)bh * gg.n_cap * gg.d * gg.elt);
+  uint4* ko = (uint4*)((char*)ga.ko[layer] + (int64_t)obh * gg.n_cap * gg.d * gg.elt);
+  uint4* vo = (uint4*)((char*)ga.vo[layer] + (int64_t)obh * gg.n_cap * gg.d * gg.elt);
   for (int slot = blockIdx.x * blockDim.x + threadIdx.x; slot < total; slot += gridDim.x * blockDim.x) {
     const int r = slot / vpr, vi = slot - r * vpr;
     const int j = min(max(idx[r], 0), T - 1);

@@ -53,7 +53,7 @@ score_simt_kernel(const E* __restrict__ q, const E* __restrict__ k, ScoreGeom g,
       float val = 0.f;
       if (r < g.wG) {
         int gm = r / g.w, qi = r % g.w;           // row r = (group member gm, window row qi)
-        val = to_float(q[(int64_t)b * g.q_stride_b + (int64_t)qi * g.q_stride_w +
+        val = to_float(q[(int64_t)(b >> g.pair) * g.q_stride_b + (int64_t)qi * g.q_stride_w +
                          (int64_t)(h * g.G + gm) * g.q_stride_h + e]);
       }
       qs[row * ld + e] = val;
@@ -174,6 +174,7 @@ finalize_kernel(ScoreGeom g, const __grid_constant__ SeqTable st, const float* _
   scores += blockIdx.z * g.scores_gs;
   pdl_wait();
   decode_unit(st, g.Hkv, gu, b, h, u);
+  if (g.pair && !(b & 1)) return;               // a kept prefix: in the normaliser only
   const int T = st.cu[b + 1] - st.cu[b];
   const int C = (T + g.c - 1) / g.c;
   if (min(g.cpu, C - u * g.cpu) <= cb) return;  // no chunk of this unit in this block
@@ -202,7 +203,7 @@ finalize_kernel(ScoreGeom g, const __grid_constant__ SeqTable st, const float* _
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int wg = WG > 0 ? WG : g.wG;
   const bin_t* ub = bins + ((int64_t)gu * g.cpu + cb) * wg;
-  float* out = scores + ((int64_t)b * g.Hkv + h) * g.C_max + (int64_t)u * g.cpu + cb;
+  float* out = scores + ((int64_t)(b >> g.pair) * g.Hkv + h) * g.C_max + (int64_t)u * g.cpu + cb;
   constexpr int kW = kFinThreads / 32;
   if (fin_wide(wg)) {
     for (int ch0 = warp * kFinWideGroup; ch0 < nc; ch0 += kW * kFinWideGroup)
@@ -231,12 +232,14 @@ lse_kernel(ScoreGeom g, const __grid_constant__ SeqTable st, const float* __rest
   const int b = bh / g.Hkv, h = bh - b * g.Hkv;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int r = blockIdx.y * 32 + lane;
-  const int U = st.uoff[b + 1] - st.uoff[b];
+  // paired sequences: the units of the kept prefix and of the tail (adjacent) merge into one row lse
+  const int b0 = g.pair ? (b & ~1) : b, b1 = g.pair ? (b | 1) + 1 : b + 1;
+  const int U = st.uoff[b1] - st.uoff[b0];
   rl += blockIdx.z * g.rl_gs;                   // this CTA's reuse group
   lse += blockIdx.z * g.lse_gs;
   pdl_wait();
   const int64_t ustride = (int64_t)g.Hkv * 2 * g.wG;
-  const float* base = rl + ((int64_t)st.uoff[b] * g.Hkv + h) * 2 * g.wG + r;
+  const float* base = rl + ((int64_t)st.uoff[b0] * g.Hkv + h) * 2 * g.wG + r;
   float M = -INFINITY, S = 0.f;
   if (r < g.wG) {
     int v = warp;
@@ -276,10 +279,11 @@ __global__ void zero_scores_kernel(ScoreGeom g, const __grid_constant__ SeqTable
   scores += blockIdx.z * g.scores_gs;
   pdl_wait();
   decode_unit(st, g.Hkv, blockIdx.x, b, h, u);
+  if (g.pair && !(b & 1)) return;
   const int T = st.cu[b + 1] - st.cu[b];
   const int C = (T + g.c - 1) / g.c;
   const int nc = min(g.cpu, C - u * g.cpu);
-  float* out = scores + ((int64_t)b * g.Hkv + h) * g.C_max + (int64_t)u * g.cpu;
+  float* out = scores + ((int64_t)(b >> g.pair) * g.Hkv + h) * g.C_max + (int64_t)u * g.cpu;
   for (int ch = threadIdx.x; ch < nc; ch += blockDim.x) out[ch] = 0.f;
   pdl_trigger();
 }

@@ -4,13 +4,13 @@
 // in the single-pass unit decomposition described in score.cu: each work item
 // is one (reuse group, scoring unit, 128-row M tile of the window rows), and one
 // persistent launch covers the items of every reuse group.  Per item the CTA
-//   - has the item's 128 packed window rows (Q) loaded by TMA and copied into
-//     TMEM (only when the tile differs from the previous item's),
+//   - has the item's 128 packed window rows (Q) loaded by TMA into shared
+//     memory (only when the tile differs from the previous item's),
 //   - streams the unit's keys in tiles of 80 through shared memory by TMA,
-//   - computes S = Q K^T (128 x 80, fp32) with tcgen05.mma (A in TMEM, B in
-//     shared memory) into one of two TMEM accumulator stages,
+//   - computes S = Q K^T (128 x 80, fp32) with tcgen05.mma (A and B in shared
+//     memory) into one of three TMEM accumulator stages,
 //   - lets each of 128 softmax threads own one window row: it reads its row of
-//     S from TMEM, forms 2^(s*log2(e)/sqrt(d) - R) with R the row maximum of the
+//     S from TMEM (16 columns at a time, the next 16 in flight), forms 2^(s*log2(e)/sqrt(d) - R) with R the row maximum of the
 //     item's first tile, and sums those per chunk (chunk boundaries are compile
 //     time constants for each of the C / gcd(80, C) tile phases), writing one
 //     16-bit bin per (chunk, row) and the row's (R, sum) at the end of the item.
@@ -36,15 +36,12 @@ constexpr int kN = 80;                         // keys per tile (MMA N)
 constexpr int kD = 128;                        // head dimension
 constexpr int kStagesK = 4;                    // key tiles in shared memory (two CTAs of 112 KB per SM)
 constexpr int kStagesQ = 1;                    // Q tile in shared memory (reused across items)
-// The window-row tile lives in TMEM (columns 0..63, copied from shared memory
-// once per tile change) and feeds the MMAs as operand A, so that the tensor
-// core reads only the key tile from shared memory (with both operands there an
-// M=128, N=80 MMA asks for more shared-memory bandwidth than an SM has).  The
-// accumulators take the columns after it.
-constexpr int kQCols = 64;                     // 128 rows x 128 bf16 = 64 32-bit columns
-constexpr int kStagesT = 2;                    // accumulator stages in TMEM (80 columns each)
+// The window-row tile stays in shared memory as MMA operand A (both operands
+// there), which leaves all 256 TMEM columns of a CTA to three 80-column fp32
+// accumulator stages: the MMAs of two tiles can run ahead of the softmax.
+constexpr int kStagesT = 3;                    // accumulator stages in TMEM (80 columns each)
 constexpr int kTmemCols = 256;
-static_assert(kStagesT >= 2 && kQCols + kStagesT * kN <= kTmemCols, "TMEM budget");
+static_assert(kStagesT >= 2 && kStagesT * kN <= kTmemCols, "TMEM budget");
 constexpr int kThreads = 192;                  // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
 constexpr int kPanelQ = 128 * 128;             // one 64-element (128 B) panel of 128 rows
 constexpr int kPanelK = kN * 128;              // one 128 B panel of 80 key rows
@@ -75,6 +72,7 @@ struct TcGeom {
   int32_t G;                         // query heads per KV head
   int32_t q_direct;                  // 1: window rows read from Q_w itself (maps.q[group]), 0: packed (maps.q[0])
   int32_t qm;                        // query heads per 128-row M tile when q_direct (128 / w)
+  int32_t qshift;                    // 1: paired sequences (ScoreGeom::pair), sequence b reads window b >> 1
   int32_t items_pg;                  // work items per group: units x M tiles
   int32_t n_items;                   // items_pg x groups of this launch
   int64_t slot_bytes;                // bytes between the scratch slots of consecutive groups
@@ -181,17 +179,12 @@ __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
-// D (+)= A B^T with A (128 x 16 bf16) in TMEM at a_tmem (row m in lane m, element pairs per column).
-__device__ __forceinline__ void tc_mma_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t acc) {
+// D (+)= A B^T with A (128 x 16 bf16) in shared memory (matrix descriptor).
+__device__ __forceinline__ void tc_mma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t acc) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}"
-      ::"r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(kIdesc), "r"(acc) : "memory");
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}"
+      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(acc) : "memory");
 }
-// 128 rows x 32 bytes from shared memory (matrix descriptor) into 128 lanes x 8 TMEM columns.
-__device__ __forceinline__ void tc_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
-
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row groups 1024 B apart.
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
@@ -319,12 +312,19 @@ __device__ __forceinline__ void tile_seg(const uint32_t (&r)[16], float2 alpha2,
   s.carry = acc;
 }
 
+// The columns of a tile, software-pipelined: segment SEG is processed while
+// segment SEG + 1 is on its way from TMEM (one x16 load in flight beside the
+// arithmetic, 32 registers of tile data instead of 80).
 template <int C, int PH, int SEG, bool MASK>
-__device__ __forceinline__ void tile_segs(const uint32_t (&r)[kN / 16][16], float2 alpha, RowState& s, bin_t* bin,
-                                          int wG, int valid, bool write, uint64_t pol) {
+__device__ __forceinline__ void tile_segs_pipe(uint32_t taddr, uint32_t (&ra)[16], uint32_t (&rb)[16], float2 alpha,
+                                               RowState& s, bin_t* bin, int wG, int valid, bool write, uint64_t pol) {
   if constexpr (SEG < kN / 16) {
-    tile_seg<C, PH, SEG, MASK>(r[SEG], alpha, s, bin, wG, valid, write, pol);
-    tile_segs<C, PH, SEG + 1, MASK>(r, alpha, s, bin, wG, valid, write, pol);
+    if constexpr (SEG + 1 < kN / 16) tmem_ld16(taddr + 16 * (SEG + 1), rb);
+    tile_seg<C, PH, SEG, MASK>(ra, alpha, s, bin, wG, valid, write, pol);
+    if constexpr (SEG + 1 < kN / 16) {
+      tmem_wait16(rb);
+      tile_segs_pipe<C, PH, SEG + 1, MASK>(taddr, rb, ra, alpha, s, bin, wG, valid, write, pol);
+    }
   }
 }
 
@@ -371,21 +371,25 @@ __device__ __forceinline__ void tile_cols_rt(const uint32_t (&r)[kN / 16][16], f
   s.carry = acc;
 }
 
-// One tile of kN columns: the whole row segment is loaded from TMEM first
-// (kN/16 x16 loads, one wait), so the column pairs are independent work that
-// the scheduler can interleave freely.
+// One tile of kN columns: compile-time chunk sizes take the pipelined segments;
+// a chunk size known only at run time loads the whole row segment from TMEM
+// first (kN/16 x16 loads, one wait) and counts its chunk ends.
 template <int C, int PH, bool MASK>
 __device__ __forceinline__ void tile_phase(uint32_t taddr, float2 alpha, RowState& s, bin_t* bin, int wG, int valid,
                                            bool write, uint64_t pol, int c, int ph) {
+  if constexpr (C > 0) {
+    uint32_t ra[16], rb[16];
+    tmem_ld16(taddr, ra);
+    tmem_wait16(ra);
+    tile_segs_pipe<C, PH, 0, MASK>(taddr, ra, rb, alpha, s, bin, wG, valid, write, pol);
+    return;
+  }
   uint32_t r[kN / 16][16];
 #pragma unroll
   for (int sg = 0; sg < kN / 16; ++sg) tmem_ld16(taddr + 16 * sg, r[sg]);
 #pragma unroll
   for (int sg = 0; sg < kN / 16; ++sg) tmem_wait16(r[sg]);
-  if constexpr (C == 0)
-    tile_cols_rt<MASK>(r, alpha, s, bin, wG, valid, write, pol, c, ph);
-  else
-    tile_segs<C, PH, 0, MASK>(r, alpha, s, bin, wG, valid, write, pol);
+  tile_cols_rt<MASK>(r, alpha, s, bin, wG, valid, write, pol, c, ph);
 }
 
 // C > 0: the tile phases ph = (t * kN) mod C are the multiples of gcd(kN, C)
@@ -432,8 +436,8 @@ __device__ __forceinline__ void load_q(const TcMaps& maps, const TcGeom& g, cons
   if (g.q_direct) {
     const CUtensorMap* qm = &maps.q[it.grp];
     const int hq0 = it.h * g.G + it.mt * g.qm;
-    tma_load_4d(sq, qm, bar, 0, 0, hq0, it.b);
-    tma_load_4d(sq + kPanelQ, qm, bar, 64, 0, hq0, it.b);
+    tma_load_4d(sq, qm, bar, 0, 0, hq0, it.b >> g.qshift);
+    tma_load_4d(sq + kPanelQ, qm, bar, 64, 0, hq0, it.b >> g.qshift);
   } else {
     tma_load_2d(sq, &maps.q[0], bar, 0, it.key * 128);
     tma_load_2d(sq + kPanelQ, &maps.q[0], bar, 64, it.key * 128);
@@ -463,8 +467,7 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
   uint64_t* k_empty = k_full + kStagesK;                       // [kStagesK]
   uint64_t* t_full = k_empty + kStagesK;                       // [kStagesT]
   uint64_t* t_empty = t_full + kStagesT;                       // [kStagesT]
-  uint64_t* qt_done = t_empty + kStagesT;                      // [1] MMAs of the old TMEM window tile / its copy done
-  uint64_t* drained = qt_done + 1;                             // [1] all MMAs done (teardown after a give-up)
+  uint64_t* drained = t_empty + kStagesT;                      // [1] all MMAs done (teardown after a give-up)
   uint32_t* tmem_slot = (uint32_t*)(drained + 1);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
@@ -473,7 +476,6 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
     for (int i = 0; i < kStagesQ; ++i) { mbar_init(smem_u32(&q_full[i]), 1); mbar_init(smem_u32(&q_empty[i]), 1); }
     for (int i = 0; i < kStagesK; ++i) { mbar_init(smem_u32(&k_full[i]), 1); mbar_init(smem_u32(&k_empty[i]), 1); }
     for (int i = 0; i < kStagesT; ++i) { mbar_init(smem_u32(&t_full[i]), 1); mbar_init(smem_u32(&t_empty[i]), 128); }
-    mbar_init(smem_u32(&qt_done[0]), 1);
     mbar_init(smem_u32(drained), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -541,7 +543,7 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
-      uint32_t kc = 0, qc = 0, tc = 0, qtc = 0;        // this warp's own counts of the same phases
+      uint32_t kc = 0, qc = 0, tc = 0;                 // this warp's own counts of the same phases
       int qkey = -1;
       const uint32_t qaddr = smem_u32(sQ);
       for (int item = blockIdx.x; item < g.n_items && !*abort_flag; item += gridDim.x) {
@@ -549,21 +551,9 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
         const int ntile = it.ntile;
         const int key = it.key;
         if (key != qkey) {
-          // the TMEM tile is overwritten only after the MMAs that read it are done
-          if (qkey >= 0) {
-            tc_commit(smem_u32(&qt_done[0]));
-            if (!wait_bar(ctl, smem_u32(&qt_done[0]), qtc & 1, kDevTimeoutMma)) break;
-            ++qtc;
-          }
+          // the shared-memory tile is refilled only after the MMAs that read it are done
+          if (qkey >= 0) tc_commit(smem_u32(&q_empty[0]));
           if (!wait_bar(ctl, smem_u32(&q_full[0]), qc & 1, kDevTimeoutMma)) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk)      // 16 elements (32 B of each row) per copy
-            tc_cp_128x256b(tmem + kk * 8, sw128_desc(qaddr + (kk >> 2) * kPanelQ + (kk & 3) * 32));
-          tc_commit(smem_u32(&q_empty[0]));                    // shared-memory tile free once copied
-          tc_commit(smem_u32(&qt_done[0]));
-          if (!wait_bar(ctl, smem_u32(&qt_done[0]), qtc & 1, kDevTimeoutMma)) break;
-          ++qtc;
           tc_fence_after();
           ++qc;
           qkey = key;
@@ -578,12 +568,12 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
           }
           tc_fence_after();
           const uint32_t kaddr = smem_u32(sK + ks * kKBytes);
-          const uint32_t d = tmem + kQCols + ts * kN;
+          const uint32_t d = tmem + ts * kN;
 #pragma unroll
           for (int kk = 0; kk < kD / 16; ++kk) {
             const uint32_t off = (kk & 3) * 32;                  // 16 bf16 = 32 B inside the swizzle atom
-            const uint64_t bd = sw128_desc(kaddr + (kk >> 2) * kPanelK + off);
-            tc_mma_ta(d, tmem + kk * 8, bd, kk > 0 ? 1u : 0u);
+            tc_mma_ss(d, sw128_desc(qaddr + (kk >> 2) * kPanelQ + off), sw128_desc(kaddr + (kk >> 2) * kPanelK + off),
+                      kk > 0 ? 1u : 0u);
           }
           tc_commit(smem_u32(&k_empty[ks]));
           tc_commit(smem_u32(&t_full[ts]));
@@ -625,7 +615,7 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
         }
         tc_fence_after();
         if (warp_live) {
-          const uint32_t taddr = lane_base + kQCols + ts * kN;
+          const uint32_t taddr = lane_base + ts * kN;
           int valid = min(kN, nk - t * kN);
           bool mask = valid < kN;
           if (CAUSAL && it.tok0 + t * kN + kN > causal_from) {
@@ -743,7 +733,7 @@ __global__ void pack_q_kernel(const __grid_constant__ PackArgs pa, ScoreGeom g, 
     uint4 val = make_uint4(0, 0, 0, 0);
     if (r < g.wG) {
       const int gm = r / g.w, qi = r % g.w;
-      val = *(const uint4*)(q + (int64_t)b * g.q_stride_b + (int64_t)qi * g.q_stride_w +
+      val = *(const uint4*)(q + (int64_t)(b >> g.pair) * g.q_stride_b + (int64_t)qi * g.q_stride_w +
                             (int64_t)(h * g.G + gm) * g.q_stride_h + vi * 8);
     }
     *(uint4*)(qp + row * kD + vi * 8) = val;
@@ -912,7 +902,7 @@ namespace tc {
 // stride of an axis of extent 1 is never used and is then set to 16 bytes.
 bool encode_q_direct(EncodeFn enc, CUtensorMap* map, const void* q, const Plan& pl, const ScoreGeom& g) {
   if (pl.w < 1 || 128 % pl.w != 0) return false;
-  const int64_t ext[3] = {pl.w, (int64_t)pl.Hkv * pl.G, pl.B};
+  const int64_t ext[3] = {pl.w, (int64_t)pl.Hkv * pl.G, pl.B >> g.pair};   // window rows of B (or B / 2 caches)
   const int64_t st[3] = {g.q_stride_w, g.q_stride_h, g.q_stride_b};
   cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)ext[0], (cuuint64_t)ext[1], (cuuint64_t)ext[2]};
   cuuint64_t strides[3];
@@ -988,6 +978,7 @@ cudaError_t launch_score_tc(const Plan& pl, const ScoreGeom& g, const SeqTable& 
     tg.G = pl.G;
     tg.q_direct = direct ? 1 : 0;
     tg.qm = direct ? 128 / pl.w : 0;
+    tg.qshift = g.pair;
     tg.items_pg = g.n_units * MT;
     tg.n_items = tg.items_pg * n;
     tg.slot_bytes = slot_bytes;

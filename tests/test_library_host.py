@@ -221,3 +221,34 @@ def test_rescale_inputs_cross_the_threshold(ckv):
         for u0 in range(0, wl.T_total - 240, 240):
             lift = s[:, u0 + 150] - s[:, u0:u0 + 80].max(dim=1).values
             assert lift[0::2].min() > 23 and lift[1::2].max() < -23
+
+
+def test_tail_pass_sizes_and_argument_checks(ckv):
+    # the incremental pass sizes its outputs from the new tails, its workspace from prefix + tail
+    from chunk_level_kv_gb300._lib import LIB
+    p, keep = _p(ckv, cu_seqlens=[0, 500, 1300], c=10, w=8, L_max=50)
+    n_cap, c_max, ws = ckv.chunkkv_tail_sizes(p, [300, 0])
+    assert (n_cap, c_max) == (58, 80)                  # tails of 200 and 800 tokens; k = 5
+    assert ws >= ckv.chunkkv_workspace_size(p) > 0
+    assert ckv.chunkkv_tail_sizes(p, [500, 800])[:2] == (0, 0)      # nothing new: nothing to append
+    P = ctypes.byref(p)
+    n_cap_, c_, w_ = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_size_t()
+    out = (ctypes.byref(n_cap_), ctypes.byref(c_), ctypes.byref(w_))
+
+    def sizes(n_prev):
+        arr = (ctypes.c_int32 * 2)(*n_prev) if n_prev is not None else None
+        return LIB.chunkkv_tail_sizes(P, arr, *out)
+    assert sizes([501, 0]) == 1                        # a prefix longer than its cache
+    assert sizes([-1, 0]) == 1
+    assert sizes(None) == 1
+    pc, keep_c = _p(ckv, cu_seqlens=[0, 500, 1300], causal_window=True)
+    assert LIB.chunkkv_tail_sizes(ctypes.byref(pc), (ctypes.c_int32 * 2)(0, 0), *out) == 2
+    pb, keep_b = _p(ckv, cu_seqlens=list(range(0, 600)))   # 599 caches: the paired table would exceed the batch limit
+    assert LIB.chunkkv_tail_sizes(ctypes.byref(pb), (ctypes.c_int32 * 599)(), *out) == 2
+    # null or misaligned pointers and a short workspace are rejected before any launch
+    n_prev = (ctypes.c_int32 * 2)(300, 0)
+    assert LIB.chunkkv_compress_tail(P, n_prev, None, None, None, None, None, None, None, None, None, 0, None) == 1
+    assert LIB.chunkkv_compress_tail(P, n_prev, 0x1000, 0x2008, 0x3000, 0x4000, 0x5000, 0x6000, 0x7000, None,
+                                     0x8000, ws, None) == 1
+    assert LIB.chunkkv_compress_tail(P, n_prev, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 0x7000, None,
+                                     0x8000, 16, None) == 3
