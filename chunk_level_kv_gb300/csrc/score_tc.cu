@@ -382,14 +382,14 @@ __device__ __forceinline__ void tile_phase(uint32_t taddr, float2 alpha, RowStat
     tmem_ld16(taddr, ra);
     tmem_wait16(ra);
     tile_segs_pipe<C, PH, 0, MASK>(taddr, ra, rb, alpha, s, bin, wG, valid, write, pol);
-    return;
+  } else {
+    uint32_t r[kN / 16][16];
+#pragma unroll
+    for (int sg = 0; sg < kN / 16; ++sg) tmem_ld16(taddr + 16 * sg, r[sg]);
+#pragma unroll
+    for (int sg = 0; sg < kN / 16; ++sg) tmem_wait16(r[sg]);
+    tile_cols_rt<MASK>(r, alpha, s, bin, wG, valid, write, pol, c, ph);
   }
-  uint32_t r[kN / 16][16];
-#pragma unroll
-  for (int sg = 0; sg < kN / 16; ++sg) tmem_ld16(taddr + 16 * sg, r[sg]);
-#pragma unroll
-  for (int sg = 0; sg < kN / 16; ++sg) tmem_wait16(r[sg]);
-  tile_cols_rt<MASK>(r, alpha, s, bin, wG, valid, write, pol, c, ph);
 }
 
 // C > 0: the tile phases ph = (t * kN) mod C are the multiples of gcd(kN, C)
@@ -545,7 +545,7 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
     if (lane == 0) {
       uint32_t kc = 0, qc = 0, tc = 0;                 // this warp's own counts of the same phases
       int qkey = -1;
-      const uint32_t qaddr = smem_u32(sQ);
+      const uint64_t qdesc = sw128_desc(smem_u32(sQ));   // the window-row tile never moves
       for (int item = blockIdx.x; item < g.n_items && !*abort_flag; item += gridDim.x) {
         const Item it = decode_item(g, st, item);
         const int ntile = it.ntile;
@@ -567,12 +567,14 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
             break;
           }
           tc_fence_after();
-          const uint32_t kaddr = smem_u32(sK + ks * kKBytes);
+          const uint64_t kdesc = sw128_desc(smem_u32(sK + ks * kKBytes));
           const uint32_t d = tmem + ts * kN;
+          // step kk reads 16 bf16 (32 B) of every row: panel kk / 4, offset 32 (kk % 4) inside the
+          // swizzle atom; the descriptors' start-address fields (16-byte units) advance by that
 #pragma unroll
           for (int kk = 0; kk < kD / 16; ++kk) {
-            const uint32_t off = (kk & 3) * 32;                  // 16 bf16 = 32 B inside the swizzle atom
-            tc_mma_ss(d, sw128_desc(qaddr + (kk >> 2) * kPanelQ + off), sw128_desc(kaddr + (kk >> 2) * kPanelK + off),
+            const uint32_t off = (kk & 3) * 32;
+            tc_mma_ss(d, qdesc + (((kk >> 2) * kPanelQ + off) >> 4), kdesc + (((kk >> 2) * kPanelK + off) >> 4),
                       kk > 0 ? 1u : 0u);
           }
           tc_commit(smem_u32(&k_empty[ks]));
@@ -597,8 +599,10 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
       const int nk = it.nk, ntile = it.ntile;
       const int row = it.mt * 128 + rloc;
       const int wg = WG > 0 ? WG : g.wG;                            // bin stride between chunks
-      const bool write = row < g.wG;
       const bool warp_live = it.mt * 128 + lg * 32 < g.wG;         // whole warp of padding rows: no work
+      // rows that own bins; with a compile-time w*G that is a multiple of 32 every row of a live warp
+      // does, which lets the bin stores go without a branch each
+      const bool write = (WG > 0 && WG % 32 == 0) ? warp_live : row < g.wG;
       bin_t* ubins = (bin_t*)((char*)bins + it.grp * g.slot_bytes) + (size_t)it.unit * g.cpu * g.wG + row;
       float* url = (float*)((char*)rl + it.grp * g.slot_bytes) + (size_t)it.unit * 2 * g.wG + row;
       RowState s{make_float2(0.f, 0.f), make_float2(0.f, 0.f), 0.f};
@@ -847,8 +851,8 @@ cudaError_t launch_causal(bool causal, const TcGeom& tg, const TcMaps& maps, con
   }
 }
 
-// Token-level chunks (c = 1) and chunk sizes without an instance of their own
-// (C = 0: c read at run time): the causal window or any w*G.
+// Chunk sizes without an instance of their own (C = 0: c read at run time): the
+// causal window or any w*G.
 template <int C>
 cudaError_t launch_any_wg(bool causal, const TcGeom& tg, const TcMaps& maps, const SeqTable& st, float* rl,
                           bin_t* bins, int32_t* err, int slot, cudaStream_t s) {
@@ -987,11 +991,12 @@ cudaError_t launch_score_tc(const Plan& pl, const ScoreGeom& g, const SeqTable& 
     float* rlg = (float*)((char*)rl + g0 * slot_bytes);
     bin_t* bg = (bin_t*)((char*)bins + g0 * slot_bytes);
     // compile-time instances (the chunk ends of every tile phase are constants) for
-    // the common chunk sizes; any other c >= 2 runs the C = 0 instance
+    // the common chunk sizes (the notes' ablation set 1, 3, 5, 10, 15, 20, 30 among
+    // them); any other c >= 2 runs the C = 0 instance
     const bool causal = g.causal != 0;
     cudaError_t e = cudaErrorNotSupported;
     switch (pl.c) {
-      case 1: e = tc::launch_any_wg<1>(causal, tg, maps, st, rlg, bg, err, 8, s); break;
+      case 1: e = tc::launch_causal<1>(causal, tg, maps, st, rlg, bg, err, 8, s); break;
       case 3: e = tc::launch_causal<3>(causal, tg, maps, st, rlg, bg, err, 0, s); break;
       case 4: e = tc::launch_causal<4>(causal, tg, maps, st, rlg, bg, err, 1, s); break;
       case 5: e = tc::launch_causal<5>(causal, tg, maps, st, rlg, bg, err, 2, s); break;
@@ -1000,6 +1005,7 @@ cudaError_t launch_score_tc(const Plan& pl, const ScoreGeom& g, const SeqTable& 
       case 16: e = tc::launch_causal<16>(causal, tg, maps, st, rlg, bg, err, 5, s); break;
       case 20: e = tc::launch_causal<20>(causal, tg, maps, st, rlg, bg, err, 6, s); break;
       case 30: e = tc::launch_causal<30>(causal, tg, maps, st, rlg, bg, err, 7, s); break;
+      case 15: e = tc::launch_causal<15>(causal, tg, maps, st, rlg, bg, err, 10, s); break;
       default: e = tc::launch_any_wg<0>(causal, tg, maps, st, rlg, bg, err, 9, s); break;
     }
     if (e != cudaSuccess) return e;
