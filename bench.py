@@ -387,9 +387,40 @@ def device_timing(ckv, wl, args, dev, local, ws_n, peaks, peak_src, ex2_rate):
             "score_roofs": score_roofs, "dominant": dominant}
 
 
+def parse_cpulist(text: str) -> set:
+    """CPU numbers of a Linux cpulist ("0-3,8,10-11")."""
+    cpus = set()
+    for part in text.strip().split(","):
+        if not part:
+            continue
+        lo, _, hi = part.partition("-")
+        cpus.update(range(int(lo), int(hi or lo) + 1))
+    return cpus
+
+
+def bind_to_gpu_cpus(gpu_index: int):
+    """Restrict this process to the host CPUs that the PCI topology lists as local to the GPU (its
+    NUMA node), before any host buffer is allocated, so that pinned host memory lands next to the
+    GPU.  Returns the CPUs kept, or None when the topology gives nothing usable."""
+    try:
+        bus = subprocess.run(["nvidia-smi", f"--id={gpu_index}", "--query-gpu=pci.bus_id", "--format=csv,noheader"],
+                             capture_output=True, text=True, timeout=30).stdout.strip().lower()
+        dom, rest = bus.split(":", 1)
+        path = f"/sys/bus/pci/devices/{int(dom, 16):04x}:{rest}/local_cpulist"
+        with open(path) as f:
+            local = parse_cpulist(f.read()) & os.sched_getaffinity(0)
+        if local:
+            os.sched_setaffinity(0, local)
+            return sorted(local)
+    except Exception:
+        pass
+    return None
+
+
 def run_gpu(args):
     import chunk_level_kv_gb300 as ckv
     ws_n, rank, local = dist_env()
+    host_cpus = bind_to_gpu_cpus(local)
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     if ws_n > 1:
@@ -531,6 +562,8 @@ def run_gpu(args):
         d2h = nbytes_of([hidx, hcnt]) + 2 * row * sum(kept)
         e2e = {"value": round(nbytes * ws_n / (e2e_ms * 1e-3) / 1e9, 3), "unit": UNIT,
                "link_probe": link_probe(dev),
+               "host_cpus": (f"{len(host_cpus)} CPUs local to the GPU ({host_cpus[0]}-{host_cpus[-1]}), "
+                             f"pinned buffers allocated after binding") if host_cpus else "not bound",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms, 4),
                "transfers": "window queries and scoring-layer keys copied in (two device buffer sets); "
                             "kept K/V rows read from and K'/V' written to pinned host memory by the gather "

@@ -94,3 +94,11 @@ def test_exponential_roof_of_the_128k_scoring(monkeypatch, rate, bound):
 
 def test_job_rate_counts_every_rank():
     assert bench.job_rate(100.0, 4, 2.0) == pytest.approx(200000.0)
+
+
+def test_cpulist_parsing():
+    # the host CPUs local to the GPU come from a Linux cpulist in sysfs
+    import bench
+    assert bench.parse_cpulist("0-3,8,10-11\n") == {0, 1, 2, 3, 8, 10, 11}
+    assert bench.parse_cpulist("72-143") == set(range(72, 144))
+    assert bench.parse_cpulist("") == set()
