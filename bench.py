@@ -481,13 +481,19 @@ def run_gpu(args):
     # ---- end to end through the C-ABI with host buffers (pinned), transfers inside the timed region
     e2e = e2e_staged = None
     if not args.no_e2e:
-        hq = [q.cpu().pin_memory() if q is not None else None for q in qs]
-        hk = [x.cpu().pin_memory() for x in ks]
-        hv = [x.cpu().pin_memory() for x in vs]
-        hko = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in ko]
-        hvo = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in vo]
-        hidx = torch.empty(idx.shape, dtype=idx.dtype).pin_memory()
-        hcnt = torch.empty(cnt.shape, dtype=cnt.dtype).pin_memory()
+        # pinned host buffers allocated directly (no pageable copy in between) and filled from the device
+        def pinned_like(x, fill=True):
+            h = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+            if fill:
+                h.copy_(x)
+            return h
+        hq = [pinned_like(q) if q is not None else None for q in qs]
+        hk = [pinned_like(x) for x in ks]
+        hv = [pinned_like(x) for x in vs]
+        hko = [pinned_like(x, False) for x in ko]
+        hvo = [pinned_like(x, False) for x in vo]
+        hidx = pinned_like(idx, False)
+        hcnt = pinned_like(cnt, False)
         nbytes_of = lambda ts: sum(x.numel() * x.element_size() for x in ts if x is not None)
         cin, cout = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
