@@ -600,6 +600,7 @@ def run_gpu(args):
                    "Hkv": wl.Hkv, "d": wl.d, "w": wl.w, "c": wl.c, "L_max": wl.L_max,
                    "l2": t["l2_note"], "parallelism": f"replicas x{ws_n}"},
         "tokens_per_s": round(t["tokens_s"], 1),
+        "token_layers_per_s": round(t["tokens_s"] * wl.n_layers, 1),
         "algorithmic_bytes_per_step": nbytes,
         "hbm_roof_frac": round(value / ws_n / peaks["hbm_gbs"], 4),
         "roofline": t["dominant"],
