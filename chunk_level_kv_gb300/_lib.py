@@ -48,8 +48,9 @@ def _load():
         "chunkkv_select": [P, vp, vp, vp, vp],
         "chunkkv_gather": [P, i32, vp, vp, pp, pp, pp, pp, vp],
         "chunkkv_compress_layers": [P, i32, i32, pp, pp, pp, pp, pp, vp, vp, vp, vp, sz, vp],
-        "chunkkv_tail_sizes": [P, ctypes.POINTER(i32), ctypes.POINTER(i32), ctypes.POINTER(i32), ctypes.POINTER(sz)],
-        "chunkkv_compress_tail": [P, ctypes.POINTER(i32), vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
+        "chunkkv_tail_sizes": [P, ctypes.POINTER(i32), i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32),
+                               ctypes.POINTER(sz)],
+        "chunkkv_compress_tail": [P, ctypes.POINTER(i32), i32, i32, pp, pp, pp, pp, pp, vp, vp, vp, vp, sz, vp],
         "chunkkv_status_check": [vp, vp, ctypes.POINTER(i32)],
         "chunkkv_score_path": [P],
         "chunkkv_score_noalloc": [P, vp, vp, vp, vp],

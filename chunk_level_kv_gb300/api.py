@@ -154,21 +154,25 @@ def _n_prev_array(n_prev):
     return (ctypes.c_int32 * max(len(n_prev), 1))(*[int(x) for x in n_prev])
 
 
-def chunkkv_tail_sizes(p: Params, n_prev):
+def chunkkv_tail_sizes(p: Params, n_prev, n_layers: int = 1, n_reuse: int = 1):
     """(n_cap_max, C_max, workspace bytes) of an incremental pass (chunkkv_compress_tail)."""
     n_cap, c_max, ws = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_size_t()
-    _check("chunkkv_tail_sizes", LIB.chunkkv_tail_sizes(ctypes.byref(p), _n_prev_array(n_prev), ctypes.byref(n_cap),
-                                                        ctypes.byref(c_max), ctypes.byref(ws)))
+    _check("chunkkv_tail_sizes", LIB.chunkkv_tail_sizes(ctypes.byref(p), _n_prev_array(n_prev), n_layers, n_reuse,
+                                                        ctypes.byref(n_cap), ctypes.byref(c_max), ctypes.byref(ws)))
     return n_cap.value, c_max.value, ws.value
 
 
-def chunkkv_compress_tail(p: Params, n_prev, q_win, k, v, k_out, v_out, indices, counts, chunk_scores, ws) -> None:
-    """One incremental pass during decoding: n_prev (host ints, one per sequence) positions of each
-    cache are kept as they are, the rest is the new tail to compress (tail positions in indices)."""
+def chunkkv_compress_tail(p: Params, n_prev, n_reuse: int, q_win, k, v, k_out, v_out, indices, counts,
+                          chunk_scores, ws) -> None:
+    """One incremental pass during decoding over the layers in the lists q_win (None for reuse layers), k,
+    v, k_out, v_out: n_prev (host ints, one per sequence) positions of each cache are kept as they are,
+    the rest is the new tail to compress (tail positions in indices)."""
+    n = len(k)
     _check("chunkkv_compress_tail",
-           LIB.chunkkv_compress_tail(ctypes.byref(p), _n_prev_array(n_prev), _ptr(q_win), _ptr(k), _ptr(v),
-                                     _ptr(k_out), _ptr(v_out), _ptr(indices), _ptr(counts), _ptr(chunk_scores),
-                                     _ptr(ws), ws.numel() * ws.element_size(), _stream(counts.device)))
+           LIB.chunkkv_compress_tail(ctypes.byref(p), _n_prev_array(n_prev), n, n_reuse, _ptr_array(q_win),
+                                     _ptr_array(k), _ptr_array(v), _ptr_array(k_out), _ptr_array(v_out),
+                                     _ptr(indices), _ptr(counts), _ptr(chunk_scores), _ptr(ws),
+                                     ws.numel() * ws.element_size(), _stream(counts.device)))
 
 
 def chunkkv_layer_overlap(p: Params, indices, counts):
@@ -246,24 +250,30 @@ def compress_layers(q_win, k, v, cu_seqlens, *, Hq: int, Hkv: int, w: int, c: in
 
 
 def compress_tail(q_win, k, v, cu_seqlens, n_prev, *, Hq: int, Hkv: int, w: int, c: int, L_tail: int,
-                  return_scores: bool = False, workspace=None) -> CompressResult:
-    """Allocate outputs with torch and run chunkkv_compress_tail (one layer) on the current stream.
-    The result's indices / counts / chunk_scores carry a leading group axis of 1, like compress_layers'."""
-    p, keep = params_for(q_win, k, cu_seqlens, Hkv=Hkv, w=w, c=c, L_max=L_tail)
+                  n_reuse: int = 1, return_scores: bool = False, workspace=None) -> CompressResult:
+    """Allocate outputs with torch and run chunkkv_compress_tail on the current stream.  q_win, k, v are
+    tensors (one layer) or lists of per-layer tensors (q_win None for reuse layers)."""
+    if torch.is_tensor(k):
+        q_win, k, v = [q_win], [k], [v]
+    k0 = k[0]
+    q0 = next(x for x in q_win if x is not None)
+    p, keep = params_for(q0, k0, cu_seqlens, Hkv=Hkv, w=w, c=c, L_max=L_tail)
     assert p.Hq == Hq
-    n_cap, c_max, ws_bytes = chunkkv_tail_sizes(p, n_prev)
+    n_layers = len(k)
+    n_cap, c_max, ws_bytes = chunkkv_tail_sizes(p, n_prev, n_layers, n_reuse)
+    groups = -(-n_layers // n_reuse)
     B = len(cu_seqlens) - 1
-    dev, d = k.device, k.shape[2]
-    k_out = torch.empty(B, Hkv, n_cap, d, dtype=k.dtype, device=dev)
-    v_out = torch.empty(B, Hkv, n_cap, d, dtype=k.dtype, device=dev)
-    indices = torch.empty(1, B, Hkv, max(n_cap, 1), dtype=torch.int32, device=dev)
-    counts = torch.empty(1, B, Hkv, dtype=torch.int32, device=dev)
-    scores = torch.empty(1, B, Hkv, max(c_max, 1), dtype=torch.float32, device=dev) if return_scores else None
+    dev, d = k0.device, k0.shape[2]
+    k_out = [torch.empty(B, Hkv, n_cap, d, dtype=k0.dtype, device=dev) for _ in range(n_layers)]
+    v_out = [torch.empty(B, Hkv, n_cap, d, dtype=k0.dtype, device=dev) for _ in range(n_layers)]
+    indices = torch.empty(groups, B, Hkv, max(n_cap, 1), dtype=torch.int32, device=dev)
+    counts = torch.empty(groups, B, Hkv, dtype=torch.int32, device=dev)
+    scores = torch.empty(groups, B, Hkv, max(c_max, 1), dtype=torch.float32, device=dev) if return_scores else None
     if workspace is None:
         workspace = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
-    chunkkv_compress_tail(p, n_prev, q_win, k, v, k_out, v_out, indices, counts, scores, workspace)
+    chunkkv_compress_tail(p, n_prev, n_reuse, q_win, k, v, k_out, v_out, indices, counts, scores, workspace)
     del keep
-    return CompressResult([k_out], [v_out], indices, counts, scores, workspace)
+    return CompressResult(k_out, v_out, indices, counts, scores, workspace)
 
 
 __all__ = [

@@ -539,13 +539,14 @@ chunkkv_status tail_tables(const chunkkv_params* p, const int32_t* n_prev, TailT
 }  // namespace
 }  // namespace chunkkv
 
-chunkkv_status chunkkv_tail_sizes(const chunkkv_params* p, const int32_t* n_prev, int32_t* n_cap_max,
-                                  int32_t* C_max, size_t* ws_bytes) {
+chunkkv_status chunkkv_tail_sizes(const chunkkv_params* p, const int32_t* n_prev, int32_t n_layers, int32_t n_reuse,
+                                  int32_t* n_cap_max, int32_t* C_max, size_t* ws_bytes) {
   static thread_local TailTables t;
   chunkkv_status s = tail_tables(p, n_prev, t);
   if (s != CHUNKKV_OK) return s;
+  if (n_layers < 1 || n_reuse < 1) return CHUNKKV_ERR_INVALID_ARG;
   Plan pv, pt;
-  if ((s = make_plan(&t.pv, 1, 1, pv, nullptr)) != CHUNKKV_OK) return s;
+  if ((s = make_plan(&t.pv, n_layers, n_reuse, pv, nullptr)) != CHUNKKV_OK) return s;
   if ((s = make_plan(&t.pt, 1, 1, pt, nullptr)) != CHUNKKV_OK) return s;
   if (n_cap_max) *n_cap_max = pt.n_cap;
   if (C_max) *C_max = pt.C_max;
@@ -553,55 +554,78 @@ chunkkv_status chunkkv_tail_sizes(const chunkkv_params* p, const int32_t* n_prev
   return CHUNKKV_OK;
 }
 
-chunkkv_status chunkkv_compress_tail(const chunkkv_params* p, const int32_t* n_prev, const void* q_win,
-                                     const void* k, const void* v, void* k_out, void* v_out, int32_t* indices,
-                                     int32_t* counts, float* chunk_scores, void* ws, size_t ws_bytes,
-                                     chunkkv_stream_t stream) {
+chunkkv_status chunkkv_compress_tail(const chunkkv_params* p, const int32_t* n_prev, int32_t n_layers, int32_t n_reuse,
+                                     const void* const* q_win, const void* const* k, const void* const* v,
+                                     void* const* k_out, void* const* v_out, int32_t* indices, int32_t* counts,
+                                     float* chunk_scores, void* ws, size_t ws_bytes, chunkkv_stream_t stream) {
   static thread_local TailTables t;
   static thread_local SeqTable st_v, st_t;
   chunkkv_status s = tail_tables(p, n_prev, t);
   if (s != CHUNKKV_OK) return s;
+  if (n_layers < 1 || n_reuse < 1) return CHUNKKV_ERR_INVALID_ARG;
   Plan pv, pt;
-  if ((s = make_plan(&t.pv, 1, 1, pv, &st_v)) != CHUNKKV_OK) return s;
+  if ((s = make_plan(&t.pv, n_layers, n_reuse, pv, &st_v)) != CHUNKKV_OK) return s;
   if ((s = make_plan(&t.pt, 1, 1, pt, &st_t)) != CHUNKKV_OK) return s;
   if (pt.B * pt.Hkv == 0) return CHUNKKV_OK;
-  if ((pv.wG > 0 && (!q_win || !aligned16(q_win))) || !k || !v || !k_out || !v_out || !counts || !ws ||
-      !aligned16(k) || !aligned16(v) || !aligned16(k_out) || !aligned16(v_out) || !aligned16(ws))
-    return CHUNKKV_ERR_INVALID_ARG;
+  if (!q_win || !k || !v || !k_out || !v_out || !counts || !ws || !aligned16(ws)) return CHUNKKV_ERR_INVALID_ARG;
   if (pt.n_cap > 0 && !indices) return CHUNKKV_ERR_INVALID_ARG;
+  for (int l = 0; l < n_layers; ++l) {
+    if (l % n_reuse == 0 && pv.wG > 0 && (!q_win[l] || !aligned16(q_win[l]))) return CHUNKKV_ERR_INVALID_ARG;
+    if (!k[l] || !v[l] || !k_out[l] || !v_out[l] || !aligned16(k[l]) || !aligned16(v[l]) || !aligned16(k_out[l]) ||
+        !aligned16(v_out[l]))
+      return CHUNKKV_ERR_INVALID_ARG;
+  }
   if (ws_bytes < pv.total_bytes) return CHUNKKV_ERR_WORKSPACE_TOO_SMALL;
-  if (pv.use_tc && !device_memory(k)) return CHUNKKV_ERR_INVALID_ARG;
+  if (pv.use_tc)
+    for (int l = 0; l < n_layers; l += n_reuse)
+      if (!device_memory(k[l])) return CHUNKKV_ERR_INVALID_ARG;
+  const int n_groups = pv.n_groups;
   cudaStream_t cs = (cudaStream_t)stream;
   char* w = (char*)ws;
   char* base = w + pv.header_bytes;
-  char* slot = base + pv.off_slots;
+  char* slots = base + pv.off_slots;
   ScoreGeom g = score_geom(&t.pv, pv);
   g.pair = 1;
-  g.C_max = pt.C_max;                       // chunk scores of the tails only, [B, Hkv, C_max]
+  g.C_max = pt.C_max;                       // chunk scores of the tails only, [groups, B, Hkv, C_max]
+  g.scores_gs = (int64_t)pt.B * pt.Hkv * pt.C_max;
   float* scores = chunk_scores ? chunk_scores : (float*)(base + pv.off_scores);
-  cudaError_t e = cudaSuccess;
-  const bool direct = tc_q_direct(pv, g, q_win) && device_memory(q_win);
-  char* qpack = direct ? nullptr : base + pv.off_qpack;
-  if (pv.use_tc && pv.wG > 0 && !direct) {
-    const void* ql[1] = {q_win};
-    e = launch_pack_q(pv, g, ql, 1, qpack, cs);
+  static thread_local std::vector<const void*> qsel, ksel;
+  qsel.resize(n_groups);
+  ksel.resize(n_groups);
+  for (int i = 0; i < n_groups; ++i) {
+    qsel[i] = q_win[i * n_reuse];
+    ksel[i] = k[i * n_reuse];
   }
-  if (e == cudaSuccess) e = run_score_groups(pv, g, st_v, &q_win, &k, 1, slot, qpack, (int32_t*)w, cs);
-  if (e == cudaSuccess) e = run_post_score(pv, g, st_v, slot, scores, 1, cs);
-  if (e == cudaSuccess) e = launch_select(pt, select_geom(&t.pt, pt), st_t, scores, indices, counts, 1, cs);
+  cudaError_t e = cudaSuccess;
+  bool direct = tc_q_direct(pv, g, qsel[0]);
+  for (int i = 0; direct && i < n_groups; ++i) direct = device_memory(qsel[i]);
+  char* qpack = direct ? nullptr : base + pv.off_qpack;
+  if (pv.use_tc && pv.wG > 0 && !direct) e = launch_pack_q(pv, g, qsel.data(), n_groups, qpack, cs);
+  if (e == cudaSuccess) e = run_score_groups(pv, g, st_v, qsel.data(), ksel.data(), n_groups, slots, qpack, (int32_t*)w, cs);
+  if (e == cudaSuccess) e = run_post_score(pv, g, st_v, slots, scores, n_groups, cs);
+  SelectGeom sg = select_geom(&t.pt, pt);
+  if (e == cudaSuccess) e = launch_select(pt, sg, st_t, scores, indices, counts, n_groups, cs);
   if (e == cudaSuccess && pt.n_cap > 0) {
-    // every (cache, head) of the paired table; the kept prefixes append nothing
+    // every layer of every (cache, head) of the paired table, layer l with group l / n_reuse;
+    // the kept prefixes append nothing
     GatherGeom gg = gather_geom(&t.pt, pt);
     gg.pair = 1;
-    GatherArgs ga;
-    ga.n_layers = 1;
-    ga.k[0] = k;
-    ga.v[0] = v;
-    ga.ko[0] = k_out;
-    ga.vo[0] = v_out;
+    gg.n_reuse = n_reuse;
     Plan pg = pt;
     pg.B = pv.B;
-    e = launch_gather(pg, gg, st_v, ga, indices, counts, cs);
+    const int per_launch = std::max(1, std::min(CHUNKKV_MAX_GATHER_LAYERS, 65535 / std::max(1, pv.B * pv.Hkv)));
+    for (int l0 = 0; l0 < n_layers && e == cudaSuccess; l0 += per_launch) {
+      GatherArgs ga;
+      ga.n_layers = std::min(per_launch, n_layers - l0);
+      gg.l0 = l0;
+      for (int i = 0; i < ga.n_layers; ++i) {
+        ga.k[i] = k[l0 + i];
+        ga.v[i] = v[l0 + i];
+        ga.ko[i] = k_out[l0 + i];
+        ga.vo[i] = v_out[l0 + i];
+      }
+      e = launch_gather(pg, gg, st_v, ga, indices, counts, cs);
+    }
   }
   return cuda_status(e);
 }

@@ -180,39 +180,47 @@ chunkkv_status chunkkv_compress_layers(const chunkkv_params* p, int32_t n_layers
 /*
  * Incremental compression during decoding (the notes keep the compressed cache
  * through decoding, ChunkKV §5.6; Kara §2 Eqs. (2)-(3) compress again once the
- * cache reaches its threshold).  Sequence b of p is the current cache of one
+ * cache reaches its threshold), over n_layers layers with the index reuse of
+ * ChunkKV §4.2 Algorithm 2.  Sequence b of p is the current cache of one
  * sequence: its first n_prev[b] positions were kept by earlier passes, the
- * rest are the n_new = T_b - n_prev[b] tokens decoded since.  The pass
- * re-scores the new tail only (ChunkKV §4.1 Algorithm 1 on the tail), with
- * every window row normalised over all T_b keys of the cache:
- *   A[b][h][i] = sum over g, q and tail tokens j in chunk i of softmax over all T_b keys,
+ * rest are the n_new = T_b - n_prev[b] tokens decoded since.  A scoring layer
+ * (l % n_reuse == 0) re-scores the new tail only (ChunkKV §4.1 Algorithm 1 on
+ * the tail), with every window row normalised over all T_b keys of the cache:
+ *   A[g][b][h][i] = sum over g', q and tail tokens j in chunk i of softmax over all T_b keys,
  * chunk i being tail tokens [i*c, min(i*c + c, n_new)); it keeps the
  * min(L_max / c, ceil(n_new / c)) best tail chunks (ties to the lower index)
- * plus the last w tail tokens, and gathers them:
- *   indices[b][h][r]: ascending TAIL positions (0 = the first token after the
- *                     kept prefix), r < counts[b][h];
- *   k_out[b][h][r][:] = k[cu_seqlens[b] + n_prev[b] + indices[b][h][r]][h][:], same for v,
+ * plus the last w tail tokens into index group g = l / n_reuse, and every
+ * layer l gathers its own rows with group l / n_reuse:
+ *   indices[g][b][h][r]: ascending TAIL positions (0 = the first token after
+ *                        the kept prefix), r < counts[g][b][h];
+ *   k_out[l][b][h][r][:] = k[l][cu_seqlens[b] + n_prev[b] + indices[l / n_reuse][b][h][r]][h][:],
+ *                        same for v,
  * which the caller appends after the n_prev[b] rows it keeps.  L_max is the
- * budget for the tail of this pass.  The prefix positions are never selected
- * or moved.  Caches of different KV heads usually differ in length after a
- * pass: pass each head's cache as a sequence of its own (Hkv = 1, its G query
- * heads) when they do.
+ * budget for the tail of this pass; n_prev is the same for every layer (the
+ * layers' caches grow together).  The prefix positions are never selected or
+ * moved.  Caches of different KV heads usually differ in length after a pass:
+ * pass each head's cache as a sequence of its own (Hkv = 1, its G query heads)
+ * when they do.
  *   n_prev: HOST [B], 0 <= n_prev[b] <= T_b;
- *   q_win, k, v, k_out, v_out: as chunkkv_score / chunkkv_gather for one layer,
- *          k_out, v_out [B, Hkv, n_cap_max, d] with n_cap_max from chunkkv_tail_sizes;
- *   indices: device [B, Hkv, n_cap_max]; counts: device [B, Hkv];
- *   chunk_scores: NULL, or device [B, Hkv, C_max] (tail chunks, entries >= C_b unspecified);
- *   ws: device workspace of ws_bytes >= chunkkv_tail_sizes' ws_bytes (zero-filled
- *       before its first use, like chunkkv_workspace_size's).
+ *   q_win, k, v, k_out, v_out: HOST arrays of n_layers pointers as for
+ *          chunkkv_compress_layers; k_out[l], v_out[l] [B, Hkv, n_cap_max, d] with
+ *          n_cap_max from chunkkv_tail_sizes;
+ *   indices: device [ceil(n_layers / n_reuse), B, Hkv, n_cap_max];
+ *   counts:  device [ceil(n_layers / n_reuse), B, Hkv];
+ *   chunk_scores: NULL, or device [ceil(n_layers / n_reuse), B, Hkv, C_max] (tail
+ *          chunks; entries >= C_b unspecified);
+ *   ws: device workspace of ws_bytes >= chunkkv_tail_sizes' ws_bytes for the same
+ *       n_layers and n_reuse (zero-filled before its first use, like
+ *       chunkkv_workspace_size's).
  * B may be at most CHUNKKV_MAX_BATCH / 2 (the prefix and the tail of each cache
  * are scored as two sequences); causal_window must be 0 (CHUNKKV_ERR_UNSUPPORTED).
  */
-chunkkv_status chunkkv_tail_sizes(const chunkkv_params* p, const int32_t* n_prev, int32_t* n_cap_max,
-                                  int32_t* C_max, size_t* ws_bytes);
-chunkkv_status chunkkv_compress_tail(const chunkkv_params* p, const int32_t* n_prev, const void* q_win,
-                                     const void* k, const void* v, void* k_out, void* v_out, int32_t* indices,
-                                     int32_t* counts, float* chunk_scores, void* ws, size_t ws_bytes,
-                                     chunkkv_stream_t stream);
+chunkkv_status chunkkv_tail_sizes(const chunkkv_params* p, const int32_t* n_prev, int32_t n_layers, int32_t n_reuse,
+                                  int32_t* n_cap_max, int32_t* C_max, size_t* ws_bytes);
+chunkkv_status chunkkv_compress_tail(const chunkkv_params* p, const int32_t* n_prev, int32_t n_layers, int32_t n_reuse,
+                                     const void* const* q_win, const void* const* k, const void* const* v,
+                                     void* const* k_out, void* const* v_out, int32_t* indices, int32_t* counts,
+                                     float* chunk_scores, void* ws, size_t ws_bytes, chunkkv_stream_t stream);
 
 /*
  * Window scores for callers that cannot allocate device memory.  The ChunkKV

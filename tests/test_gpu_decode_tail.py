@@ -3,7 +3,8 @@
 A cache of one (sequence, KV head) holds the positions kept by earlier passes followed by the
 tokens decoded since.  chunkkv_compress_tail re-scores only the new tail: every window row's
 softmax runs over all keys of the cache (Kara §2 Eq. (1)), the tail is chunked from its first
-token and ChunkKV §4.1 Algorithm 1 steps 2-6 select from it.  The oracle is
+token and ChunkKV §4.1 Algorithm 1 steps 2-6 select from it; with several layers, the layers that
+do not score gather with their group's list (§4.2 Algorithm 2).  The oracle is
 oracle.compress_tail_head; the comparison rules are tests/parity.py's (scores within 1e-5 + 1e-3
 relative, indices exact unless the oracle's cut is a near-tie, gathered rows bit-exact).
 """
@@ -118,3 +119,39 @@ def test_prefill_then_two_incremental_passes(ckv):
             cache_k[h] = torch.cat([cache_k[h], out.k_out[0][h, 0, :n]])
             cache_v[h] = torch.cat([cache_v[h], out.v_out[0][h, 0, :n]])
     assert all(x.shape[0] > kept[h] for h, x in enumerate(cache_k))
+
+
+def test_tail_pass_over_layers_with_index_reuse(ckv):
+    # ChunkKV §4.2 Algorithm 2 during decoding: layers 0 and 2 re-score their new tails, layers 1 and 3
+    # gather with the index lists of layers 0 and 2 (every layer's cache has the same lengths)
+    pairs = [(700, 900), (0, 640), (1200, 75)]
+    d, G, Hkv, w, c, L, n_layers, n_reuse = 128, 4, 2, 32, 10, 150, 4, 2
+    qs, ks, vs = [], [], []
+    for layer in range(n_layers):
+        cu, q, k, v = _caches(pairs, Hkv, G, d, w, torch.bfloat16, seed=20 + layer, needle_len=2 * c)
+        qs.append(q if layer % n_reuse == 0 else None)
+        ks.append(k)
+        vs.append(v)
+    n_prev = [p for p, _ in pairs]
+    out = ckv.compress_tail(qs, ks, vs, cu, n_prev, Hq=Hkv * G, Hkv=Hkv, w=w, c=c, L_tail=L, n_reuse=n_reuse,
+                            return_scores=True)
+    assert ckv.chunkkv_status_check(out.workspace) == 0
+    scores = out.chunk_scores.cpu().numpy()
+    idx = out.indices.cpu().numpy()
+    cnt = out.counts.cpu().numpy()
+    for grp in range(n_layers // n_reuse):
+        src = oracle.scoring_layer(grp * n_reuse, n_reuse)
+        qf, kf = f64(qs[src]), f64(ks[src])
+        for b, (n_p, n_new) in enumerate(pairs):
+            for h in range(Hkv):
+                A, _, _ = oracle.compress_tail_head(oracle.group_window_rows(qf[b], h, G), kf[cu[b]:cu[b + 1], h],
+                                                    n_p, c, w, L)
+                tag = f"group {grp} cache {b} head {h}"
+                check_scores(scores[grp, b, h], A, tag)
+                n = int(cnt[grp, b, h])
+                got = idx[grp, b, h, :n]
+                check_indices(got, A, n_new, c, w, L, tag)
+                tail = slice(cu[b] + n_p, cu[b + 1])
+                for layer in range(grp * n_reuse, (grp + 1) * n_reuse):
+                    check_gather(out.k_out[layer][b, h, :n], ks[layer][tail, h], got, f"{tag} layer {layer} K'")
+                    check_gather(out.v_out[layer][b, h, :n], vs[layer][tail, h], got, f"{tag} layer {layer} V'")

@@ -235,20 +235,24 @@ def test_tail_pass_sizes_and_argument_checks(ckv):
     n_cap_, c_, w_ = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_size_t()
     out = (ctypes.byref(n_cap_), ctypes.byref(c_), ctypes.byref(w_))
 
-    def sizes(n_prev):
+    def sizes(n_prev, n_layers=1, n_reuse=1):
         arr = (ctypes.c_int32 * 2)(*n_prev) if n_prev is not None else None
-        return LIB.chunkkv_tail_sizes(P, arr, *out)
+        return LIB.chunkkv_tail_sizes(P, arr, n_layers, n_reuse, *out)
     assert sizes([501, 0]) == 1                        # a prefix longer than its cache
     assert sizes([-1, 0]) == 1
     assert sizes(None) == 1
+    assert sizes([300, 0], 0, 1) == 1 and sizes([300, 0], 4, 0) == 1      # no layers, no reuse depth
+    assert sizes([300, 0], 4, 2) == 0 and w_.value > ws                    # two scoring layers: two scratch slots
     pc, keep_c = _p(ckv, cu_seqlens=[0, 500, 1300], causal_window=True)
-    assert LIB.chunkkv_tail_sizes(ctypes.byref(pc), (ctypes.c_int32 * 2)(0, 0), *out) == 2
+    assert LIB.chunkkv_tail_sizes(ctypes.byref(pc), (ctypes.c_int32 * 2)(0, 0), 1, 1, *out) == 2
     pb, keep_b = _p(ckv, cu_seqlens=list(range(0, 600)))   # 599 caches: the paired table would exceed the batch limit
-    assert LIB.chunkkv_tail_sizes(ctypes.byref(pb), (ctypes.c_int32 * 599)(), *out) == 2
+    assert LIB.chunkkv_tail_sizes(ctypes.byref(pb), (ctypes.c_int32 * 599)(), 1, 1, *out) == 2
     # null or misaligned pointers and a short workspace are rejected before any launch
     n_prev = (ctypes.c_int32 * 2)(300, 0)
-    assert LIB.chunkkv_compress_tail(P, n_prev, None, None, None, None, None, None, None, None, None, 0, None) == 1
-    assert LIB.chunkkv_compress_tail(P, n_prev, 0x1000, 0x2008, 0x3000, 0x4000, 0x5000, 0x6000, 0x7000, None,
-                                     0x8000, ws, None) == 1
-    assert LIB.chunkkv_compress_tail(P, n_prev, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 0x7000, None,
-                                     0x8000, 16, None) == 3
+    arr = lambda x: (ctypes.c_void_p * 1)(x)
+    assert LIB.chunkkv_compress_tail(P, n_prev, 1, 1, None, None, None, None, None, None, None, None, None, 0,
+                                     None) == 1
+    assert LIB.chunkkv_compress_tail(P, n_prev, 1, 1, arr(0x1000), arr(0x2008), arr(0x3000), arr(0x4000),
+                                     arr(0x5000), 0x6000, 0x7000, None, 0x8000, ws, None) == 1
+    assert LIB.chunkkv_compress_tail(P, n_prev, 1, 1, arr(0x1000), arr(0x2000), arr(0x3000), arr(0x4000),
+                                     arr(0x5000), 0x6000, 0x7000, None, 0x8000, 16, None) == 3
