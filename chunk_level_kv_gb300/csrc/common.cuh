@@ -108,6 +108,12 @@ enum DeviceError : int32_t {
   kDevMisalignedSmem = 0x201,
 };
 
+// The workspace header (256 bytes, zero-filled before the workspace's first use):
+// int32 word 0 is the device error word; words kSchedWord and kSchedWord + 1 are
+// the tensor-core scoring launch's item counter and count of finished CTAs, which
+// the launch's last CTA sets back to zero.
+constexpr int kSchedWord = 4;
+
 // Decode a global unit id into (b, h, u).
 __device__ __forceinline__ void decode_unit(const SeqTable& st, int Hkv, int gu, int& b, int& h, int& u) {
   h = gu % Hkv;

@@ -3,7 +3,10 @@
 // ChunkKV §4.1 Algorithm 1 steps 1-3 with the probabilities of Kara §2 Eq. (1),
 // in the single-pass unit decomposition described in score.cu: each work item
 // is one (reuse group, scoring unit, 128-row M tile of the window rows), and one
-// persistent launch covers the items of every reuse group.  Per item the CTA
+// persistent launch covers the items of every reuse group.  CTAs claim items in
+// order from a counter in the workspace header (the M tiles of a unit go to CTAs
+// that start them at about the same time, so their key tiles meet in L2), and a
+// CTA that drew short items takes more.  Per item the CTA
 //   - has the item's 128 packed window rows (Q) loaded by TMA into shared
 //     memory (only when the tile differs from the previous item's),
 //   - streams the unit's keys in tiles of 80 through shared memory by TMA,
@@ -43,6 +46,9 @@ constexpr int kStagesT = 3;                    // accumulator stages in TMEM (80
 constexpr int kTmemCols = 256;
 static_assert(kStagesT >= 2 && kStagesT * kN <= kTmemCols, "TMEM budget");
 constexpr int kThreads = 192;                  // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
+// Work items handed from the producer to the MMA issuer and the softmax warps
+// through a ring in shared memory (the producer claims them from a counter).
+constexpr int kItemRing = 2;
 constexpr int kPanelQ = 128 * 128;             // one 64-element (128 B) panel of 128 rows
 constexpr int kPanelK = kN * 128;              // one 128 B panel of 80 key rows
 constexpr int kQBytes = 2 * kPanelQ;           // 32 KB per Q tile
@@ -51,6 +57,9 @@ constexpr int kKBytes = 2 * kPanelK;           // 20 KB per K tile
 // the kernel checks this and reports an error instead of computing on a
 // misaligned swizzle pattern.
 constexpr int kSmemBytes = kStagesQ * kQBytes + kStagesK * kKBytes + 256;
+// barriers, TMEM address, abort flag and item ring in the last 256 bytes
+static_assert(8 * (2 * kStagesQ + 2 * kStagesK + 2 * kStagesT + 1 + 2 * kItemRing) + 8 + 4 * kItemRing <= 256,
+              "control block");
 constexpr uint32_t kIdesc = (1u << 4)                         // D = fp32
                           | (1u << 7) | (1u << 10)           // A = B = bf16
                           | ((uint32_t)(kN >> 3) << 17)      // N
@@ -451,7 +460,8 @@ __device__ __forceinline__ void load_q(const TcMaps& maps, const TcGeom& g, cons
 template <int C, bool CAUSAL, int WG>
 __global__ void __launch_bounds__(kThreads, 2)
 score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_constant__ SeqTable st,
-                float* __restrict__ rl, bin_t* __restrict__ bins, int32_t* __restrict__ err) {
+                float* __restrict__ rl, bin_t* __restrict__ bins, int32_t* __restrict__ err,
+                int32_t* __restrict__ sched) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw;
   if (smem_u32(smem_raw) & 1023u) {                         // swizzled tiles need 1024-byte alignment
@@ -468,8 +478,11 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
   uint64_t* t_full = k_empty + kStagesK;                       // [kStagesT]
   uint64_t* t_empty = t_full + kStagesT;                       // [kStagesT]
   uint64_t* drained = t_empty + kStagesT;                      // [1] all MMAs done (teardown after a give-up)
-  uint32_t* tmem_slot = (uint32_t*)(drained + 1);
+  uint64_t* item_full = drained + 1;                           // [kItemRing]
+  uint64_t* item_empty = item_full + kItemRing;                // [kItemRing]
+  uint32_t* tmem_slot = (uint32_t*)(item_empty + kItemRing);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+  volatile int* s_items = abort_flag + 1;                      // [kItemRing] claimed item (-1: none left)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -477,6 +490,8 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
     for (int i = 0; i < kStagesK; ++i) { mbar_init(smem_u32(&k_full[i]), 1); mbar_init(smem_u32(&k_empty[i]), 1); }
     for (int i = 0; i < kStagesT; ++i) { mbar_init(smem_u32(&t_full[i]), 1); mbar_init(smem_u32(&t_empty[i]), 128); }
     mbar_init(smem_u32(drained), 1);
+    // an item is released by the MMA issuer and one lane of each softmax warp
+    for (int i = 0; i < kItemRing; ++i) { mbar_init(smem_u32(&item_full[i]), 1); mbar_init(smem_u32(&item_empty[i]), 5); }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&maps.q[0]) : "memory");
@@ -506,7 +521,15 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
       // (unit, head) read each key tile too (evict-first cost re-reads from HBM)
       const uint64_t kpol = policy_evict_normal();
       bool ok = true;
-      for (int item = blockIdx.x; item < g.n_items && ok && !*abort_flag; item += gridDim.x) {
+      for (uint32_t n = 0; ok && !*abort_flag; ++n) {
+        // claim the next item of the launch and pass it on; -1 ends every role's loop
+        const int slot = n % kItemRing;
+        if (!wait_bar(ctl, smem_u32(&item_empty[slot]), ((n / kItemRing) & 1) ^ 1, kDevTimeoutTmaProducer)) break;
+        int item = atomicAdd(&sched[0], 1);
+        if (item >= g.n_items) item = -1;
+        s_items[slot] = item;
+        mbar_arrive(smem_u32(&item_full[slot]));
+        if (item < 0) break;
         const Item it = decode_item(g, st, item);
         const CUtensorMap* kmap = &maps.k[it.grp];
         // A new window-row tile is loaded only after the first K tiles of the item
@@ -546,7 +569,12 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
       uint32_t kc = 0, qc = 0, tc = 0;                 // this warp's own counts of the same phases
       int qkey = -1;
       const uint64_t qdesc = sw128_desc(smem_u32(sQ));   // the window-row tile never moves
-      for (int item = blockIdx.x; item < g.n_items && !*abort_flag; item += gridDim.x) {
+      for (uint32_t n = 0; !*abort_flag; ++n) {
+        const int slot = n % kItemRing;
+        if (!wait_bar(ctl, smem_u32(&item_full[slot]), (n / kItemRing) & 1, kDevTimeoutMma)) break;
+        const int item = s_items[slot];
+        mbar_arrive(smem_u32(&item_empty[slot]));
+        if (item < 0) break;
         const Item it = decode_item(g, st, item);
         const int ntile = it.ntile;
         const int key = it.key;
@@ -594,7 +622,13 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
     pdl_wait();                                      // previous kernel of the stream done (and its writes visible)
     const uint32_t lane_base = tmem + ((uint32_t)(lg * 32) << 16);
     uint32_t tc = 0;
-    for (int item = blockIdx.x; item < g.n_items && !*abort_flag; item += gridDim.x) {
+    for (uint32_t n = 0; !*abort_flag; ++n) {
+      const int slot = n % kItemRing;
+      if (!wait_bar(ctl, smem_u32(&item_full[slot]), (n / kItemRing) & 1, kDevTimeoutEpilogue)) break;
+      const int item = s_items[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&item_empty[slot]));
+      if (item < 0) break;
       const Item it = decode_item(g, st, item);
       const int nk = it.nk, ntile = it.ntile;
       const int row = it.mt * 128 + rloc;
@@ -682,6 +716,15 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (threadIdx.x == 0) {
+    // The last CTA to finish (every producer has stopped claiming by then) sets
+    // the item counter back to zero for the next launch on this workspace.
+    __threadfence();
+    if (atomicAdd(&sched[1], 1) == (int)gridDim.x - 1) {
+      atomicExch(&sched[0], 0);
+      atomicExch(&sched[1], 0);
+    }
+  }
   if (*abort_flag) {
     // A role gave up: copies and MMAs this CTA started may still be in flight, and
     // they must land before its shared memory and TMEM are released.  The producer
@@ -815,6 +858,7 @@ DeviceInfo& device_info(int dev) {
 template <int C, bool CAUSAL, int WG>
 cudaError_t launch_c(const TcGeom& tg, const TcMaps& maps, const SeqTable& st, float* rl, bin_t* bins, int32_t* err,
                      int slot, cudaStream_t s) {
+  int32_t* sched = err + kSchedWord;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -824,15 +868,11 @@ cudaError_t launch_c(const TcGeom& tg, const TcMaps& maps, const SeqTable& st, f
     if (e != cudaSuccess) return e;
     di.attr_set[slot] = true;
   }
-  // A grid that is a multiple of Hkv * MT keeps each CTA on one (head, M tile)
-  // from item to item (items of a group are a multiple of Hkv * MT too), so the
-  // window-row tile changes only with the sequence or the group.
-  int grid = 2 * di.sms;
-  const int period = tg.Hkv * tg.MT;
-  if (grid >= period) grid -= grid % period;
-  grid = std::min(tg.n_items, grid);
+  // Two CTAs per SM; each claims items from the counter until none are left, so
+  // a CTA that drew short items (the last unit of a sequence) takes more.
+  const int grid = std::min(tg.n_items, 2 * di.sms);
   return launch_pdl(score_tc_kernel<C, CAUSAL, WG>, dim3(grid), dim3(kThreads), (size_t)kSmemBytes, s, maps, tg, st, rl,
-                    bins, err);
+                    bins, err, sched);
 }
 
 // Instances per chunk size: the causal window (any w*G), and without it w*G of
