@@ -242,6 +242,41 @@ def test_phase_events_mark_every_phase(ckv):
     assert all(torch.equal(a, b) for a, b in zip(out.k_out, ref.k_out))
 
 
+@pytest.mark.parametrize("n_layers,n_reuse,seqlens", [(6, 2, (2500, 0, 4100)), (64, 1, (700, 333))])
+def test_claimed_items_counter_returns_to_zero(ckv, n_layers, n_reuse, seqlens):
+    # The tensor-core scoring CTAs claim their work items from a counter in the workspace header
+    # (int32 words 4 and 5: next item, finished CTAs), which the launch's last CTA sets back to zero.
+    # Calls that share a workspace then see every item: repeated calls give identical outputs, and so
+    # does the second scoring launch of a call with more than 32 reuse groups (64 layers, N_reuse 1).
+    wl = configs.llama_model().with_params(seqlens=seqlens, B=len(seqlens), n_layers=n_layers, n_reuse=n_reuse, L_max=300,
+                                           name=f"claim_counter_{n_layers}L")
+    qs, ks, vs, spans = gen.make_all_layers(wl, DEV)
+    p, _ = ckv.make_params(cu_seqlens=wl.cu_seqlens, Hq=wl.Hq, Hkv=wl.Hkv, d=wl.d, w=wl.w, c=wl.c,
+                           L_max=wl.L_max, dtype=torch.bfloat16)
+    assert ckv.chunkkv_score_path(p) == 1
+    first, _ = run_and_check(ckv, wl, qs=qs, ks=ks, vs=vs, spans=spans,
+                             layers_to_check=None if n_layers < 10 else [0, 31, 32, 63])
+    header = lambda out: out.workspace[:32].view(torch.int32).cpu()
+    assert header(first)[4] == 0 and header(first)[5] == 0
+    kw = dict(Hq=wl.Hq, Hkv=wl.Hkv, w=wl.w, c=wl.c, L_max=wl.L_max, n_reuse=wl.n_reuse, return_scores=True)
+    cu = wl.cu_seqlens
+    n_chunks = [-(-(cu[b + 1] - cu[b]) // wl.c) for b in range(wl.B)]   # entries past them are not written
+    for _ in range(3):
+        again = ckv.compress_layers(qs, ks, vs, wl.cu_seqlens, workspace=first.workspace, **kw)
+        assert ckv.chunkkv_status_check(again.workspace) == 0
+        assert header(again)[4] == 0 and header(again)[5] == 0
+        assert torch.equal(again.counts, first.counts)
+        for b, C in enumerate(n_chunks):
+            assert torch.equal(again.chunk_scores[:, b, :, :C], first.chunk_scores[:, b, :, :C])
+            for grp in range(first.counts.shape[0]):
+                for h in range(wl.Hkv):
+                    n = int(first.counts[grp, b, h])
+                    assert torch.equal(again.indices[grp, b, h, :n], first.indices[grp, b, h, :n])
+                    for layer in range(grp * wl.n_reuse, min((grp + 1) * wl.n_reuse, wl.n_layers)):
+                        assert torch.equal(again.k_out[layer][b, h, :n], first.k_out[layer][b, h, :n])
+                        assert torch.equal(again.v_out[layer][b, h, :n], first.v_out[layer][b, h, :n])
+
+
 def test_bounded_wait_gives_up_and_reports(ckv):
     import ctypes
     from chunk_level_kv_gb300._lib import LIB
