@@ -113,6 +113,9 @@ chunkkv_status chunkkv_out_capacity(const chunkkv_params* p, int32_t* n_cap_max,
  * these shapes (n_layers, n_reuse as passed to chunkkv_compress_layers; use
  * 1, 1 for chunkkv_score).  The workspace must be zero-filled before its first
  * use (cudaMemset / torch.zeros); afterwards the library keeps it consistent.
+ * Its first 256 bytes hold the device error word (chunkkv_status_check) and the
+ * counter from which the CTAs of a tensor-core scoring launch claim their work
+ * items; the launch leaves the counter at zero when it ends.
  * One workspace must not be used by two calls that can run at the same time.
  */
 chunkkv_status chunkkv_workspace_size(const chunkkv_params* p, int32_t n_layers, int32_t n_reuse,
