@@ -19,7 +19,9 @@ cudaError_t launch_pack_q(const Plan& pl, const ScoreGeom& g, const void* const*
                           void* qpack, cudaStream_t s);
 cudaError_t launch_score_tc(const Plan& pl, const ScoreGeom& g, const SeqTable& st, const void* const* q_groups,
                             const void* const* k_groups, int n_groups, int64_t slot_bytes, float* rl, bin_t* bins,
-                            const void* qpack, int32_t* err, cudaStream_t s);
+                            const void* qpack, int32_t* err, cudaStream_t s, int mode, const float* lse);
+cudaError_t launch_sum_partials(const Plan& pl, const ScoreGeom& g, const SeqTable& st, const float* part,
+                                int64_t slot_bytes, float* scores, int n_groups, cudaStream_t s);   // score_tc.cu
 bool tc_q_direct(const Plan& pl, const ScoreGeom& g, const void* q);                   // score_tc.cu
 bool head_path(const Plan& pl, int n_groups, int sms);                                 // select.cu
 cudaError_t launch_head(const Plan& pl, const ScoreGeom& g, const SelectGeom& sg, const SeqTable& st,
@@ -210,6 +212,19 @@ ScoreGeom score_geom(const chunkkv_params* p, const Plan& pl) {
 
 chunkkv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? CHUNKKV_OK : CHUNKKV_ERR_CUDA; }
 
+// Token-level chunks (c = 1) on the tensor-core path take two passes over the
+// keys instead of one: the first forms each row's (R, l) pairs only, the
+// log-sum-exp kernel their lse, and the second sums every key's probabilities
+// over the window rows directly.  A bin per logit (16 bits per row and key,
+// written and read back) would cost more than reading the keys twice.  Not with
+// the causal window or paired sequences (they keep the single pass).  The second
+// pass's partial arrays (fp32 per token and KV head, one per warp of window rows:
+// 4 ceil(wG / 32) bytes per token and head) go where the bins would be (2 wG
+// bytes per token and head, the units covering every token): they fit for wG >= 2.
+bool two_pass(const Plan& pl, const ScoreGeom& g) {
+  return pl.use_tc && pl.c == 1 && !g.causal && !g.pair && pl.wG >= 2;
+}
+
 // Scoring of n_groups reuse groups into consecutive scratch slots from `slots`.
 // q and k hold each group's scoring layer; on the tensor-core path one
 // persistent launch covers all groups, reading the window rows from q itself
@@ -220,7 +235,9 @@ cudaError_t run_score_groups(const Plan& pl, const ScoreGeom& g, const SeqTable&
   float* rl = (float*)(slots + pl.off_rl);
   bin_t* bins = (bin_t*)(slots + pl.off_bins);
   const int64_t slot_gs = (int64_t)(pl.slot_bytes / sizeof(float));
-  if (pl.use_tc) return launch_score_tc(pl, g, st, q, k, n_groups, (int64_t)pl.slot_bytes, rl, bins, qpack, err, s);
+  if (pl.use_tc)
+    return launch_score_tc(pl, g, st, q, k, n_groups, (int64_t)pl.slot_bytes, rl, bins, qpack, err, s,
+                           two_pass(pl, g) ? 1 : 0, nullptr);
   for (int i = 0; i < n_groups; ++i) {
     cudaError_t e = launch_score_simt(pl, g, st, q[i], k[i], rl + i * slot_gs,
                                       (bin_t*)((char*)bins + i * pl.slot_bytes), s);
@@ -240,15 +257,25 @@ cudaError_t phase_mark(int i, cudaStream_t s) {
   return cudaEventRecord((cudaEvent_t)t_phase_ev[i], s);
 }
 
-// Log-sum-exp and finalisation of n_groups consecutive slots into their chunk scores.
+// Log-sum-exp and finalisation of n_groups consecutive slots into their chunk
+// scores; for two-pass token-level chunks the finalisation is the second pass
+// over the keys (q, k, qpack, err as for run_score_groups) and the sum of its
+// partial arrays.
 cudaError_t run_post_score(const Plan& pl, const ScoreGeom& g, const SeqTable& st, char* slots, float* scores,
-                           int n_groups, cudaStream_t s) {
+                           int n_groups, cudaStream_t s, const void* const* q, const void* const* k,
+                           const void* qpack, int32_t* err) {
   float* rl = (float*)(slots + pl.off_rl);
   float* lse = (float*)(slots + pl.off_lse);
+  bin_t* bins = (bin_t*)(slots + pl.off_bins);
   cudaError_t e = launch_lse(g, st, rl, lse, n_groups, s);
   if (e == cudaSuccess) e = phase_mark(3, s);
   if (e != cudaSuccess) return e;
-  return launch_finalize(pl, g, st, rl, (const bin_t*)(slots + pl.off_bins), lse, scores, n_groups, s);
+  if (two_pass(pl, g)) {
+    e = launch_score_tc(pl, g, st, q, k, n_groups, (int64_t)pl.slot_bytes, rl, bins, qpack, err, s, 2, lse);
+    if (e != cudaSuccess) return e;
+    return launch_sum_partials(pl, g, st, (const float*)bins, (int64_t)pl.slot_bytes, scores, n_groups, s);
+  }
+  return launch_finalize(pl, g, st, rl, bins, lse, scores, n_groups, s);
 }
 
 SelectGeom select_geom(const chunkkv_params* p, const Plan& pl) {
@@ -376,7 +403,8 @@ chunkkv_status chunkkv_score(const chunkkv_params* p, const void* q_win, const v
   }
   if (e == cudaSuccess)
     e = run_score_groups(pl, g, st, &q_win, &k, 1, slot, direct ? nullptr : qpack, (int32_t*)w, cs);
-  if (e == cudaSuccess) e = run_post_score(pl, g, st, slot, chunk_scores, 1, cs);
+  if (e == cudaSuccess)
+    e = run_post_score(pl, g, st, slot, chunk_scores, 1, cs, &q_win, &k, direct ? nullptr : qpack, (int32_t*)w);
   return cuda_status(e);
 }
 
@@ -478,7 +506,7 @@ chunkkv_status chunkkv_compress_layers(const chunkkv_params* p, int32_t n_layers
   if (e == cudaSuccess) e = phase_mark(2, cs);
   SelectGeom sg = select_geom(p, pl);
   sg.scores_gs = g.scores_gs;
-  if (head_path(pl, n_groups, current_sm_count())) {
+  if (!two_pass(pl, g) && head_path(pl, n_groups, current_sm_count())) {
     // enough (group, sequence, head) CTAs to fill the GPU: log-sum-exp, finalisation and selection
     // of a head in one CTA (the lse and select phases are then empty)
     if (e == cudaSuccess) e = phase_mark(3, cs);
@@ -489,7 +517,9 @@ chunkkv_status chunkkv_compress_layers(const chunkkv_params* p, int32_t n_layers
     }
     if (e == cudaSuccess) e = phase_mark(4, cs);
   } else {
-    if (e == cudaSuccess) e = run_post_score(pl, g, st, base + pl.off_slots, scores, n_groups, cs);
+    if (e == cudaSuccess)
+      e = run_post_score(pl, g, st, base + pl.off_slots, scores, n_groups, cs, qsel.data(), ksel.data(), qpack,
+                         (int32_t*)w);
     if (e == cudaSuccess) e = phase_mark(4, cs);
     if (e == cudaSuccess) e = launch_select(pl, sg, st, scores, indices, counts, n_groups, cs);
   }
@@ -602,7 +632,8 @@ chunkkv_status chunkkv_compress_tail(const chunkkv_params* p, const int32_t* n_p
   char* qpack = direct ? nullptr : base + pv.off_qpack;
   if (pv.use_tc && pv.wG > 0 && !direct) e = launch_pack_q(pv, g, qsel.data(), n_groups, qpack, cs);
   if (e == cudaSuccess) e = run_score_groups(pv, g, st_v, qsel.data(), ksel.data(), n_groups, slots, qpack, (int32_t*)w, cs);
-  if (e == cudaSuccess) e = run_post_score(pv, g, st_v, slots, scores, n_groups, cs);
+  if (e == cudaSuccess)
+    e = run_post_score(pv, g, st_v, slots, scores, n_groups, cs, qsel.data(), ksel.data(), qpack, (int32_t*)w);
   SelectGeom sg = select_geom(&t.pt, pt);
   if (e == cudaSuccess) e = launch_select(pt, sg, st_t, scores, indices, counts, n_groups, cs);
   if (e == cudaSuccess && pt.n_cap > 0) {

@@ -30,7 +30,7 @@
 
 #include <mutex>
 
-#include "common.cuh"
+#include "fin.cuh"
 
 namespace chunkkv {
 namespace tc {
@@ -282,7 +282,7 @@ struct RowState {
 // pair's two lanes are folded when a chunk ends (compile-time positions).  bin
 // points at bins[(gu*cpu + q)*wG + row], q being the unit-local chunk that holds
 // the tile's column 0.  C = 1 (token-level chunks) stores every column as a bin.
-template <int C, int PH, int SEG, bool MASK>
+template <int C, int PH, int SEG, bool MASK, bool STORE>
 __device__ __forceinline__ void tile_seg(const uint32_t (&r)[16], float2 alpha2, RowState& s, bin_t* bin, int wG,
                                          int valid, bool write, uint64_t pol) {
   static_assert(C >= 1, "compile-time chunk sizes");
@@ -298,7 +298,7 @@ __device__ __forceinline__ void tile_seg(const uint32_t (&r)[16], float2 alpha2,
       e.y = (c0 + 1 < valid) ? e.y : 0.f;
     }
     if constexpr (C == 1) {
-      if (write) {
+      if (STORE && write) {
         st_keep(bin + (size_t)c0 * wG, e.x, pol);
         st_keep(bin + (size_t)(c0 + 1) * wG, e.y, pol);
       }
@@ -324,15 +324,15 @@ __device__ __forceinline__ void tile_seg(const uint32_t (&r)[16], float2 alpha2,
 // The columns of a tile, software-pipelined: segment SEG is processed while
 // segment SEG + 1 is on its way from TMEM (one x16 load in flight beside the
 // arithmetic, 32 registers of tile data instead of 80).
-template <int C, int PH, int SEG, bool MASK>
+template <int C, int PH, int SEG, bool MASK, bool STORE>
 __device__ __forceinline__ void tile_segs_pipe(uint32_t taddr, uint32_t (&ra)[16], uint32_t (&rb)[16], float2 alpha,
                                                RowState& s, bin_t* bin, int wG, int valid, bool write, uint64_t pol) {
   if constexpr (SEG < kN / 16) {
     if constexpr (SEG + 1 < kN / 16) tmem_ld16(taddr + 16 * (SEG + 1), rb);
-    tile_seg<C, PH, SEG, MASK>(ra, alpha, s, bin, wG, valid, write, pol);
+    tile_seg<C, PH, SEG, MASK, STORE>(ra, alpha, s, bin, wG, valid, write, pol);
     if constexpr (SEG + 1 < kN / 16) {
       tmem_wait16(rb);
-      tile_segs_pipe<C, PH, SEG + 1, MASK>(taddr, rb, ra, alpha, s, bin, wG, valid, write, pol);
+      tile_segs_pipe<C, PH, SEG + 1, MASK, STORE>(taddr, rb, ra, alpha, s, bin, wG, valid, write, pol);
     }
   }
 }
@@ -383,14 +383,14 @@ __device__ __forceinline__ void tile_cols_rt(const uint32_t (&r)[kN / 16][16], f
 // One tile of kN columns: compile-time chunk sizes take the pipelined segments;
 // a chunk size known only at run time loads the whole row segment from TMEM
 // first (kN/16 x16 loads, one wait) and counts its chunk ends.
-template <int C, int PH, bool MASK>
+template <int C, int PH, bool MASK, bool STORE>
 __device__ __forceinline__ void tile_phase(uint32_t taddr, float2 alpha, RowState& s, bin_t* bin, int wG, int valid,
                                            bool write, uint64_t pol, int c, int ph) {
   if constexpr (C > 0) {
     uint32_t ra[16], rb[16];
     tmem_ld16(taddr, ra);
     tmem_wait16(ra);
-    tile_segs_pipe<C, PH, 0, MASK>(taddr, ra, rb, alpha, s, bin, wG, valid, write, pol);
+    tile_segs_pipe<C, PH, 0, MASK, STORE>(taddr, ra, rb, alpha, s, bin, wG, valid, write, pol);
   } else {
     uint32_t r[kN / 16][16];
 #pragma unroll
@@ -403,23 +403,56 @@ __device__ __forceinline__ void tile_phase(uint32_t taddr, float2 alpha, RowStat
 
 // C > 0: the tile phases ph = (t * kN) mod C are the multiples of gcd(kN, C)
 // below C, each a compile-time instance; C = 0 (chunk size c known at run time)
-// passes the phase on.
-template <int C, int PH = 0>
+// passes the phase on.  STORE = false forms the row sums only (no bins).
+template <int C, bool STORE, int PH = 0>
 __device__ __forceinline__ void tile_dispatch(int ph, bool mask, uint32_t taddr, float2 alpha, RowState& s, bin_t* bin,
                                               int wG, int valid, bool write, uint64_t pol, int c) {
   if constexpr (C == 0) {
     if (mask)
-      tile_phase<0, 0, true>(taddr, alpha, s, bin, wG, valid, write, pol, c, ph);
+      tile_phase<0, 0, true, STORE>(taddr, alpha, s, bin, wG, valid, write, pol, c, ph);
     else
-      tile_phase<0, 0, false>(taddr, alpha, s, bin, wG, valid, write, pol, c, ph);
+      tile_phase<0, 0, false, STORE>(taddr, alpha, s, bin, wG, valid, write, pol, c, ph);
   } else if constexpr (PH < C) {
     if (ph == PH) {
       if (mask)
-        tile_phase<C, PH, true>(taddr, alpha, s, bin, wG, valid, write, pol, c, ph);
+        tile_phase<C, PH, true, STORE>(taddr, alpha, s, bin, wG, valid, write, pol, c, ph);
       else
-        tile_phase<C, PH, false>(taddr, alpha, s, bin, wG, valid, write, pol, c, ph);
+        tile_phase<C, PH, false, STORE>(taddr, alpha, s, bin, wG, valid, write, pol, c, ph);
     } else {
-      tile_dispatch<C, PH + gcd_c(kN, C)>(ph, mask, taddr, alpha, s, bin, wG, valid, write, pol, c);
+      tile_dispatch<C, STORE, PH + gcd_c(kN, C)>(ph, mask, taddr, alpha, s, bin, wG, valid, write, pol, c);
+    }
+  }
+}
+
+// Token-level chunks, second pass: the row's base-2 log-sum-exp L is known, so
+// 2^(s * alpha - L) is the key's softmax probability in this row.  Each 16-column
+// segment is summed over the warp's 32 rows by a transpose reduction (fin.cuh,
+// warp_sum_each: lanes 2j and 2j + 1 end with column j's sum) and the even lanes
+// store the warp's 16 column sums to `out` (the warp's partial array at the
+// tile's column 0).  Padding rows carry L = +inf and add zeros.
+template <int SEG, bool MASK>
+__device__ __forceinline__ void direct_segs(uint32_t taddr, uint32_t (&ra)[16], uint32_t (&rb)[16], float2 alpha2,
+                                            float2 negL, float* out, int valid, int lane) {
+  if constexpr (SEG < kN / 16) {
+    if constexpr (SEG + 1 < kN / 16) tmem_ld16(taddr + 16 * (SEG + 1), rb);
+    float v[16];
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+      const int c0 = SEG * 16 + 2 * p;
+      const float2 x = make_float2(__uint_as_float(ra[2 * p]), __uint_as_float(ra[2 * p + 1]));
+      const float2 t = __ffma2_rn(x, alpha2, negL);
+      v[2 * p] = ex2(t.x);
+      v[2 * p + 1] = ex2(t.y);
+      if (MASK) {
+        v[2 * p] = (c0 < valid) ? v[2 * p] : 0.f;
+        v[2 * p + 1] = (c0 + 1 < valid) ? v[2 * p + 1] : 0.f;
+      }
+    }
+    const int col = SEG * 16 + warp_sum_each<16>(v, lane);
+    if (!(lane & 1) && (!MASK || col < valid)) out[col] = v[0];
+    if constexpr (SEG + 1 < kN / 16) {
+      tmem_wait16(rb);
+      direct_segs<SEG + 1, MASK>(taddr, rb, ra, alpha2, negL, out, valid, lane);
     }
   }
 }
@@ -457,11 +490,17 @@ __device__ __forceinline__ void load_q(const TcMaps& maps, const TcGeom& g, cons
 // WG > 0: the window rows per KV head are known at compile time (the common
 // shapes), so each bin store of the softmax takes its address as base plus an
 // immediate; WG = 0 reads them from the geometry.
-template <int C, bool CAUSAL, int WG>
+// MODE 0: bins and (R, l) pairs (single pass).  Token-level chunks (C = 1) take
+// two passes instead: MODE 1 writes only the (R, l) pairs, from which the
+// log-sum-exp kernel forms each row's lse; MODE 2 reads lse and writes each key's
+// probability summed over the rows of a warp (one partial array per warp of
+// window rows, summed by sum_partials_kernel), so no bins are written or read.
+template <int C, bool CAUSAL, int WG, int MODE = 0>
 __global__ void __launch_bounds__(kThreads, 2)
 score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_constant__ SeqTable st,
                 float* __restrict__ rl, bin_t* __restrict__ bins, int32_t* __restrict__ err,
-                int32_t* __restrict__ sched) {
+                int32_t* __restrict__ sched, const float* __restrict__ lse_rows) {
+  static_assert(MODE == 0 || (C == 1 && !CAUSAL), "two passes: token-level chunks without the causal window");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw;
   if (smem_u32(smem_raw) & 1023u) {                         // swizzled tiles need 1024-byte alignment
@@ -634,6 +673,41 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
       const int row = it.mt * 128 + rloc;
       const int wg = WG > 0 ? WG : g.wG;                            // bin stride between chunks
       const bool warp_live = it.mt * 128 + lg * 32 < g.wG;         // whole warp of padding rows: no work
+      if constexpr (MODE == 2) {
+        const float2 alpha2 = make_float2(g.alpha, g.alpha);
+        const float L = row < g.wG ? lse_rows[(int64_t)it.grp * (g.slot_bytes / 4) +
+                                              ((int64_t)it.b * g.Hkv + it.h) * g.wG + row]
+                                   : INFINITY;
+        const float2 negL = make_float2(-L, -L);
+        // this warp's partial array: warp p = 4 mt + lane quarter of the head's window rows
+        float* part = (float*)((char*)bins + it.grp * g.slot_bytes) +
+                      ((int64_t)(it.mt * 4 + lg) * g.Hkv + it.h) * st.cu[st.B] + it.tok0;
+        bool ok = true;
+        for (int t = 0; t < ntile; ++t) {
+          const int ts = tc % kStagesT;
+          if (!wait_bar(ctl, smem_u32(&t_full[ts]), (tc / kStagesT) & 1, kDevTimeoutEpilogue)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (warp_live) {
+            const uint32_t taddr = lane_base + ts * kN;
+            const int valid = min(kN, nk - t * kN);
+            uint32_t ra[16], rb[16];
+            tmem_ld16(taddr, ra);
+            tmem_wait16(ra);
+            if (valid < kN)
+              direct_segs<0, true>(taddr, ra, rb, alpha2, negL, part + t * kN, valid, lane);
+            else
+              direct_segs<0, false>(taddr, ra, rb, alpha2, negL, part + t * kN, valid, lane);
+          }
+          tc_fence_before();
+          mbar_arrive(smem_u32(&t_empty[ts]));
+          ++tc;
+        }
+        if (!ok) break;
+        continue;
+      }
       // rows that own bins; with a compile-time w*G that is a multiple of 32 every row of a live warp
       // does, which lets the bin stores go without a branch each
       const bool write = (WG > 0 && WG % 32 == 0) ? warp_live : row < g.wG;
@@ -670,7 +744,7 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
           const int ph = (t * kN) % cc;
           const int q = (t * kN) / cc;
           const RowState before = s;
-          tile_dispatch<C>(ph, mask, taddr, alpha2, s, ubins + (size_t)q * wg, wg, valid, write, bpol, cc);
+          tile_dispatch<C, MODE == 0>(ph, mask, taddr, alpha2, s, ubins + (size_t)q * wg, wg, valid, write, bpol, cc);
           // every bin is at most the row sum: one test per tile catches any value
           // that outgrew the reference (and inf / NaN)
           const bool over = !(s.l <= kBig);
@@ -681,7 +755,7 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
             const float tm = tile_max(taddr, valid) * g.alpha + kBinShift;
             const float R2 = over ? fmaxf(R, tm) : R;
             const float f = ex2(R - R2);
-            if (over && write)
+            if (MODE == 0 && over && write)
               for (int ch = 0; ch < q; ++ch)
                 ubins[(size_t)ch * g.wG] = bin_encode(bin_decode(ubins[(size_t)ch * g.wG]) * f);
             s = before;
@@ -689,7 +763,7 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
             s.carry = make_float2(s.carry.x * f, s.carry.y * f);
             R = R2;
             s.negR = make_float2(-R2, -R2);
-            tile_dispatch<C>(ph, mask, taddr, alpha2, s, ubins + (size_t)q * wg, wg, valid, write, bpol, cc);
+            tile_dispatch<C, MODE == 0>(ph, mask, taddr, alpha2, s, ubins + (size_t)q * wg, wg, valid, write, bpol, cc);
           }
         }
         tc_fence_before();
@@ -699,7 +773,7 @@ score_tc_kernel(const __grid_constant__ TcMaps maps, TcGeom g, const __grid_cons
       if (!ok) break;
       if (warp_live && write) {
         // the item ended inside a chunk (last, partial chunk of the sequence)
-        if ((ntile * kN) % cc != 0) {
+        if (MODE == 0 && (ntile * kN) % cc != 0) {
           const float cs = s.carry.x + s.carry.y;
           const int ch = (ntile * kN) / cc;
           if (ch < g.cpu) ubins[(size_t)ch * g.wG] = bin_encode(cs);
@@ -855,24 +929,25 @@ DeviceInfo& device_info(int dev) {
   return d;
 }
 
-template <int C, bool CAUSAL, int WG>
+template <int C, bool CAUSAL, int WG, int MODE = 0>
 cudaError_t launch_c(const TcGeom& tg, const TcMaps& maps, const SeqTable& st, float* rl, bin_t* bins, int32_t* err,
-                     int slot, cudaStream_t s) {
+                     int slot, cudaStream_t s, const float* lse = nullptr) {
   int32_t* sched = err + kSchedWord;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   DeviceInfo& di = device_info(dev);
   if (!di.attr_set[slot]) {
-    e = cudaFuncSetAttribute(score_tc_kernel<C, CAUSAL, WG>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    e = cudaFuncSetAttribute(score_tc_kernel<C, CAUSAL, WG, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes);
     if (e != cudaSuccess) return e;
     di.attr_set[slot] = true;
   }
   // Two CTAs per SM; each claims items from the counter until none are left, so
   // a CTA that drew short items (the last unit of a sequence) takes more.
   const int grid = std::min(tg.n_items, 2 * di.sms);
-  return launch_pdl(score_tc_kernel<C, CAUSAL, WG>, dim3(grid), dim3(kThreads), (size_t)kSmemBytes, s, maps, tg, st, rl,
-                    bins, err, sched);
+  return launch_pdl(score_tc_kernel<C, CAUSAL, WG, MODE>, dim3(grid), dim3(kThreads), (size_t)kSmemBytes, s, maps, tg,
+                    st, rl, bins, err, sched, lse);
 }
 
 // Instances per chunk size: the causal window (any w*G), and without it w*G of
@@ -898,6 +973,20 @@ cudaError_t launch_any_wg(bool causal, const TcGeom& tg, const TcMaps& maps, con
                           bin_t* bins, int32_t* err, int slot, cudaStream_t s) {
   if (causal) return launch_c<C, true, 0>(tg, maps, st, rl, bins, err, 5 * slot + 1, s);
   return launch_c<C, false, 0>(tg, maps, st, rl, bins, err, 5 * slot, s);
+}
+
+// The two passes of token-level chunks (MODE 1, MODE 2) with the same w*G
+// instances; slots 55 .. 62 of the one-time shared-memory attribute.
+template <int MODE>
+cudaError_t launch_two_pass(const TcGeom& tg, const TcMaps& maps, const SeqTable& st, float* rl, bin_t* bins,
+                            int32_t* err, const float* lse, cudaStream_t s) {
+  const int slot = 55 + 4 * (MODE - 1);
+  switch (tg.wG) {
+    case 128: return launch_c<1, false, 128, MODE>(tg, maps, st, rl, bins, err, slot + 1, s, lse);
+    case 256: return launch_c<1, false, 256, MODE>(tg, maps, st, rl, bins, err, slot + 2, s, lse);
+    case 448: return launch_c<1, false, 448, MODE>(tg, maps, st, rl, bins, err, slot + 3, s, lse);
+    default: return launch_c<1, false, 0, MODE>(tg, maps, st, rl, bins, err, slot, s, lse);
+  }
 }
 
 int lcm_i(int a, int b) { return a / gcd_c(a, b) * b; }
@@ -972,10 +1061,12 @@ bool tc_q_direct(const Plan& pl, const ScoreGeom& g, const void* q) {
 // i reads keys k_groups[i] and writes the scratch slot at rl + i * slot_gs and
 // bins + i * slot_gs (slot_gs in floats).  Window rows come from q_groups[i]
 // itself when qpack is null (tc_q_direct said yes), otherwise packed back to
-// back from qpack (launch_pack_q).
+// back from qpack (launch_pack_q).  mode 1 and 2 are the two passes of token-level
+// chunks (score_tc_kernel's MODE); mode 2 reads the rows' lse from lse + i * slot_gs
+// and writes the partial arrays into the bins' place.
 cudaError_t launch_score_tc(const Plan& pl, const ScoreGeom& g, const SeqTable& st, const void* const* q_groups,
                             const void* const* k_groups, int n_groups, int64_t slot_bytes, float* rl, bin_t* bins,
-                            const void* qpack, int32_t* err, cudaStream_t s) {
+                            const void* qpack, int32_t* err, cudaStream_t s, int mode, const float* lse) {
   const bool direct = qpack == nullptr;
   tc::EncodeFn enc = tc::encode_fn();
   if (enc == nullptr) return cudaErrorNotSupported;
@@ -1030,6 +1121,13 @@ cudaError_t launch_score_tc(const Plan& pl, const ScoreGeom& g, const SeqTable& 
     tg.timeout = 4000000000LL;     // about two seconds of clock64 cycles per wait
     float* rlg = (float*)((char*)rl + g0 * slot_bytes);
     bin_t* bg = (bin_t*)((char*)bins + g0 * slot_bytes);
+    if (mode == 1 || mode == 2) {
+      const float* lg = lse ? (const float*)((const char*)lse + g0 * slot_bytes) : nullptr;
+      const cudaError_t e = mode == 1 ? tc::launch_two_pass<1>(tg, maps, st, rlg, bg, err, lg, s)
+                                      : tc::launch_two_pass<2>(tg, maps, st, rlg, bg, err, lg, s);
+      if (e != cudaSuccess) return e;
+      continue;
+    }
     // compile-time instances (the chunk ends of every tile phase are constants) for
     // the common chunk sizes (the notes' ablation set 1, 3, 5, 10, 15, 20, 30 among
     // them); any other c >= 2 runs the C = 0 instance
@@ -1051,6 +1149,40 @@ cudaError_t launch_score_tc(const Plan& pl, const ScoreGeom& g, const SeqTable& 
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+namespace tc {
+// Token-level chunk scores from the second pass's partial arrays: the score of
+// key j of (sequence b, KV head h) is the sum, in warp order, of the n_parts
+// partial sums part[p][h][cu[b] + j] (one per warp of the head's window rows).
+__global__ void sum_partials_kernel(ScoreGeom g, const __grid_constant__ SeqTable st, const float* __restrict__ part,
+                                    int64_t slot_floats, int n_parts, float* __restrict__ scores) {
+  const int bh = blockIdx.y;
+  const int b = bh / g.Hkv, h = bh - b * g.Hkv;
+  part += blockIdx.z * slot_floats;
+  scores += blockIdx.z * g.scores_gs + (int64_t)bh * g.C_max;
+  pdl_wait();
+  const int T = st.cu[b + 1] - st.cu[b];
+  const int64_t T_total = st.cu[st.B];
+  const float* src = part + (int64_t)h * T_total + st.cu[b];
+  for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < T; j += gridDim.x * blockDim.x) {
+    float a = 0.f;
+    for (int p = 0; p < n_parts; ++p) a += __ldcs(src + (int64_t)p * g.Hkv * T_total + j);
+    scores[j] = a;
+  }
+  pdl_trigger();
+}
+}  // namespace tc
+
+// Partial arrays of n_groups consecutive slots (at `part`, slot_bytes apart)
+// into their token-level chunk scores.
+cudaError_t launch_sum_partials(const Plan& pl, const ScoreGeom& g, const SeqTable& st, const float* part,
+                                int64_t slot_bytes, float* scores, int n_groups, cudaStream_t s) {
+  if (pl.B * pl.Hkv == 0 || n_groups == 0 || pl.C_max == 0) return cudaSuccess;
+  const int n_parts = (pl.wG + 31) / 32;
+  const dim3 grid((unsigned)std::min(64, (pl.C_max + 1023) / 1024), pl.B * pl.Hkv, n_groups);
+  return launch_pdl(tc::sum_partials_kernel, grid, dim3(256), 0, s, g, st, part, slot_bytes / (int64_t)sizeof(float),
+                    n_parts, scores);
 }
 
 cudaError_t launch_wait_selftest(int32_t* err, long long timeout, cudaStream_t s) {

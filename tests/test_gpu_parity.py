@@ -114,6 +114,8 @@ def test_tiny_fp32_exact(ckv):
     (1999, 2, 32, 28, 4, 200),       # c = 2, window rows 224: a chunk end in every column pair
     (4100, 100, 16, 16, 4, 1000),    # c = 100: chunks spanning tiles, a whole-tile unit of 400 keys
     (3000, 1, 32, 28, 4, 256),       # token-level selection on 224 window rows (two M tiles)
+    (3001, 1, 64, 28, 4, 700),       # token-level, two passes on 448 window rows (last M tile half padding)
+    (2600, 1, 32, 32, 8, 400),       # token-level, two passes on 128 window rows
 ])
 def test_bf16_shapes(ckv, T, c, w, Hq, Hkv, L_max):
     wl = configs.llama_layer().with_params(seqlens=(T,), c=c, w=w, Hq=Hq, Hkv=Hkv, L_max=L_max,

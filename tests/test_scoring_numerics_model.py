@@ -181,3 +181,80 @@ def test_a_rescale_that_forgets_the_written_codes_breaks_the_tolerance():
     rows, keys = _rescale_case()
     with pytest.raises(AssertionError):
         _check(rows, keys, 10, 240, rescale_codes=False)
+
+
+# ---------------------------------------------------------------- token-level chunks: two passes
+def model_two_pass_token_scores(rows, keys, unit_keys, drop_lse_of_later_items=False):
+    """Per-token scores (c = 1) of one KV head by the two-pass scheme of the tensor-core path.
+
+    Pass 1 forms each work item's (R, l) per row exactly as the single pass does (R = first-tile
+    maximum + 86, l summed in fp32, a row whose l outgrows the bound moves R to that tile's maximum and
+    rescales l), but writes no bins; the rows' base-2 log-sum-exps merge the pairs of all items.  Pass 2
+    recomputes the logits and forms 2^(t - lse) in fp32, sums them per key over each warp's 32 rows,
+    then over the warps in order.  drop_lse_of_later_items plants a fault: the normaliser of a row is
+    that of its first item only.
+    """
+    T, d = keys.shape
+    n_rows = rows.shape[0]
+    alpha = np.float32(1.0 / math.log(2) / math.sqrt(d))
+    s_all = (rows.astype(np.float32) @ keys.astype(np.float32).T).astype(np.float32)
+    pairs = []
+    for k0 in range(0, T, unit_keys):
+        nk = min(unit_keys, T - k0)
+        s = s_all[:, k0:k0 + nk]
+        R = (s[:, :min(TILE, nk)].max(axis=1) * alpha + np.float32(SHIFT)).astype(np.float32)
+        l = np.zeros(n_rows, np.float32)
+        for t0 in range(0, nk, TILE):
+            blk = s[:, t0:min(t0 + TILE, nk)]
+            l_t = (l + np.exp2((blk * alpha - R[:, None]).astype(np.float32)).astype(np.float32).sum(axis=1,
+                                                                                                 dtype=np.float32))
+            over = ~(l_t <= BIG)
+            if over.any():
+                tm = (blk.max(axis=1) * alpha + np.float32(SHIFT)).astype(np.float32)
+                R2 = np.where(over, np.maximum(R, tm), R).astype(np.float32)
+                l = (l * np.exp2((R - R2).astype(np.float32))).astype(np.float32)
+                R = R2
+                l_t = (l + np.exp2((blk * alpha - R[:, None]).astype(np.float32)).astype(np.float32).sum(
+                    axis=1, dtype=np.float32))
+            l = l_t.astype(np.float32)
+        pairs.append((R, l))
+    if drop_lse_of_later_items:
+        pairs = pairs[:1]
+    M = np.full(n_rows, -np.inf, np.float32)
+    S = np.zeros(n_rows, np.float32)
+    for R, l in pairs:
+        Mn = np.maximum(M, R)
+        S = (S * np.exp2(M - Mn) + l * np.exp2(R - Mn)).astype(np.float32)
+        M = Mn
+    lse = (M + np.log2(S)).astype(np.float32)
+    p = np.exp2((s_all * alpha - lse[:, None]).astype(np.float32)).astype(np.float32)
+    A = np.zeros(T, np.float32)
+    for r0 in range(0, n_rows, 32):                     # warp partial sums, then the warps in order
+        A = (A + p[r0:r0 + 32].sum(axis=0, dtype=np.float32)).astype(np.float32)
+    return A.astype(np.float64)
+
+
+def _check_two_pass(rows, keys, unit_keys, **kw):
+    rows, keys = _bf16(rows), _bf16(keys)
+    got = model_two_pass_token_scores(rows, keys, unit_keys, **kw)
+    want = _oracle(rows, keys, 1)
+    err = np.abs(got - want) / (ATOL + RTOL * np.abs(want))
+    assert err.max() <= 1.0, f"worst error {err.max():.3f} of the tolerance at key {int(err.argmax())}"
+    return err.max()
+
+
+def test_two_pass_token_level_model_matches_the_oracle():
+    rng = np.random.default_rng(7)
+    worst = _check_two_pass(rng.standard_normal((128, 128)), rng.standard_normal((1500, 128)), 240)
+    assert worst < 0.05                                 # fp32 sums: far inside the tolerance
+    rows, keys = _rescale_case()                        # rows whose maximum climbs past the first tile's
+    _check_two_pass(rows, keys, 240)
+    rows, keys = _ramp_case()
+    _check_two_pass(rows, keys, 160)
+
+
+def test_two_pass_needs_the_normaliser_over_every_item():
+    # planted fault: a row's lse from its first item alone scores every key too high
+    rows, keys = _rescale_case()
+    with pytest.raises(AssertionError):
+        _check_two_pass(rows, keys, 240, drop_lse_of_later_items=True)
