@@ -260,6 +260,140 @@ __device__ __forceinline__ void select_head(const SelectGeom& sg, int T, const f
   if (tid == 0) *count = rec0 + (T - Rs);
 }
 
+// The same for kSelRegThreads * 16 < C <= kSelSmemChunks: the order keys sit in
+// shared memory (dynamic, C words) instead of registers, thread t owning chunks
+// t*n .. t*n+n-1 (n = ceil(C / 1024) <= 32), so the radix passes read them there
+// and not from global memory as select_kernel does.
+constexpr int kSelSmemChunks = 32 * kSelRegThreads;
+
+__device__ __forceinline__ void select_head_smem(const SelectGeom& sg, int T, const float* A, int32_t* out,
+                                                 int32_t* count, uint32_t* skey) {
+  using Scan = cub::BlockScan<int, kSelRegThreads>;
+  constexpr int BPT = kSelBins / kSelRegThreads;
+  __shared__ typename Scan::TempStorage scan_tmp;
+  __shared__ int hist[kSelBins];
+  __shared__ uint32_t sh_prefix;
+  __shared__ int sh_remaining, sh_straddle;
+  const int tid = threadIdx.x;
+  const int c = sg.c;
+  const int C = (T + c - 1) / c;
+  const int k = min(sg.L_max / c, C);
+  const int n = (C + kSelRegThreads - 1) / kSelRegThreads;   // chunks per thread (<= 32)
+  const int i0 = tid * n;
+  for (int i = tid; i < C; i += kSelRegThreads) skey[i] = order_key(__ldcg(A + i));
+  __syncthreads();
+
+  // ---- threshold: the k-th largest key, and how many keys equal to it are kept
+  uint32_t thr = 0;
+  int need_eq = 0;
+  if (k > 0 && k < C) {
+    uint32_t prefix = 0, mask = 0;
+    int remaining = k;
+#pragma unroll 1
+    for (int pass = 0; pass < 3; ++pass) {
+      const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+      const uint32_t dmask = pass == 2 ? 1023u : 2047u;
+      for (int i = tid; i < kSelBins; i += kSelRegThreads) hist[i] = 0;
+      __syncthreads();
+      for (int i = tid; i < C; i += kSelRegThreads) {
+        const uint32_t key = skey[i];
+        if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & dmask], 1);
+      }
+      __syncthreads();
+      // descending digits: thread t holds bins 2047 - BPT*t - i
+      int cnt[BPT], tot = 0;
+#pragma unroll
+      for (int i = 0; i < BPT; ++i) {
+        cnt[i] = hist[kSelBins - 1 - (BPT * tid + i)];
+        tot += cnt[i];
+      }
+      int excl;
+      Scan(scan_tmp).ExclusiveSum(tot, excl);
+#pragma unroll
+      for (int i = 0; i < BPT; ++i) {
+        if (excl < remaining && excl + cnt[i] >= remaining) {
+          sh_prefix = prefix | ((uint32_t)(kSelBins - 1 - (BPT * tid + i)) << shift);
+          sh_remaining = remaining - excl;
+        }
+        excl += cnt[i];
+      }
+      __syncthreads();
+      prefix = sh_prefix;
+      remaining = sh_remaining;
+      mask |= dmask << shift;
+    }
+    thr = prefix;
+    need_eq = remaining;
+  }
+
+  // ---- keep flags of this thread's chunks (bit j: chunk i0 + j): above the threshold, or equal to
+  // it and among the first need_eq in index order
+  uint32_t keep = 0, eq = 0;
+  int n_eq = 0;
+  for (int j = 0; j < n; ++j) {
+    const int i = i0 + j;
+    if (i < C && k > 0) {
+      if (k >= C) {
+        keep |= 1u << j;
+      } else {
+        const uint32_t key = skey[i];
+        if (key > thr) keep |= 1u << j;
+        if (key == thr) { eq |= 1u << j; ++n_eq; }
+      }
+    }
+  }
+  if (tid == 0) sh_straddle = 0;
+  int eq_base;
+  Scan(scan_tmp).ExclusiveSum(n_eq, eq_base);
+  __syncthreads();
+  for (int j = 0; j < n; ++j)
+    if ((eq >> j) & 1u) {
+      if (eq_base < need_eq) keep |= 1u << j;
+      ++eq_base;
+    }
+
+  // ---- expansion: whole kept chunks below Rs = max(0, T - w) land at rank * c, in order
+  const int Rs = max(0, T - sg.w);
+  const int sc = Rs / c;
+  const int part = Rs - sc * c;
+  int n_low = 0;
+  for (int j = 0; j < n; ++j) n_low += ((keep >> j) & 1u) && (i0 + j < sc);
+  int rank, low_tot;
+  Scan(scan_tmp).ExclusiveSum(n_low, rank, low_tot);
+  __syncthreads();
+  for (int j = 0; j < n; ++j) {
+    const int i = i0 + j;
+    if (((keep >> j) & 1u) && i < sc) {
+      int32_t* o = out + (int64_t)rank * c;
+      for (int t = 0; t < c; ++t) o[t] = i * c + t;
+      ++rank;
+    }
+    if (i == sc && part > 0 && ((keep >> j) & 1u)) sh_straddle = 1;
+  }
+  __syncthreads();
+  const int tail0 = low_tot * c;
+  const int strad = sh_straddle ? part : 0;
+  for (int t = tid; t < strad; t += kSelRegThreads) out[tail0 + t] = sc * c + t;
+  const int rec0 = tail0 + strad;
+  for (int t = tid; t < T - Rs; t += kSelRegThreads) out[rec0 + t] = Rs + t;
+  if (tid == 0) *count = rec0 + (T - Rs);
+}
+
+__global__ void __launch_bounds__(kSelRegThreads)
+select_smem_kernel(SelectGeom sg, const __grid_constant__ SeqTable st, const float* __restrict__ scores,
+                   int32_t* __restrict__ indices, int32_t* __restrict__ counts) {
+  extern __shared__ uint32_t skey[];
+  const int bh = blockIdx.x;
+  const int b = bh / sg.Hkv;
+  const int T = st.cu[b + 1] - st.cu[b];
+  const float* A = scores + blockIdx.y * sg.scores_gs + (int64_t)bh * sg.C_max;
+  int32_t* out = indices + blockIdx.y * sg.idx_gs + (int64_t)bh * sg.n_cap;
+  counts += blockIdx.y * sg.cnt_gs;
+  pdl_wait();
+  select_head_smem(sg, T, A, out, counts + bh, skey);
+  pdl_trigger();
+}
+
 // THREADS < kSelRegThreads: several CTAs per SM, for calls with more heads than SMs.
 template <int ITEMS, int THREADS>
 __global__ void __launch_bounds__(THREADS, kSelRegThreads / THREADS)
@@ -389,6 +523,13 @@ cudaError_t launch_select(const Plan& pl, const SelectGeom& sg, const SeqTable& 
   if (pl.C_max <= kSelRegThreads * 16)
     return launch_pdl(select_reg_kernel<16, kSelRegThreads>, grid, dim3(kSelRegThreads), 0, s, sg, st, scores,
                       indices, counts);
+  if (pl.C_max <= kSelSmemChunks) {
+    const size_t smem = (size_t)pl.C_max * sizeof(uint32_t);
+    const cudaError_t e =
+        cudaFuncSetAttribute(select_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(select_smem_kernel, grid, dim3(kSelRegThreads), smem, s, sg, st, scores, indices, counts);
+  }
   return launch_pdl(select_kernel, grid, dim3(kSelThreads), 0, s, sg, st, scores, indices, counts);
 }
 

@@ -112,12 +112,14 @@ def test_outputs_beyond_counts_are_left_unwritten(ckv, n_layers):
 
 
 @pytest.mark.parametrize("many_heads,C_max", [
-    (False, 4096), (False, 4097), (False, 13312), (False, 13313), (False, 16384), (False, 16385),
+    (False, 4096), (False, 4097), (False, 13312), (False, 13313), (False, 16384), (False, 16385), (False, 32768),
+    (False, 32769),
     (True, 2048), (True, 2049), (True, 4096), (True, 4097), (True, 6144), (True, 6145)])
 def test_select_instances_at_their_limits(ckv, many_heads, C_max):
     # the selection's instance follows the chunk capacity and whether the heads fit one wave: 4, 13 or
-    # 16 keys a thread at 1024 threads and the general kernel above 16384 chunks; with more heads than
-    # SMs, 8 / 8 / 12 keys at 256 / 512 / 512 threads up to 6144 chunks.  Each limit and the next size,
+    # 16 keys a thread at 1024 threads, the keys in shared memory up to 32768 chunks and the general
+    # kernel above; with more heads than SMs, 8 / 8 / 12 keys at 256 / 512 / 512 threads up to 6144
+    # chunks.  Each limit and the next size,
     # bit-exact against the oracle on ragged sequences (one empty, one with a ragged last chunk
     # straddling the window), half of the heads with many tied scores
     sms = torch.cuda.get_device_properties(DEV).multi_processor_count
