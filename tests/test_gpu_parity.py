@@ -538,8 +538,10 @@ def test_compress_with_host_resident_kv(ckv):
     assert e.value.code == 1                  # CHUNKKV_ERR_INVALID_ARG, nothing launched
 
 
-def test_score_entry_point_alone(ckv):
-    wl = configs.llama_layer().with_params(seqlens=(5000, 3000), B=2, name="score_only")
+@pytest.mark.parametrize("c", [10, 1])
+def test_score_entry_point_alone(ckv, c):
+    # c = 1 takes the two passes over the keys (row lse, then per-key sums) inside chunkkv_score too
+    wl = configs.llama_layer().with_params(seqlens=(5000, 3000), B=2, c=c, name=f"score_only_c{c}")
     q, k, v, _ = gen.make_all_layers(wl, DEV)
     p, keep = ckv.params_for(q[0], k[0], wl.cu_seqlens, Hkv=wl.Hkv, w=wl.w, c=wl.c, L_max=wl.L_max)
     n_cap, C_max = ckv.chunkkv_out_capacity(p)
