@@ -306,6 +306,8 @@ def workload_of(args):
         wl = wl.with_params(c=c, L_max=L, name=f"{base}_c{c}_L{L}")
     if args.layers:
         wl = wl.with_params(n_layers=args.layers, name=f"{wl.name}_first{args.layers}L")
+    if getattr(args, "causal", False):
+        wl = wl.with_params(name=f"{wl.name}_causal")
     return wl
 
 
@@ -315,7 +317,7 @@ def device_timing(ckv, wl, args, dev, local, ws_n, peaks, peak_src, ex2_rate):
     measured figures of the workload."""
     qs, ks, vs, _ = gen.make_all_layers(wl, dev)
     p, keep = ckv.params_for(next(q for q in qs if q is not None), ks[0], wl.cu_seqlens, Hkv=wl.Hkv, w=wl.w,
-                             c=wl.c, L_max=wl.L_max)
+                             c=wl.c, L_max=wl.L_max, causal_window=getattr(args, "causal", False))
     n_cap, C_max = ckv.chunkkv_out_capacity(p)
     groups = -(-wl.n_layers // wl.n_reuse)
     ko = [torch.empty(wl.B, wl.Hkv, n_cap, wl.d, dtype=ks[0].dtype, device=dev) for _ in range(wl.n_layers)]
@@ -584,7 +586,7 @@ def run_gpu(args):
                       "ms_per_step": round(staged_ms, 4)}
 
     cpu = None
-    if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
+    if rank == 0 and ws_n == 1 and not args.no_cpu_baseline and not args.causal:   # the oracle sample has no causal window
         cpu = cpu_baseline(args, budget_s=args.cpu_seconds)
 
     if ws_n > 1:
@@ -598,7 +600,7 @@ def run_gpu(args):
         "config": {"workload": wl.name, "B": wl.B, "T": list(wl.seqlens) if wl.B <= 4 else "ragged",
                    "T_total": wl.T_total, "layers": wl.n_layers, "n_reuse": wl.n_reuse, "Hq": wl.Hq,
                    "Hkv": wl.Hkv, "d": wl.d, "w": wl.w, "c": wl.c, "L_max": wl.L_max,
-                   "l2": t["l2_note"], "parallelism": f"replicas x{ws_n}"},
+                   "causal_window": bool(args.causal), "l2": t["l2_note"], "parallelism": f"replicas x{ws_n}"},
         "tokens_per_s": round(t["tokens_s"], 1),
         "token_layers_per_s": round(t["tokens_s"] * wl.n_layers, 1),
         "algorithmic_bytes_per_step": nbytes,
@@ -614,6 +616,106 @@ def run_gpu(args):
         "e2e_staged": e2e_staged,
         "gpu_launches": int(t["launches"]),
         "clocks": t["clocks"],
+    }
+    print(json.dumps(line), flush=True)
+
+
+def tail_case(base, n_new: int):
+    """The caches of an incremental pass over workload `base`: (workload of the caches, kept prefix per
+    sequence, the tail's budget).  A prefill pass keeps at most k c + w positions of a prompt (k =
+    L_max // c chunks and the window), so each cache is that prefix followed by n_new decoded tokens; the
+    tail's budget keeps the prefill's ratio L_max / T over the longest prompt, at least one chunk."""
+    n_prev = [min(T, base.L_max // base.c * base.c + base.w) for T in base.seqlens]
+    L_tail = max(base.c, base.L_max * n_new // max(base.seqlens))
+    wl = base.with_params(seqlens=tuple(x + n_new for x in n_prev), B=len(n_prev), name=f"{base.name}_tail{n_new}")
+    return wl, n_prev, L_tail
+
+
+def run_tail(args):
+    """Incremental pass during decoding (chunkkv_compress_tail): every cache of the workload holds the
+    positions a prefill pass kept (min(T_b, k c + w) of its prompt) followed by args.tail decoded
+    tokens; each pass re-scores that tail against the whole cache on the scoring layers and gathers the
+    kept tail rows of every layer.  The tail's budget keeps the prefill's ratio (L_max / T_b).  Device
+    time per pass with the inputs resident in HBM; bytes counted as for the prefill path (the whole
+    cache's keys on each scoring layer, Q_w, and the kept rows' K and V read and written)."""
+    import chunk_level_kv_gb300 as ckv
+    ws_n, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws_n > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    peaks, peak_src = measured_peaks()
+    n_new = args.tail
+    wl, n_prev, L_tail = tail_case(workload_of(args), n_new)
+    qs, ks, vs, _ = gen.make_all_layers(wl, dev)
+    p, keep = ckv.params_for(next(q for q in qs if q is not None), ks[0], wl.cu_seqlens, Hkv=wl.Hkv, w=wl.w,
+                             c=wl.c, L_max=L_tail)
+    n_cap, c_max, ws_bytes = ckv.chunkkv_tail_sizes(p, n_prev, wl.n_layers, wl.n_reuse)
+    groups = -(-wl.n_layers // wl.n_reuse)
+    ko = [torch.empty(wl.B, wl.Hkv, max(n_cap, 1), wl.d, dtype=ks[0].dtype, device=dev) for _ in range(wl.n_layers)]
+    vo = [torch.empty_like(x) for x in ko]
+    idx = torch.empty(groups, wl.B, wl.Hkv, max(n_cap, 1), dtype=torch.int32, device=dev)
+    cnt = torch.empty(groups, wl.B, wl.Hkv, dtype=torch.int32, device=dev)
+    ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ckv.chunkkv_compress_tail(p, n_prev, wl.n_reuse, qs, ks, vs, ko, vo, idx, cnt, None, ws)
+
+    for _ in range(args.warmup):
+        step()
+    ckv.chunkkv_status_check(ws)
+    in_bytes = sum(x.numel() * x.element_size() for x in ks + vs)
+    l2_note = "inputs larger than L2 (no flush)" if in_bytes > 2 * 129e6 else "L2 flushed between steps"
+    flush = torch.empty(int(2 * 129e6) // 4, dtype=torch.float32, device=dev) if in_bytes <= 2 * 129e6 else None
+    sampler = ClockSampler(local)
+    if ws_n > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    launches0 = ckv.chunkkv_launch_count()
+    times = []
+    for _ in range(args.steps):
+        if flush is not None:
+            flush.fill_(1.0)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        times.append((e0, e1))
+    torch.cuda.synchronize()
+    launches = ckv.chunkkv_launch_count() - launches0
+    if ws_n > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    ms = [a.elapsed_time(b) for a, b in times]
+    ckv.chunkkv_status_check(ws)
+    step_ms = slowest_rank(sum(ms) / len(ms), ws_n)
+    nbytes = algorithmic_bytes(wl, cnt)
+    value = job_rate(nbytes, ws_n, step_ms) / 1e9
+    del keep
+    if rank != 0:
+        return
+    hbm = peaks["hbm_gbs"]
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": ws_n, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic (seeded, needles planted)",
+        "config": {"workload": wl.name, "mode": "incremental pass during decoding", "B": wl.B, "n_prev": n_prev,
+                   "tail": n_new, "layers": wl.n_layers, "n_reuse": wl.n_reuse, "Hq": wl.Hq, "Hkv": wl.Hkv,
+                   "d": wl.d, "w": wl.w, "c": wl.c, "L_tail": L_tail, "l2": l2_note,
+                   "parallelism": f"replicas x{ws_n}"},
+        "tail_tokens_per_s": round(job_rate(n_new * wl.B, ws_n, step_ms), 1),
+        "algorithmic_bytes_per_step": nbytes,
+        "hbm_roof_frac": round(value / ws_n / hbm, 4),
+        "roofline": {"bound": "hbm", "achieved": round(value / ws_n, 2), "peak": hbm, "unit": "GB/s",
+                     "frac": round(value / ws_n / hbm, 4), "traffic": None, "kernel": "whole pass",
+                     "peak_source": f"{peak_src} hbm_gbs"},
+        "cpu_baseline": None, "e2e": None,
+        "gpu_launches": int(launches),
+        "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
 
@@ -752,6 +854,9 @@ def main():
     ap.add_argument("--layers", type=int, default=0, help="keep only the first N layers (profiling)")
     ap.add_argument("--chunk", type=int, default=0, help="chunk size c instead of the workload's (a sweep point)")
     ap.add_argument("--budget", type=int, default=0, help="L_max instead of the workload's (a sweep point)")
+    ap.add_argument("--causal", action="store_true", help="causal window (chunkkv_params.causal_window)")
+    ap.add_argument("--tail", type=int, default=0,
+                    help="time the incremental pass during decoding with this many new tokens per cache instead")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-baseline-child", action="store_true", help=argparse.SUPPRESS)
@@ -762,6 +867,8 @@ def main():
         run_cpu_baseline_child(args)
     elif args.impl == "reference":
         run_reference(args)
+    elif args.tail > 0:
+        run_tail(args)
     else:
         run_gpu(args)
 

@@ -102,3 +102,17 @@ def test_cpulist_parsing():
     assert bench.parse_cpulist("0-3,8,10-11\n") == {0, 1, 2, 3, 8, 10, 11}
     assert bench.parse_cpulist("72-143") == set(range(72, 144))
     assert bench.parse_cpulist("") == set()
+
+
+def test_tail_case_keeps_the_prefill_prefix_and_ratio():
+    import bench
+    from synthetic import configs
+    base = configs.llama_model()
+    wl, n_prev, L_tail = bench.tail_case(base, 4096)
+    kept = base.L_max // base.c * base.c + base.w            # k c + w positions of a prefill pass
+    assert n_prev == [min(T, kept) for T in base.seqlens] and wl.seqlens == tuple(x + 4096 for x in n_prev)
+    assert L_tail == base.L_max * 4096 // max(base.seqlens) and wl.B == base.B and wl.n_layers == base.n_layers
+    rag = configs.mistral_ragged()
+    wl, n_prev, L_tail = bench.tail_case(rag, 100)
+    assert all(p <= T for p, T in zip(n_prev, rag.seqlens)) and L_tail == rag.c    # one chunk at least
+    assert wl.cu_seqlens[-1] == sum(n_prev) + 100 * rag.B
