@@ -695,6 +695,18 @@ def run_tail(args):
     step_ms = slowest_rank(sum(ms) / len(ms), ws_n)
     nbytes = algorithmic_bytes(wl, cnt)
     value = job_rate(nbytes, ws_n, step_ms) / 1e9
+    # device time of each phase: K more passes with the library's phase events
+    n_ev = len(ckv.PHASES) + 1
+    phase_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
+    for evs in phase_evs:
+        if flush is not None:
+            flush.fill_(1.0)
+        ckv.chunkkv_set_phase_events(evs)
+        step()
+    ckv.chunkkv_set_phase_events(None)
+    torch.cuda.synchronize()
+    phase_ms = {name: sum(evs[i].elapsed_time(evs[i + 1]) for evs in phase_evs) / len(phase_evs)
+                for i, name in enumerate(ckv.PHASES)}
     del keep
     if rank != 0:
         return
@@ -708,6 +720,7 @@ def run_tail(args):
                    "d": wl.d, "w": wl.w, "c": wl.c, "L_tail": L_tail, "l2": l2_note,
                    "parallelism": f"replicas x{ws_n}"},
         "tail_tokens_per_s": round(job_rate(n_new * wl.B, ws_n, step_ms), 1),
+        "phases_ms": {k: round(v, 5) for k, v in phase_ms.items()},
         "algorithmic_bytes_per_step": nbytes,
         "hbm_roof_frac": round(value / ws_n / hbm, 4),
         "roofline": {"bound": "hbm", "achieved": round(value / ws_n, 2), "peak": hbm, "unit": "GB/s",

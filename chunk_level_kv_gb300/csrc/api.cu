@@ -627,15 +627,24 @@ chunkkv_status chunkkv_compress_tail(const chunkkv_params* p, const int32_t* n_p
     ksel[i] = k[i * n_reuse];
   }
   cudaError_t e = cudaSuccess;
+  struct InCompress {                   // phase events are recorded inside this call too
+    InCompress() { t_in_compress = true; }
+    ~InCompress() { t_in_compress = false; }
+  } in_compress;
   bool direct = tc_q_direct(pv, g, qsel[0]);
   for (int i = 0; direct && i < n_groups; ++i) direct = device_memory(qsel[i]);
   char* qpack = direct ? nullptr : base + pv.off_qpack;
-  if (pv.use_tc && pv.wG > 0 && !direct) e = launch_pack_q(pv, g, qsel.data(), n_groups, qpack, cs);
+  e = phase_mark(0, cs);
+  if (e == cudaSuccess && pv.use_tc && pv.wG > 0 && !direct) e = launch_pack_q(pv, g, qsel.data(), n_groups, qpack, cs);
+  if (e == cudaSuccess) e = phase_mark(1, cs);
   if (e == cudaSuccess) e = run_score_groups(pv, g, st_v, qsel.data(), ksel.data(), n_groups, slots, qpack, (int32_t*)w, cs);
+  if (e == cudaSuccess) e = phase_mark(2, cs);
   if (e == cudaSuccess)
     e = run_post_score(pv, g, st_v, slots, scores, n_groups, cs, qsel.data(), ksel.data(), qpack, (int32_t*)w);
+  if (e == cudaSuccess) e = phase_mark(4, cs);
   SelectGeom sg = select_geom(&t.pt, pt);
   if (e == cudaSuccess) e = launch_select(pt, sg, st_t, scores, indices, counts, n_groups, cs);
+  if (e == cudaSuccess) e = phase_mark(5, cs);
   if (e == cudaSuccess && pt.n_cap > 0) {
     // every layer of every (cache, head) of the paired table, layer l with group l / n_reuse;
     // the kept prefixes append nothing
@@ -658,6 +667,7 @@ chunkkv_status chunkkv_compress_tail(const chunkkv_params* p, const int32_t* n_p
       e = launch_gather(pg, gg, st_v, ga, indices, counts, cs);
     }
   }
+  if (e == cudaSuccess) e = phase_mark(6, cs);
   return cuda_status(e);
 }
 

@@ -324,19 +324,22 @@ int32_t chunkkv_score_path(const chunkkv_params* p);
 uint64_t chunkkv_launch_count(void);
 
 /*
- * Phase timing of chunkkv_compress_layers (a measurement aid).
+ * Phase timing of chunkkv_compress_layers and chunkkv_compress_tail (a
+ * measurement aid).
  *   events: HOST array of CHUNKKV_PHASE_EVENTS cudaEvent_t handles (as void*)
  *           that the caller created and keeps alive; NULL with n_events = 0
  *           switches recording off.
- * While set, each chunkkv_compress_layers call made by the same host thread
- * records events[i] on its stream at phase boundary i: 0 before the window-row
- * packing (a phase without a launch when the scoring kernel reads the window
- * rows from q_win itself: w divides 128), 1 before scoring, 2 before the log-sum-exp, 3 before the
- * finalisation, 4 before the top-k selection, 5 before the gather, 6 after the
- * gather.  When one kernel takes the log-sum-exp, the finalisation and the
- * selection (calls with enough (group, sequence, head) triples to fill the
- * GPU), boundaries 2 and 3 come before it and 4 after it, so its time shows as
- * the finalisation's.  A record between two launches ends the
+ * While set, each chunkkv_compress_layers or chunkkv_compress_tail call made
+ * by the same host thread records events[i] on its stream at phase boundary i:
+ * 0 before the window-row packing (a phase without a launch when the scoring
+ * kernel reads the window rows from q_win itself: w divides 128), 1 before
+ * scoring, 2 before the log-sum-exp, 3 before the finalisation (for token-level
+ * chunks in two passes: the second pass and the sum of its partial arrays), 4
+ * before the top-k selection, 5 before the gather, 6 after the gather.  When
+ * one kernel takes the log-sum-exp, the finalisation and the selection (calls
+ * with enough (group, sequence, head) triples to fill the GPU), boundaries 2
+ * and 3 come before it and 4 after it, so its time shows as the
+ * finalisation's.  A record between two launches ends the
  * programmatic-dependent-launch overlap there, so recorded calls run a little
  * slower than unrecorded ones.
  * Returns CHUNKKV_ERR_INVALID_ARG if n_events is neither 0 nor

@@ -155,3 +155,31 @@ def test_tail_pass_over_layers_with_index_reuse(ckv):
                 for layer in range(grp * n_reuse, (grp + 1) * n_reuse):
                     check_gather(out.k_out[layer][b, h, :n], ks[layer][tail, h], got, f"{tag} layer {layer} K'")
                     check_gather(out.v_out[layer][b, h, :n], vs[layer][tail, h], got, f"{tag} layer {layer} V'")
+
+
+def test_tail_pass_records_phase_events(ckv):
+    # the phase events of chunkkv_set_phase_events mark the incremental pass's phases too, and a recorded
+    # pass computes what an unrecorded one does
+    pairs = [(700, 900), (0, 640)]
+    d, G, Hkv, w, c, L = 128, 4, 2, 32, 10, 150
+    cu, q, k, v = _caches(pairs, Hkv, G, d, w, torch.bfloat16, seed=31, needle_len=2 * c)
+    n_prev = [p for p, _ in pairs]
+    kw = dict(Hq=Hkv * G, Hkv=Hkv, w=w, c=c, L_tail=L, return_scores=True)
+    ref = ckv.compress_tail(q, k, v, cu, n_prev, **kw)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(ckv.PHASES) + 1)]
+    ckv.chunkkv_set_phase_events(evs)
+    try:
+        out = ckv.compress_tail(q, k, v, cu, n_prev, **kw)
+    finally:
+        ckv.chunkkv_set_phase_events(None)
+    torch.cuda.synchronize()
+    times = [evs[i].elapsed_time(evs[i + 1]) for i in range(len(ckv.PHASES))]
+    assert all(t >= 0 for t in times) and times[1] > 0 and times[-1] > 0       # scoring and gather ran
+    assert torch.equal(out.counts, ref.counts)
+    for b, (n_p, n_new) in enumerate(pairs):
+        C = -(-n_new // c)                                  # chunk scores past the tail's are not written
+        assert torch.equal(out.chunk_scores[0, b, :, :C], ref.chunk_scores[0, b, :, :C])
+        for h in range(Hkv):
+            n = int(ref.counts[0, b, h])
+            assert torch.equal(out.indices[0, b, h, :n], ref.indices[0, b, h, :n])
+            assert torch.equal(out.k_out[0][b, h, :n], ref.k_out[0][b, h, :n])
