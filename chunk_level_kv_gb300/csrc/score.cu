@@ -218,8 +218,8 @@ finalize_kernel(ScoreGeom g, const __grid_constant__ SeqTable st, const float* _
 
 // Row log-sum-exp (base 2) of every (sequence, head) from the per-unit (R, l)
 // pairs: lse_r = M + log2(sum_u l_u 2^(R_u - M)), M = max_u R_u.  One CTA per
-// (sequence, head, 32 rows): lane = row (128-byte loads), the 32 warps take every
-// 32nd unit, four units per step with their loads issued together, and the
+// (sequence, head, 32 rows): lane = row (128-byte loads), the 8 warps take every
+// 8th unit, four units per step with their loads issued together, and the
 // partial (M, S) pairs are merged through shared memory.
 constexpr int kLseThreads = 256;
 
@@ -266,9 +266,55 @@ lse_kernel(ScoreGeom g, const __grid_constant__ SeqTable st, const float* __rest
   pdl_trigger();
 }
 
+// The same for heads of few units (kLseRowsMaxUnits at most): one thread per
+// (sequence, head, row) merges all of the row's units, four loads in flight, and
+// a CTA covers 128 rows; no warps split the units, since most would be idle.
+constexpr int kLseRowsMaxUnits = 16;
+
+__global__ void __launch_bounds__(128)
+lse_rows_kernel(ScoreGeom g, const __grid_constant__ SeqTable st, const float* __restrict__ rl,
+                float* __restrict__ lse) {
+  const int bh = blockIdx.x;
+  const int b = bh / g.Hkv, h = bh - b * g.Hkv;
+  const int r = blockIdx.y * 128 + threadIdx.x;
+  const int b0 = g.pair ? (b & ~1) : b, b1 = g.pair ? (b | 1) + 1 : b + 1;
+  const int U = st.uoff[b1] - st.uoff[b0];
+  rl += blockIdx.z * g.rl_gs;
+  lse += blockIdx.z * g.lse_gs;
+  pdl_wait();
+  if (r < g.wG) {
+    const int64_t ustride = (int64_t)g.Hkv * 2 * g.wG;
+    const float* base = rl + ((int64_t)st.uoff[b0] * g.Hkv + h) * 2 * g.wG + r;
+    float M = -INFINITY, S = 0.f;
+    int v = 0;
+    for (; v + 3 < U; v += 4) {
+      float Rv[4], lv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        Rv[i] = base[(v + i) * ustride];
+        lv[i] = base[(v + i) * ustride + g.wG];
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) lse_merge(M, S, Rv[i], lv[i]);
+    }
+    for (; v < U; ++v) lse_merge(M, S, base[v * ustride], base[v * ustride + g.wG]);
+    lse[(int64_t)bh * g.wG + r] = M + log2f(S);
+  }
+  pdl_trigger();
+}
+
 cudaError_t launch_lse(const ScoreGeom& g, const SeqTable& st, const float* rl, float* lse, int n_groups,
                        cudaStream_t s) {
   if (g.n_units == 0 || g.wG == 0 || n_groups == 0) return cudaSuccess;
+  int u_max = 0;                                  // units of the longest (paired) sequence, per head
+  for (int b = 0; b < st.B; b += g.pair ? 2 : 1) {
+    const int b1 = g.pair ? std::min(b + 2, st.B) : b + 1;
+    u_max = std::max(u_max, st.uoff[b1] - st.uoff[b]);
+  }
+  if (u_max <= kLseRowsMaxUnits) {
+    dim3 grid(st.B * g.Hkv, (g.wG + 127) / 128, n_groups);
+    return launch_pdl(lse_rows_kernel, grid, dim3(128), 0, s, g, st, rl, lse);
+  }
   dim3 grid(st.B * g.Hkv, (g.wG + 31) / 32, n_groups);
   return launch_pdl(lse_kernel, grid, dim3(kLseThreads), 0, s, g, st, rl, lse);
 }
