@@ -116,6 +116,7 @@ def test_tiny_fp32_exact(ckv):
     (3000, 1, 32, 28, 4, 256),       # token-level selection on 224 window rows (two M tiles)
     (3001, 1, 64, 28, 4, 700),       # token-level, two passes on 448 window rows (last M tile half padding)
     (2600, 1, 32, 32, 8, 400),       # token-level, two passes on 128 window rows
+    (2100, 1, 24, 28, 4, 300),       # token-level, two passes on packed window rows (w = 24), 168 rows
 ])
 def test_bf16_shapes(ckv, T, c, w, Hq, Hkv, L_max):
     wl = configs.llama_layer().with_params(seqlens=(T,), c=c, w=w, Hq=Hq, Hkv=Hkv, L_max=L_max,
