@@ -666,6 +666,22 @@ def run_tail(args):
     for _ in range(args.warmup):
         step()
     ckv.chunkkv_status_check(ws)
+    timed = step
+    if args.graph:
+        # the pass captured once in a CUDA graph and replayed: no host work between passes (a decode
+        # loop with fixed cache sizes can do the same)
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step()
+        stream.wait_stream(side)
+        n0 = ckv.chunkkv_launch_count()
+        with torch.cuda.graph(graph):
+            step()
+        per_replay = ckv.chunkkv_launch_count() - n0                 # kernels each replay launches
+        torch.cuda.synchronize()
+        timed = graph.replay
     in_bytes = sum(x.numel() * x.element_size() for x in ks + vs)
     l2_note = "inputs larger than L2 (no flush)" if in_bytes > 2 * 129e6 else "L2 flushed between steps"
     flush = torch.empty(int(2 * 129e6) // 4, dtype=torch.float32, device=dev) if in_bytes <= 2 * 129e6 else None
@@ -677,16 +693,20 @@ def run_tail(args):
     time.sleep(0.3)
     launches0 = ckv.chunkkv_launch_count()
     times = []
+    t_host = time.perf_counter()
     for _ in range(args.steps):
         if flush is not None:
             flush.fill_(1.0)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        step()
+        timed()
         e1.record(stream)
         times.append((e0, e1))
+    t_host = (time.perf_counter() - t_host) / args.steps * 1e3           # host time to issue one pass
     torch.cuda.synchronize()
     launches = ckv.chunkkv_launch_count() - launches0
+    if args.graph:
+        launches = per_replay * args.steps        # replays bypass the library's host-side launch count
     if ws_n > 1:
         torch.distributed.barrier()
     clocks = sampler.stop()
@@ -720,6 +740,7 @@ def run_tail(args):
                    "d": wl.d, "w": wl.w, "c": wl.c, "L_tail": L_tail, "l2": l2_note,
                    "parallelism": f"replicas x{ws_n}"},
         "tail_tokens_per_s": round(job_rate(n_new * wl.B, ws_n, step_ms), 1),
+        "cuda_graph": bool(args.graph), "host_ms_per_pass": round(t_host, 4),
         "phases_ms": {k: round(v, 5) for k, v in phase_ms.items()},
         "algorithmic_bytes_per_step": nbytes,
         "hbm_roof_frac": round(value / ws_n / hbm, 4),
@@ -870,6 +891,7 @@ def main():
     ap.add_argument("--causal", action="store_true", help="causal window (chunkkv_params.causal_window)")
     ap.add_argument("--tail", type=int, default=0,
                     help="time the incremental pass during decoding with this many new tokens per cache instead")
+    ap.add_argument("--graph", action="store_true", help="with --tail: replay the pass from a CUDA graph")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-baseline-child", action="store_true", help=argparse.SUPPRESS)

@@ -183,3 +183,36 @@ def test_tail_pass_records_phase_events(ckv):
             n = int(ref.counts[0, b, h])
             assert torch.equal(out.indices[0, b, h, :n], ref.indices[0, b, h, :n])
             assert torch.equal(out.k_out[0][b, h, :n], ref.k_out[0][b, h, :n])
+
+
+def test_tail_pass_replays_from_a_cuda_graph(ckv):
+    # every step of the pass is a stream-ordered launch, so a decode loop can capture it once and replay
+    # it; the replayed pass (its claim counter reset by each launch) computes what the eager one does
+    pairs = [(700, 900), (0, 640), (1200, 75)]
+    d, G, Hkv, w, c, L = 128, 4, 2, 32, 10, 150
+    cu, q, k, v = _caches(pairs, Hkv, G, d, w, torch.bfloat16, seed=41, needle_len=2 * c)
+    n_prev = [p for p, _ in pairs]
+    kw = dict(Hq=Hkv * G, Hkv=Hkv, w=w, c=c, L_tail=L, return_scores=True)
+    ref = ckv.compress_tail(q, k, v, cu, n_prev, **kw)
+    out = ckv.compress_tail(q, k, v, cu, n_prev, **kw)              # warm-up; outputs and workspace reused
+    p, keep = ckv.params_for(q, k, cu, Hkv=Hkv, w=w, c=c, L_max=L)
+    for x in (out.indices, out.counts, out.chunk_scores, *out.k_out, *out.v_out):
+        x.fill_(-1)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        ckv.chunkkv_compress_tail(p, n_prev, 1, [q], [k], [v], out.k_out, out.v_out, out.indices, out.counts,
+                                  out.chunk_scores, out.workspace)
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert ckv.chunkkv_status_check(out.workspace) == 0
+    assert torch.equal(out.counts, ref.counts)
+    for b, (n_p, n_new) in enumerate(pairs):
+        C = -(-n_new // c)
+        assert torch.equal(out.chunk_scores[0, b, :, :C], ref.chunk_scores[0, b, :, :C])
+        for h in range(Hkv):
+            n = int(ref.counts[0, b, h])
+            assert torch.equal(out.indices[0, b, h, :n], ref.indices[0, b, h, :n])
+            assert torch.equal(out.k_out[0][b, h, :n], ref.k_out[0][b, h, :n])
+            assert torch.equal(out.v_out[0][b, h, :n], ref.v_out[0][b, h, :n])
+    del keep
