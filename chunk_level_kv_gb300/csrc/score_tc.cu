@@ -13,15 +13,12 @@
 //   - computes S = Q K^T (128 x 80, fp32) with tcgen05.mma (A and B in shared
 //     memory) into one of three TMEM accumulator stages,
 //   - lets each of 128 softmax threads own one window row: it reads its row of
-//     S from TMEM (16 columns at a time, the next 16 in flight), forms
-//     2^(s*log2(e)/sqrt(d) - R) with R the row maximum of the item's first
-//     tile, and sums those per chunk (chunk boundaries are compile
+//     S from TMEM (16 columns at a time, the next 16 in flight), forms 2^(s*log2(e)/sqrt(d) - R) with R the row maximum of the
+//     item's first tile, and sums those per chunk (chunk boundaries are compile
 //     time constants for each of the C / gcd(80, C) tile phases), writing one
 //     16-bit bin per (chunk, row) and the row's (R, sum) at the end of the item.
 // A row whose values would outgrow the first-tile reference by more than 2^23
-// switches to the new maximum and rescales what it already wrote.  Token-level
-// chunks (c = 1) run the kernel twice instead (MODE 1: the (R, sum) pairs only;
-// MODE 2: each key's probability summed over the rows, given the rows' lse).
+// switches to the new maximum and rescales what it already wrote.
 //
 // Warp roles (192 threads): warp 0 = TMA producer, warp 1 = TMEM owner and MMA
 // issuer, warps 2-5 = softmax (warp w reads TMEM lanes 32*(w%4) .. +31).  Two
